@@ -1,0 +1,403 @@
+/*
+ * sdv_oracle.c -- plain fp64 CPU oracle of the batched lossless
+ * draft-verification step with test-time self-selection.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg; never by the product path.  It shares no code
+ * with the CUDA library.  Every step is written in the order the method states
+ * it, with no blocking, fusion or reordering; the only parallelism is over
+ * independent sequences.  See sdv_oracle.h for the passages followed.
+ */
+#include "sdv_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10 (Salmon et al., SC'11).  Pinned by the published            */
+/* known-answer vectors and by cuRAND's Philox4_32_10 generator.            */
+/* ------------------------------------------------------------------------ */
+
+/* Multipliers and Weyl key increments of Philox4x32 as published. */
+#define PHILOX_MUL0 0xD2511F53u
+#define PHILOX_MUL1 0xCD9E8D57u
+#define PHILOX_WEYL0 0x9E3779B9u
+#define PHILOX_WEYL1 0xBB67AE85u
+
+void sdvo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += PHILOX_WEYL0;
+            k1 += PHILOX_WEYL1;
+        }
+        /* One round: two 32x32->64 products; the high halves are mixed with
+         * the other two words and the key, the low halves pass through. */
+        uint64_t prod0 = (uint64_t)PHILOX_MUL0 * (uint64_t)x0;
+        uint64_t prod1 = (uint64_t)PHILOX_MUL1 * (uint64_t)x2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t y0 = hi1 ^ x1 ^ k0;
+        uint32_t y1 = lo1;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+double sdvo_uniform24(uint32_t word)
+{
+    return (double)(word >> 8) * (1.0 / 16777216.0);
+}
+
+void sdvo_uniforms(uint64_t seed, uint32_t b, uint32_t j, double* u, double* w)
+{
+    uint32_t ctr[4] = {j, b, 0u, 0u};
+    uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    sdvo_philox4x32_10(ctr, key, out);
+    if (u) *u = sdvo_uniform24(out[0]);
+    if (w) *w = sdvo_uniform24(out[1]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Temperature softmax of one row.  Pinned by closed forms (uniform rows,    */
+/* two-element rows, shifts) and by scipy's logsumexp.                      */
+/* ------------------------------------------------------------------------ */
+
+double sdvo_logit(const void* row, int dtype, int64_t index)
+{
+    if (dtype == SDVO_BF16) {
+        /* bf16 is the top half of an IEEE binary32: widen exactly. */
+        uint16_t h = ((const uint16_t*)row)[index];
+        uint32_t bits = (uint32_t)h << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float*)row)[index];
+}
+
+double sdvo_row_lse(const void* row, int dtype, int64_t V, double T)
+{
+    /* Pass 1: the maximum of z_v = l_v / T (and a scan for NaN / +inf). */
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        double z = sdvo_logit(row, dtype, v) / T;
+        if (isnan(z) || z == INFINITY) return NAN;
+        if (z > m) m = z;
+    }
+    if (m == -INFINITY) return -INFINITY;
+    /* Pass 2: LSE = m + log sum_v exp(z_v - m). */
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        double z = sdvo_logit(row, dtype, v) / T;
+        s += exp(z - m);
+    }
+    return m + log(s);
+}
+
+double sdvo_logprob(const void* row, int dtype, int64_t x, double T, double lse)
+{
+    return sdvo_logit(row, dtype, x) / T - lse;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Acceptance rule, streak score, self-selection.  Pinned by the closed form */
+/* E_{x~q}[min(1,p/q)] = sum_v min(p_v,q_v), by exact enumeration of the    */
+/* committed-token law (K = 1 equals p; the K = 2 counter-example law), by  */
+/* Monte Carlo of E[L] = S, and by the q == p invariant.                    */
+/* ------------------------------------------------------------------------ */
+
+double sdvo_accept_ratio(double lp, double lq)
+{
+    if (lq == -INFINITY) return 1.0;       /* q(x) = 0 <= p(x): accept        */
+    if (lp == -INFINITY) return 0.0;       /* p(x) = 0 < q(x): never accept   */
+    if (lq <= lp) return 1.0;              /* q(x) <= p(x): accept at once     */
+    return exp(lp - lq);                   /* else accept with prob p/q        */
+}
+
+double sdvo_streak_score(const double* a, int gamma)
+{
+    double score = 0.0, prefix = 1.0;
+    for (int j = 0; j < gamma; ++j) {
+        prefix *= a[j];
+        score += prefix;
+    }
+    return score;
+}
+
+int sdvo_argmax_first(const double* s, int K)
+{
+    int best = 0;
+    for (int k = 1; k < K; ++k)
+        if (s[k] > s[best]) best = k;
+    return best;
+}
+
+int sdvo_accept_length(const double* a, const double* u, int gamma)
+{
+    for (int j = 0; j < gamma; ++j) {
+        int accepted = (a[j] >= 1.0) || (u[j] < a[j]);
+        if (!accepted) return j;
+    }
+    return gamma;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Inverse-CDF draw.  Pinned by exact interval integration over w on tiny    */
+/* rows and by the rule that zero-weight ids are never drawn.               */
+/* ------------------------------------------------------------------------ */
+
+int64_t sdvo_inverse_cdf(const double* r, int64_t V, double w, double* R_out,
+                         double* t_out, double* c_prev_out, double* c_v_out)
+{
+    double R = 0.0;
+    for (int64_t v = 0; v < V; ++v) R += r[v];
+    if (R_out) *R_out = R;
+    if (!(R > 0.0)) return -1;
+    double t = w * R;
+    if (t_out) *t_out = t;
+    double c = 0.0, c_prev = 0.0;
+    int64_t last_pos = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        c_prev = c;
+        c += r[v];
+        if (r[v] > 0.0) last_pos = v;
+        if (c > t) {
+            if (c_prev_out) *c_prev_out = c_prev;
+            if (c_v_out) *c_v_out = c;
+            return v;
+        }
+    }
+    /* Rounding left t at or above the total: the last id with mass. */
+    if (c_prev_out) *c_prev_out = c;
+    if (c_v_out) *c_v_out = c;
+    return last_pos;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The full step for one sequence.                                          */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int K, gamma, dtype;
+    int64_t V;
+} shape_t;
+
+static const void* p_row(const void* base, const shape_t* sh, int b, int k, int j)
+{
+    size_t elt = sh->dtype == SDVO_BF16 ? 2 : 4;
+    int64_t idx = (((int64_t)b * sh->K + k) * (sh->gamma + 1) + j) * sh->V;
+    return (const char*)base + (size_t)idx * elt;
+}
+
+static const void* q_row(const void* base, const shape_t* sh, int b, int k, int j)
+{
+    size_t elt = sh->dtype == SDVO_BF16 ? 2 : 4;
+    int64_t idx = (((int64_t)b * sh->K + k) * sh->gamma + j) * sh->V;
+    return (const char*)base + (size_t)idx * elt;
+}
+
+static int verify_one(const shape_t* sh, int b, const void* p_logits,
+                      const void* q_logits, const int32_t* drafts, double T,
+                      const double* u, const double* w, int32_t* sel_out,
+                      int32_t* len_out, int32_t* tok_out, double* lse_out,
+                      double* scores_out, double* ratio_out, int32_t* band_out,
+                      double* resid_out)
+{
+    const int K = sh->K, G = sh->gamma, dtype = sh->dtype;
+    const int64_t V = sh->V;
+    const int nrow = 2 * G + 1;
+    int err = 0;
+    *sel_out = -1; *len_out = -1; *tok_out = -1;
+    if (band_out) *band_out = 0;
+    if (resid_out) *resid_out = NAN;
+
+    if (!(T > 0.0) || isinf(T)) err |= SDVO_BAD_TEMP;
+    for (int k = 0; k < K && !err; ++k)
+        for (int j = 0; j < G; ++j) {
+            int32_t x = drafts[((int64_t)b * K + k) * G + j];
+            if (x < 0 || (int64_t)x >= V) err |= SDVO_BAD_DRAFT;
+        }
+    if (err) return err;
+
+    double* lse = (double*)malloc(sizeof(double) * (size_t)K * nrow);
+    double* a = (double*)malloc(sizeof(double) * (size_t)K * (G > 0 ? G : 1));
+    double* S = (double*)malloc(sizeof(double) * (size_t)K);
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!lse || !a || !S || !r) { free(lse); free(a); free(S); free(r); return -1; }
+
+    /* Temperature softmax of every p row (j = 0..G) and q row (j < G). */
+    for (int k = 0; k < K; ++k) {
+        for (int j = 0; j <= G; ++j)
+            lse[k * nrow + j] = sdvo_row_lse(p_row(p_logits, sh, b, k, j), dtype, V, T);
+        for (int j = 0; j < G; ++j)
+            lse[k * nrow + G + 1 + j] = sdvo_row_lse(q_row(q_logits, sh, b, k, j), dtype, V, T);
+    }
+    for (int i = 0; i < K * nrow; ++i)
+        if (!isfinite(lse[i])) err |= SDVO_BAD_ROW;
+    if (lse_out) memcpy(lse_out, lse, sizeof(double) * (size_t)K * nrow);
+    if (err) goto done;
+
+    /* Ratios a = min(1, p(x)/q(x)) at every drafted token, then the expected
+     * accepted streak of every draft. */
+    for (int k = 0; k < K; ++k) {
+        for (int j = 0; j < G; ++j) {
+            int32_t x = drafts[((int64_t)b * K + k) * G + j];
+            double lp = sdvo_logprob(p_row(p_logits, sh, b, k, j), dtype, x, T, lse[k * nrow + j]);
+            double lq = sdvo_logprob(q_row(q_logits, sh, b, k, j), dtype, x, T, lse[k * nrow + G + 1 + j]);
+            a[k * G + j] = sdvo_accept_ratio(lp, lq);
+        }
+        S[k] = sdvo_streak_score(a + (size_t)k * G, G);
+    }
+    if (scores_out) memcpy(scores_out, S, sizeof(double) * (size_t)K);
+    if (ratio_out && G > 0) memcpy(ratio_out, a, sizeof(double) * (size_t)K * G);
+
+    /* Self-selection: the draft with the largest expected streak. */
+    int sel = sdvo_argmax_first(S, K);
+    int band = 0;
+    {
+        double second = -INFINITY;
+        for (int k = 0; k < K; ++k)
+            if (k != sel && S[k] > second) second = S[k];
+        double gap = S[sel] - second;
+        if (K > 1 && gap > 0.0 && gap <= 1e-5 * S[sel]) band |= SDVO_BAND_SELECT;
+    }
+
+    /* Left-to-right acceptance of the selected draft. */
+    const double* as = a + (size_t)sel * G;
+    int L = sdvo_accept_length(as, u, G);
+    for (int j = 0; j < G && j <= L; ++j)
+        if (fabs(u[j] - as[j]) <= 1e-5 * as[j]) band |= SDVO_BAND_ACCEPT;
+
+    /* Replacement at the first rejection (residual max(0, p - q)), or the
+     * bonus token from p at position G when every draft token was accepted. */
+    int64_t tok;
+    double R = 0.0, t = 0.0, c_prev = 0.0, c_v = 0.0;
+    const void* prow = p_row(p_logits, sh, b, sel, L);
+    double lse_p = lse[sel * nrow + L];
+    if (L < G) {
+        const void* qrow = q_row(q_logits, sh, b, sel, L);
+        double lse_q = lse[sel * nrow + G + 1 + L];
+        for (int64_t v = 0; v < V; ++v) {
+            double pv = exp(sdvo_logit(prow, dtype, v) / T - lse_p);
+            double qv = exp(sdvo_logit(qrow, dtype, v) / T - lse_q);
+            double d = pv - qv;
+            r[v] = d > 0.0 ? d : 0.0;
+        }
+        tok = sdvo_inverse_cdf(r, V, w[L], &R, &t, &c_prev, &c_v);
+        if (resid_out) *resid_out = R;
+        if (R < 1e-3) band |= SDVO_BAND_RESID;
+        if (tok < 0) {
+            /* Zero residual mass (p == q on this row up to rounding): draw
+             * from p instead. */
+            for (int64_t v = 0; v < V; ++v)
+                r[v] = exp(sdvo_logit(prow, dtype, v) / T - lse_p);
+            tok = sdvo_inverse_cdf(r, V, w[L], &R, &t, &c_prev, &c_v);
+        }
+    } else {
+        for (int64_t v = 0; v < V; ++v)
+            r[v] = exp(sdvo_logit(prow, dtype, v) / T - lse_p);
+        tok = sdvo_inverse_cdf(r, V, w[G], &R, &t, &c_prev, &c_v);
+    }
+    if (fabs(t - c_v) <= 1e-5 * R || fabs(t - c_prev) <= 1e-5 * R) band |= SDVO_BAND_CDF;
+
+    *sel_out = sel;
+    *len_out = L;
+    *tok_out = (int32_t)tok;
+    if (band_out) *band_out = band;
+
+done:
+    free(lse); free(a); free(S); free(r);
+    return err;
+}
+
+static int run_batch(int B, int K, int gamma, int64_t V, int dtype,
+                     const void* p_logits, const void* q_logits,
+                     const int32_t* drafts, const double* temps,
+                     const double* u_in, const double* w_in, int use_philox,
+                     uint64_t seed, int32_t b0,
+                     int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                     double* lse, double* scores, double* ratio,
+                     int32_t* band, int32_t* err, double* resid_mass, int nthreads)
+{
+    shape_t sh = {K, gamma, dtype, V};
+    int any = 0;
+    if (B < 0 || K < 1 || gamma < 0 || V < 1 || (dtype != SDVO_BF16 && dtype != SDVO_F32))
+        return -1;
+    const int nrow = 2 * gamma + 1;
+#ifdef _OPENMP
+    int nt = nthreads > 1 ? nthreads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1) reduction(| : any)
+#endif
+    for (int b = 0; b < B; ++b) {
+        double* u = (double*)malloc(sizeof(double) * (size_t)(gamma + 1));
+        double* w = (double*)malloc(sizeof(double) * (size_t)(gamma + 1));
+        if (!u || !w) { free(u); free(w); any |= -1; continue; }
+        for (int j = 0; j <= gamma; ++j) {
+            if (use_philox) {
+                sdvo_uniforms(seed, (uint32_t)(b0 + b), (uint32_t)j, &u[j], &w[j]);
+            } else {
+                u[j] = j < gamma ? u_in[(int64_t)b * gamma + j] : 0.0;
+                w[j] = w_in[(int64_t)b * (gamma + 1) + j];
+            }
+        }
+        int e = verify_one(&sh, b, p_logits, q_logits, drafts, temps[b], u, w,
+                           &sel[b], &accept_len[b], &next_token[b],
+                           lse ? lse + (int64_t)b * K * nrow : NULL,
+                           scores ? scores + (int64_t)b * K : NULL,
+                           ratio ? ratio + (int64_t)b * K * gamma : NULL,
+                           band ? band + b : NULL,
+                           resid_mass ? resid_mass + b : NULL);
+        if (err) err[b] = e;
+        any |= e;
+        free(u); free(w);
+    }
+    (void)nthreads;
+    return any;
+}
+
+int sdvo_verify_uniforms(int B, int K, int gamma, int64_t V, int dtype,
+                         const void* p_logits, const void* q_logits,
+                         const int32_t* drafts, const double* temps,
+                         const double* u, const double* w,
+                         int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                         double* lse, double* scores, double* ratio,
+                         int32_t* band, int32_t* err, double* resid_mass,
+                         int nthreads)
+{
+    return run_batch(B, K, gamma, V, dtype, p_logits, q_logits, drafts, temps, u, w, 0, 0, 0,
+                     sel, accept_len, next_token, lse, scores, ratio, band, err, resid_mass,
+                     nthreads);
+}
+
+int sdvo_verify(int B, int K, int gamma, int64_t V, int dtype,
+                const void* p_logits, const void* q_logits,
+                const int32_t* drafts, const double* temps, uint64_t seed,
+                int32_t b0,
+                int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                double* lse, double* scores, double* ratio,
+                int32_t* band, int32_t* err, double* resid_mass,
+                int nthreads)
+{
+    return run_batch(B, K, gamma, V, dtype, p_logits, q_logits, drafts, temps, NULL, NULL, 1,
+                     seed, b0, sel, accept_len, next_token, lse, scores, ratio, band, err,
+                     resid_mass, nthreads);
+}
+
+int sdvo_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

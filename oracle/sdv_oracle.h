@@ -1,0 +1,138 @@
+/*
+ * sdv_oracle.h -- plain, slow, fp64 CPU oracle of the batched lossless
+ * draft-verification step with test-time self-selection.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library exists to check the CUDA path.
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * may load it.  It shares no code, header, table or constant with the CUDA
+ * library, and it includes nothing from it.
+ *
+ * Passages followed (page title, section):
+ *   - "SpecDiff-2: Scaling Diffusion Drafter Alignment For Faster Speculative
+ *     Decoding" (paperlayer summary), section 2 "Prelim: speculative
+ *     decoding": left-to-right commit with the standard lossless acceptance
+ *     rule, immediate acceptance when q(x|s) <= p(x|s), a replacement token
+ *     from the normalised residual at the first rejection.
+ *   - same page, Figure 2 and section 3: position-wise acceptance alpha_j and
+ *     the accepted streak.
+ *   - same page, section 5.2 "Test-time alignment: self-selection
+ *     acceptance": K joint drafts ranked by a streak-oriented verifier score,
+ *     the best is verified losslessly, verifier probabilities are reused.
+ *   - "DiffuSpec: Unlocking Diffusion Language Models for Speculative
+ *     Decoding" (paperlayer summary), section 3: residual replacement,
+ *     unbiasedness.
+ * The score formula sum_j prod_{i<=j} min(1, p/q), the Philox keying, the
+ * bonus token and the argument layout are a reading of the method: the pages
+ * state these quantities only in prose.
+ *
+ * Parity status of each function is stated next to it; every function here
+ * is pinned by a test that does not re-derive the function itself.
+ */
+#ifndef SDV_ORACLE_H
+#define SDV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDVO_BF16 0
+#define SDVO_F32 1
+
+/* Boundary-band flags (one word per sequence).  A trial whose flag is set may
+ * be decided differently by a correct fp32 implementation. */
+#define SDVO_BAND_ACCEPT 1   /* |u_j - a_j| <= 1e-5 a_j at a decided position  */
+#define SDVO_BAND_CDF 2      /* |t - C_v| <= 1e-5 R at the chosen v or v-1      */
+#define SDVO_BAND_SELECT 4   /* 0 < S_best - S_second <= 1e-5 S_best            */
+#define SDVO_BAND_RESID 8    /* residual mass R < 1e-3 (ill-conditioned draw)   */
+
+/* Status codes of sdvo_verify / sdvo_verify_uniforms (per sequence in err[]). */
+#define SDVO_OK 0
+#define SDVO_BAD_DRAFT 1     /* draft id outside [0, V)                          */
+#define SDVO_BAD_ROW 2       /* a row holds NaN/+inf or is all -inf              */
+#define SDVO_BAD_TEMP 4      /* temperature not finite or <= 0                   */
+
+/* Philox4x32-10 block function (Salmon, Moraes, Dror, Shaw, "Parallel random
+ * numbers: as easy as 1, 2, 3", SC'11): 10 rounds of the 4x32 Philox
+ * S-box, key bumped by the Weyl constants between rounds. */
+void sdvo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* 24-bit uniform in [0, 1 - 2^-24]: (word >> 8) * 2^-24. */
+double sdvo_uniform24(uint32_t word);
+
+/* Uniforms for sequence b, position j: counter (j, b, 0, 0), key (seed low
+ * word, seed high word).  Word 0 -> acceptance uniform u, word 1 -> sampling
+ * uniform w. */
+void sdvo_uniforms(uint64_t seed, uint32_t b, uint32_t j, double* u, double* w);
+
+/* Decode logit `index` of a row stored as bf16 (raw 16-bit words) or fp32. */
+double sdvo_logit(const void* row, int dtype, int64_t index);
+
+/* Log-sum-exp of z_v = l_v / T over one row, two passes (max, then sum of
+ * exp(z - max)).  Returns NaN if the row holds NaN or +inf, -inf if every
+ * entry is -inf. */
+double sdvo_row_lse(const void* row, int dtype, int64_t V, double T);
+
+/* log-probability log p(x) = l_x / T - LSE. */
+double sdvo_logprob(const void* row, int dtype, int64_t x, double T, double lse);
+
+/* Acceptance ratio a = min(1, p(x)/q(x)) from log-probabilities.  q(x) = 0
+ * (lq = -inf) counts as q <= p, so a = 1; p(x) = 0 < q(x) gives a = 0. */
+double sdvo_accept_ratio(double lp, double lq);
+
+/* Expected accepted streak S = sum_{j<gamma} prod_{i<=j} a_i. */
+double sdvo_streak_score(const double* a, int gamma);
+
+/* Index of the first maximum of s[0..K). */
+int sdvo_argmax_first(const double* s, int K);
+
+/* Accepted length: the first j with not(a_j >= 1 or u_j < a_j), else gamma. */
+int sdvo_accept_length(const double* a, const double* u, int gamma);
+
+/* Inverse CDF over non-negative weights r[0..V): R = sum r (increasing id
+ * order), t = w R, returns the first v with C_v = sum_{i<=v} r_i > t.  If no v
+ * qualifies (rounding), the last v with r_v > 0.  Returns -1 if R == 0.
+ * Optional outputs: *R_out, *t_out, *c_prev_out (C_{v-1}), *c_v_out (C_v). */
+int64_t sdvo_inverse_cdf(const double* r, int64_t V, double w, double* R_out,
+                         double* t_out, double* c_prev_out, double* c_v_out);
+
+/* Full step for a batch with explicit uniforms u[B][gamma] and
+ * w[B][gamma+1] (random numbers passed in as inputs).
+ *   p_logits [B][K][gamma+1][V], q_logits [B][K][gamma][V] (dtype), drafts
+ *   [B][K][gamma] int32, temps [B] (> 0).
+ *   Outputs (each may be NULL except sel/accept_len/next_token):
+ *   sel[B], accept_len[B], next_token[B]   (-1 for a sequence with err != 0)
+ *   lse[B][K][2 gamma + 1]: p rows j=0..gamma, then q rows j=0..gamma-1
+ *   scores[B][K], ratio[B][K][gamma], band[B], err[B], resid_mass[B].
+ * Returns the OR of all err[] words.  nthreads > 1 runs sequences in
+ * parallel (independent problems); 0 or 1 runs serially. */
+int sdvo_verify_uniforms(int B, int K, int gamma, int64_t V, int dtype,
+                         const void* p_logits, const void* q_logits,
+                         const int32_t* drafts, const double* temps,
+                         const double* u, const double* w,
+                         int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                         double* lse, double* scores, double* ratio,
+                         int32_t* band, int32_t* err, double* resid_mass,
+                         int nthreads);
+
+/* Same, with the Philox uniforms of sdvo_uniforms(seed, b0 + b, j); b0 is the
+ * index of the first sequence of this batch within the full call, so a
+ * sample of sequences can be checked on its own. */
+int sdvo_verify(int B, int K, int gamma, int64_t V, int dtype,
+                const void* p_logits, const void* q_logits,
+                const int32_t* drafts, const double* temps, uint64_t seed,
+                int32_t b0,
+                int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                double* lse, double* scores, double* ratio,
+                int32_t* band, int32_t* err, double* resid_mass,
+                int nthreads);
+
+/* Number of threads the build can run (1 without OpenMP). */
+int sdvo_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
