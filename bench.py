@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Throughput of batched lossless draft verification with self-selection.
+
+One step = one call of the whole path (row softmax statistics, ratios,
+expected streaks, self-selection, acceptance scan, residual / bonus draw)
+over one batch of the large-window workload: B = 32 sequences, K = 16
+drafts, gamma = 32, V = 152064 (Qwen2.5 vocabulary), bf16 logits, drafter
+noise rising from 0.3 to 2.0 across the window, per-sequence temperatures in
+{0.6, 1.0}.  Inputs are synthetic, seeded, resident in HBM (10.1 GB, far
+larger than the 126 MB L2, so no flush is needed between steps).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sdv|reference]
+
+N > 1 runs under torchrun, one rank per GPU, each rank verifying its own batch
+(sequences are independent: weak scaling, no collective on the data path).
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from draft_verification_sdv_gb300 import synth  # noqa: E402
+
+METRIC = "verified draft-tokens/s and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+UNIT = "draft-tokens/s"
+DEFAULT_WORKLOAD = 5
+ROWPASS_SOURCES = ["k1_rowpass.cu", "sdv_device.cuh", "sdv_plan.h"]
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "rowpass_large-window.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["sdv", "reference"], default="sdv")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device: int):
+        self.samples = []
+        self.proc = None
+        gid = None
+        try:
+            gid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            gid = vis.split(",")[device] if vis else str(device)
+        self.gid = gid
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "100", "-i", self.gid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.samples:
+            if t0 - 0.15 <= ts <= t1 + 0.15:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = sorted({self.NAMES[i] for r in rows for i in range(4)
+                          if r[2 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def rowpass_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ROWPASS_SOURCES:
+        with open(os.path.join(ROOT, "draft_verification_sdv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_per_row():
+    """DRAM bytes per logit row of the row-pass kernel from the committed ncu
+    summary, or None when that summary is absent or predates the kernel."""
+    try:
+        kv = {}
+        with open(TRAFFIC_PROFILE) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith(("kernel_source_sha256", "dram_bytes_per_row")):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip().strip("`")
+        if kv.get("kernel_source_sha256") != rowpass_source_sha():
+            return None
+        return float(kv["dram_bytes_per_row"])
+    except Exception:
+        return None
+
+
+def step_bytes(w: synth.Workload, accept_len) -> dict:
+    """Algorithmic bytes of one step: every logit row once, the re-read rows
+    of the draw (two for a residual, one for a bonus), drafts, outputs."""
+    elt = 2 if w.dtype == torch.bfloat16 else 4
+    rows = w.B * w.K * (2 * w.gamma + 1)
+    reread = sum(2 if int(L) < w.gamma else 1 for L in accept_len)
+    k1 = elt * w.V * rows
+    total = k1 + elt * w.V * reread + w.B * w.K * w.gamma * 4 + w.B * 12
+    return {"rows": rows, "k1": k1, "total": total, "reread_rows": reread}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def run_sdv(args, rank, world, local):
+    from draft_verification_sdv_gb300 import binding as bd
+    bd.load(build=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = synth.workload(args.workload, device=dev, seed=args.workload + 1000 * rank)
+    stream = torch.cuda.Stream(device=dev)
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream)
+    out = None
+
+    def step():
+        nonlocal out
+        out = v(w.p_logits, w.q_logits, w.drafts, temperature=w.temperature, seed=w.seed,
+                temps=w.temps, out=out)
+
+    for _ in range(max(args.warmup, 3) if args.warmup > 0 else 0):
+        step()
+    v.sync()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.25)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bd.sdv_profile_enable(v.ctx, True)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    bd.sdv_profile_enable(v.ctx, False)
+    time.sleep(0.2)
+    clocks.stop()
+    v.sync()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_kernels, nprof = bd.sdv_profile_read(v.ctx)
+    ms_max = max_over_ranks(ms_total, world)
+    accept_len = out["accept_len"].cpu().tolist()
+    tokens_per_step = w.B * w.K * w.gamma
+    value = world * tokens_per_step * args.steps / (ms_max / 1e3)
+    ms_step = ms_max / args.steps
+    sb = step_bytes(w, accept_len)
+    peak, peak_kind = measured_peaks()
+    k1_gbs = sb["k1"] / (ms_kernels[0] * 1e-3) / 1e9 if ms_kernels[0] > 0 else None
+    step_gbs = sb["total"] / (ms_step * 1e-3) / 1e9
+    tpr = traffic_per_row()
+    roofline = {
+        "bound": "hbm",
+        "kernel": "rowpass_kernel (online softmax statistics of every logit row)",
+        "achieved": round(k1_gbs, 1) if k1_gbs else None,
+        "peak": peak,
+        "peak_kind": peak_kind,
+        "unit": "GB/s",
+        "frac": round(k1_gbs / peak, 4) if k1_gbs else None,
+        "traffic": round(tpr * sb["rows"]) if tpr else None,
+        "algorithmic_bytes_per_launch": sb["k1"],
+        "ms_per_launch": round(ms_kernels[0], 5),
+    }
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "input_dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded logits and drafts; no model weights)",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "gamma": w.gamma, "V": w.V,
+                   "temperatures": "per-sequence {0.6, 1.0}" if w.temps is not None else w.temperature,
+                   "l2": "inputs %.2f GB > L2 (126 MB): no flush" % (sb["k1"] / 1e9),
+                   "parallelism": "replicas (one batch per GPU)" if world > 1 else "1 GPU"},
+        "hbm": {"step_gbs": round(step_gbs, 1), "frac": round(step_gbs / peak, 4),
+                "bytes_per_step": sb["total"], "reread_rows": sb["reread_rows"]},
+        "kernel_ms": {"rowpass": ms_kernels[0], "select": ms_kernels[1], "sample": ms_kernels[2],
+                      "steps": nprof},
+        "roofline": roofline,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(t0, t1),
+    }
+
+    # End to end through the host-buffer entry point: inputs copied from pinned
+    # host memory each step, outputs read back.
+    if not args.no_e2e:
+        hp = torch.empty(w.p_logits.shape, dtype=w.dtype, pin_memory=True)
+        hq = torch.empty(w.q_logits.shape, dtype=w.dtype, pin_memory=True)
+        hp.copy_(w.p_logits)
+        hq.copy_(w.q_logits)
+        hd = w.drafts.cpu().pin_memory()
+        ht = w.temps.cpu().pin_memory() if w.temps is not None else None
+        outs = [torch.empty(w.B, dtype=torch.int32).pin_memory() for _ in range(3)]
+        st = bd.sdv_verify_host(v.ctx, hp, hq, hd, w.temperature, ht, w.seed, *outs)
+        assert st == bd.SDV_OK, bd.sdv_last_error(v.ctx)
+        barrier(world)
+        te0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            st = bd.sdv_verify_host(v.ctx, hp, hq, hd, w.temperature, ht, w.seed, *outs)
+            assert st == bd.SDV_OK, bd.sdv_last_error(v.ctx)
+        te = time.perf_counter() - te0
+        te = max_over_ranks(te, world)
+        h2d = hp.numel() * hp.element_size() + hq.numel() * hq.element_size() + hd.numel() * 4 + \
+            (ht.numel() * 4 if ht is not None else 0)
+        result["e2e"] = {"value": world * tokens_per_step * args.e2e_steps / te, "unit": UNIT,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 3 * w.B * 4,
+                         "steps": args.e2e_steps, "ms_per_step": te * 1e3 / args.e2e_steps}
+        del hp, hq
+
+    # The oracle as it stands on the host cores, bounded sample (rank 0, N = 1).
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    v.close()
+    return result
+
+
+def cpu_baseline(w: synth.Workload):
+    import oracle
+    cores = os.cpu_count() or 1
+    S = max(1, min(cores, w.B))
+    p, q, d, t = synth.to_oracle_arrays(w, list(range(S)))
+    nt = min(S, oracle.max_threads()) if oracle.max_threads() > 1 else 1
+    t0 = time.perf_counter()
+    oracle.verify(p, q, d, t, w.seed, nthreads=nt)
+    dt = time.perf_counter() - t0
+    return {"value": S * w.K * w.gamma / dt, "unit": UNIT, "cores": nt, "kind": "oracle",
+            "sample": "first %d of %d sequences of the same workload, one thread per sequence "
+                      "(%.1f s wall)" % (S, w.B, dt)}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the fp64 CPU oracle as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    import oracle
+    oracle.lib()
+    pool = 4
+    c = synth.CONFIGS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    # the first `pool` sequences of the same workload (same generator and seed)
+    w = synth.workload(args.workload, device=dev, seed=args.workload, B=min(pool, c["B"]))
+    p, q, d, t = synth.to_oracle_arrays(w)
+    del w
+    if dev == "cuda":
+        torch.cuda.empty_cache()
+    nt = oracle.max_threads()
+    tokens = c["K"] * c["gamma"]
+
+    def step(i):
+        b = i % p.shape[0]
+        oracle.verify(p[b:b + 1], q[b:b + 1], d[b:b + 1], t[b:b + 1], 0, b0=b, nthreads=nt)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = tokens * args.steps / dt
+    sample = ("one sequence (%d x %d rows of V = %d) per step, cycling over the first %d sequences "
+              "of the workload; rows spread over %d threads" % (c["K"], 2 * c["gamma"] + 1, c["V"],
+                                                                 p.shape[0], nt))
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded logits and drafts; no model weights)",
+        "config": {"workload": c["name"], "B": c["B"], "K": c["K"], "gamma": c["gamma"], "V": c["V"],
+                   "parallelism": "host cores (fp64 CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    rank, world, local = dist_setup()
+    res = run_sdv(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

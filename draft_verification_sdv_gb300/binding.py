@@ -1,0 +1,258 @@
+"""ctypes binding of libsdv (``include/sdv.h``), torch tensors in and out.
+
+Argument marshalling only: every step of the verification runs in the CUDA
+kernels of ``libsdv.so``.  There is no fallback: if the library is missing or
+does not load, every call raises.
+
+The functions keep the C names (``sdv_create``, ``sdv_verify``,
+``sdv_verify_ex``, ``sdv_verify_host``, ``sdv_sync``, ``sdv_last_error``,
+``sdv_destroy``, ``sdv_plan``); ``Verifier`` wraps a context.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsdv.so")
+
+SDV_OK, SDV_ERR_ARG, SDV_ERR_CUDA, SDV_ERR_OOM, SDV_ERR_DEVICE_DATA = 0, 1, 2, 3, 4
+SDV_BF16, SDV_F32 = 0, 1
+STATUS_NAMES = {0: "SDV_OK", 1: "SDV_ERR_ARG", 2: "SDV_ERR_CUDA", 3: "SDV_ERR_OOM",
+                4: "SDV_ERR_DEVICE_DATA"}
+
+# Every entry point of include/sdv.h, with its ctypes signature.
+_VP, _I, _I64, _U64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
+SIGNATURES = {
+    "sdv_create": (_I, [ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _VP]),
+    "sdv_verify": (_I, [_VP, _VP, _VP, _VP, _F, _U64, _VP, _VP, _VP]),
+    "sdv_verify_ex": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP, _VP]),
+    "sdv_verify_host": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
+    "sdv_sync": (_I, [_VP]),
+    "sdv_last_error": (ctypes.c_char_p, [_VP]),
+    "sdv_destroy": (None, [_VP]),
+    "sdv_plan": (_I, [_VP, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I),
+                      ctypes.POINTER(_I)]),
+    "sdv_set_stream": (_I, [_VP, _VP]),
+    "sdv_profile_enable": (_I, [_VP, _I]),
+    "sdv_profile_read": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_I)]),
+}
+
+_lib = None
+
+
+class SdvError(RuntimeError):
+    def __init__(self, status: int, msg: str = ""):
+        super().__init__("%s%s" % (STATUS_NAMES.get(status, str(status)), (": " + msg) if msg else ""))
+        self.status = status
+
+
+def load(build: bool = False) -> ctypes.CDLL:
+    """Load libsdv.so (optionally building it first).  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build:
+        from . import build as _b
+        _b.build()
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libsdv.so is not built (run draft_verification_sdv_gb300.build.build());"
+                           " there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _dev_ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("%s must be a host tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(dtype: torch.dtype) -> int:
+    if dtype == torch.bfloat16:
+        return SDV_BF16
+    if dtype == torch.float32:
+        return SDV_F32
+    raise TypeError("logits must be bfloat16 or float32")
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def sdv_create(B: int, K: int, gamma: int, V: int, dtype: torch.dtype = torch.bfloat16,
+               stream=None) -> ctypes.c_void_p:
+    ctx = ctypes.c_void_p()
+    st = load().sdv_create(ctypes.byref(ctx), B, K, gamma, V, _dtype_code(dtype),
+                           ctypes.c_void_p(_stream_handle(stream)))
+    if st != SDV_OK:
+        raise SdvError(st, "sdv_create(B=%d, K=%d, gamma=%d, V=%d)" % (B, K, gamma, V))
+    return ctx
+
+
+def sdv_verify(ctx, p_logits, q_logits, drafts, temperature, seed, out_sel, out_accept_len,
+               out_next_token) -> int:
+    return load().sdv_verify(ctx, _dev_ptr(p_logits, name="p_logits"),
+                             _dev_ptr(q_logits, name="q_logits"),
+                             _dev_ptr(drafts, torch.int32, "drafts"), float(temperature),
+                             int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
+                             _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
+                             _dev_ptr(out_next_token, torch.int32, "out_next_token"))
+
+
+def sdv_verify_ex(ctx, p_logits, q_logits, drafts, temperature, temperature_per_seq, seed,
+                  out_sel, out_accept_len, out_next_token, out_scores=None, out_lse=None) -> int:
+    return load().sdv_verify_ex(
+        ctx, _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
+        _dev_ptr(drafts, torch.int32, "drafts"), float(temperature),
+        _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
+        _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
+        _dev_ptr(out_next_token, torch.int32, "out_next_token"),
+        _dev_ptr(out_scores, torch.float32, "out_scores"),
+        _dev_ptr(out_lse, torch.float32, "out_lse"))
+
+
+def sdv_verify_host(ctx, p_logits, q_logits, drafts, temperature, temperature_per_seq, seed,
+                    out_sel, out_accept_len, out_next_token) -> int:
+    return load().sdv_verify_host(
+        ctx, _host_ptr(p_logits, name="p_logits"), _host_ptr(q_logits, name="q_logits"),
+        _host_ptr(drafts, torch.int32, "drafts"), float(temperature),
+        _host_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _host_ptr(out_sel, torch.int32, "out_sel"),
+        _host_ptr(out_accept_len, torch.int32, "out_accept_len"),
+        _host_ptr(out_next_token, torch.int32, "out_next_token"))
+
+
+def sdv_sync(ctx) -> int:
+    return load().sdv_sync(ctx)
+
+
+def sdv_last_error(ctx) -> str:
+    r = load().sdv_last_error(ctx)
+    return r.decode() if r else ""
+
+
+def sdv_destroy(ctx) -> None:
+    load().sdv_destroy(ctx)
+
+
+def sdv_plan(ctx) -> dict:
+    g, ck, cv, cl = _I(), _I(), _I64(), _I()
+    st = load().sdv_plan(ctx, ctypes.byref(g), ctypes.byref(cv), ctypes.byref(ck), ctypes.byref(cl))
+    if st != SDV_OK:
+        raise SdvError(st)
+    return {"rowpass_ctas": g.value, "chunk_vectors": cv.value, "chunks_per_row": ck.value,
+            "sample_cluster": cl.value}
+
+
+def sdv_profile_enable(ctx, enable: bool = True) -> int:
+    return load().sdv_profile_enable(ctx, 1 if enable else 0)
+
+
+def sdv_profile_read(ctx):
+    """(mean ms of [row pass, select, sample], number of steps); clears the record."""
+    ms = (_F * 3)()
+    n = _I()
+    st = load().sdv_profile_read(ctx, ms, ctypes.byref(n))
+    if st != SDV_OK:
+        raise SdvError(st, sdv_last_error(ctx))
+    return [float(x) for x in ms], n.value
+
+
+def sdv_set_stream(ctx, stream) -> int:
+    return load().sdv_set_stream(ctx, ctypes.c_void_p(_stream_handle(stream)))
+
+
+class Verifier:
+    """One context for batches of shape (B, K, gamma, V).
+
+    ``v(p, q, drafts, ...)`` enqueues a step on the context's stream and returns
+    the output tensors; ``v.sync()`` waits and raises on a device-side error.
+    """
+
+    def __init__(self, B: int, K: int, gamma: int, V: int, dtype=torch.bfloat16,
+                 device=None, stream=None):
+        self.B, self.K, self.gamma, self.V, self.dtype = B, K, gamma, V, dtype
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        with torch.cuda.device(self.device):
+            self.stream = stream
+            self.ctx = sdv_create(B, K, gamma, V, dtype, stream)
+
+    def __call__(self, p_logits, q_logits, drafts, temperature: float = 1.0, seed: int = 0,
+                 temps: Optional[torch.Tensor] = None, scores: bool = False, lse: bool = False,
+                 out: Optional[dict] = None) -> dict:
+        B, K, G, V = self.B, self.K, self.gamma, self.V
+        if tuple(p_logits.shape) != (B, K, G + 1, V) or tuple(q_logits.shape) != (B, K, G, V):
+            raise ValueError("logits must be [B,K,gamma+1,V] and [B,K,gamma,V]")
+        if tuple(drafts.shape) != (B, K, G):
+            raise ValueError("drafts must be [B,K,gamma]")
+        if p_logits.dtype != self.dtype or q_logits.dtype != self.dtype:
+            raise TypeError("logits must be %s" % self.dtype)
+        dev = p_logits.device
+        if out is None:
+            out = {
+                "sel": torch.empty(B, dtype=torch.int32, device=dev),
+                "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+                "next_token": torch.empty(B, dtype=torch.int32, device=dev),
+            }
+            if scores:
+                out["scores"] = torch.empty((B, K), dtype=torch.float32, device=dev)
+            if lse:
+                out["lse"] = torch.empty((B, K, 2 * G + 1), dtype=torch.float32, device=dev)
+        st = sdv_verify_ex(self.ctx, p_logits, q_logits, drafts, temperature, temps, seed,
+                           out["sel"], out["accept_len"], out["next_token"], out.get("scores"),
+                           out.get("lse"))
+        if st != SDV_OK:
+            raise SdvError(st, sdv_last_error(self.ctx))
+        return out
+
+    def sync(self) -> None:
+        st = sdv_sync(self.ctx)
+        if st != SDV_OK:
+            raise SdvError(st, sdv_last_error(self.ctx))
+
+    def plan(self) -> dict:
+        return sdv_plan(self.ctx)
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None) is not None:
+            sdv_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

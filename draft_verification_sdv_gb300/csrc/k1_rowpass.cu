@@ -1,0 +1,158 @@
+// k1_rowpass.cu -- single-pass online softmax statistics of every logit row.
+//
+// Temperature softmax of the verifier rows p(.|s, x_<j) and drafter rows
+// q_j over the full vocabulary ("SpecDiff-2: Scaling Diffusion Drafter
+// Alignment For Faster Speculative Decoding", section 2: the verifier scores
+// all positions in parallel; section 5.2: its probabilities are computed once
+// and reused by ranking and acceptance).  Each row is read exactly once.
+//
+// Work decomposition: each row is cut into `chunks` fixed chunks of
+// `chunk_vec` 16-byte vectors.  One warp reduces one (row, chunk) item to
+// (m, s) = (max l, sum 2^{(l - m) c}), c = log2(e) / T, with a fixed lane
+// mapping and a fixed reduction tree, so two rows with the same bytes and the
+// same temperature give bit-identical partials whatever their position.  A
+// persistent grid of warps takes items round-robin.
+//
+// The kernel is HBM-bandwidth bound: per element one 2-byte load, one
+// exponential on the special-function unit and a handful of fp32 operations.
+#include "sdv_device.cuh"
+#include "sdv_plan.h"
+
+namespace sdv {
+namespace {
+
+constexpr int kUnroll = 8;   // 16-byte vectors in flight per lane per iteration
+
+// Packed 16-byte vector of -inf values: fills the lanes past a chunk's end.
+template <bool BF16>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+    const uint32_t w = BF16 ? 0xFF80FF80u : 0xFF800000u;
+    return make_uint4(w, w, w, w);
+}
+
+// Max over kUnroll vectors; NaN propagates so that a NaN row is caught.
+template <bool BF16>
+__device__ __forceinline__ float vec_max(const uint4 (&v)[kUnroll]) {
+    if constexpr (BF16) {
+        uint32_t m[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+#pragma unroll
+        for (int u = 1; u < kUnroll; ++u) {
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(v[u].x));
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[1]) : "r"(v[u].y));
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[2]) : "r"(v[u].z));
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[3]) : "r"(v[u].w));
+        }
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(m[1]));
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[2]) : "r"(m[3]));
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(m[2]));
+        float r;
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(bf16_lo(m[0])), "f"(bf16_hi(m[0])));
+        return r;
+    } else {
+        float r = __uint_as_float(v[0].x);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const float e[4] = {__uint_as_float(v[u].x), __uint_as_float(v[u].y),
+                                __uint_as_float(v[u].z), __uint_as_float(v[u].w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) asm("max.NaN.f32 %0, %0, %1;" : "+f"(r) : "f"(e[i]));
+        }
+        return r;
+    }
+}
+
+// Sum of 2^{(l - m) c} over one vector (pairwise tree).
+template <bool BF16>
+__device__ __forceinline__ float vec_sum(const uint4& v, float m, float c) {
+    if constexpr (BF16) {
+        const float e0 = ex2((bf16_lo(v.x) - m) * c), e1 = ex2((bf16_hi(v.x) - m) * c);
+        const float e2 = ex2((bf16_lo(v.y) - m) * c), e3 = ex2((bf16_hi(v.y) - m) * c);
+        const float e4 = ex2((bf16_lo(v.z) - m) * c), e5 = ex2((bf16_hi(v.z) - m) * c);
+        const float e6 = ex2((bf16_lo(v.w) - m) * c), e7 = ex2((bf16_hi(v.w) - m) * c);
+        return ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
+    } else {
+        const float e0 = ex2((__uint_as_float(v.x) - m) * c);
+        const float e1 = ex2((__uint_as_float(v.y) - m) * c);
+        const float e2 = ex2((__uint_as_float(v.z) - m) * c);
+        const float e3 = ex2((__uint_as_float(v.w) - m) * c);
+        return (e0 + e1) + (e2 + e3);
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kRowPassThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kRowPassThreads) >> 5;
+    const int64_t rows_per_seq_p = static_cast<int64_t>(a.K) * (a.G + 1);
+    const int64_t rows_per_seq_q = static_cast<int64_t>(a.K) * a.G;
+
+    for (int64_t item = warp; item < a.items; item += nwarps) {
+        const int64_t row = item / a.chunks;
+        const int64_t chunk = item - row * a.chunks;
+        const int64_t v0 = chunk * a.chunk_vec;
+        const int64_t v1 = min(v0 + a.chunk_vec, a.nvec);
+        const uint4* rowv;
+        int64_t b;
+        if (row < a.rows_p) {
+            rowv = static_cast<const uint4*>(a.p) + row * a.nvec;
+            b = row / rows_per_seq_p;
+        } else {
+            rowv = static_cast<const uint4*>(a.q) + (row - a.rows_p) * a.nvec;
+            b = (row - a.rows_p) / rows_per_seq_q;
+        }
+        const float T = a.temps ? __ldg(a.temps + b) : a.temperature;
+        const float c = kLog2e / T;
+
+        float m = -INFINITY, s = 0.0f;
+        for (int64_t base = v0 + lane; base < v1; base += 32 * kUnroll) {
+            uint4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t idx = base + 32 * u;
+                v[u] = idx < v1 ? ld_stream(rowv + idx) : neg_inf_vec<BF16>();
+            }
+            const float vm = vec_max<BF16>(v);
+            if (!(vm <= m)) {                 // new maximum (or NaN: poisons s)
+                s *= ex2((m - vm) * c);
+                m = vm;
+            }
+            if (m != -INFINITY) {             // all -inf so far: nothing to add
+                float t[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) t[u] = vec_sum<BF16>(v[u], m, c);
+#pragma unroll
+                for (int w = kUnroll / 2; w > 0; w >>= 1)
+#pragma unroll
+                    for (int u = 0; u < w; ++u) t[u] += t[u + w];
+                s += t[0];
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+            merge_stat(m, s, m2, s2, c);
+        }
+        if (lane == 0) a.part[item] = make_float2(m, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm) {
+    return bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, rowpass_kernel<true>,
+                                                                kRowPassThreads, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                      blocks_per_sm, rowpass_kernel<false>, kRowPassThreads, 0);
+}
+
+cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, int grid, cudaStream_t s) {
+    if (bf16)
+        rowpass_kernel<true><<<grid, kRowPassThreads, 0, s>>>(a);
+    else
+        rowpass_kernel<false><<<grid, kRowPassThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace sdv

@@ -1,0 +1,206 @@
+// k2_select.cu -- ratios, expected streaks, self-selection and the
+// left-to-right acceptance scan; one CTA per sequence.
+//
+// Passages: "SpecDiff-2: Scaling Diffusion Drafter Alignment For Faster
+// Speculative Decoding", section 2 (accept x when q(x) <= p(x), else with
+// probability p/q; the first rejection ends the scan), Figure 2 / section 3
+// (position-wise acceptance and the accepted streak), section 5.2 (rank the
+// K drafts by a streak-oriented verifier score, verify the best, reuse the
+// cached verifier probabilities).  The score is the expected accepted length
+// S_k = sum_j prod_{i<=j} min(1, p/q) of draft k; ties go to the lowest k.
+//
+// Uniforms: Philox4x32-10 with key (seed lo, seed hi), counter (j, b, 0, 0):
+// word 0 is the acceptance uniform u_j, word 1 the sampling uniform w_j.
+//
+// Precision: the log-ratio of a drafted token is formed as
+//   ((l_p(x) - m_p) - (l_q(x) - m_q)) * c - log2(S_p / S_q),
+// where the bf16 differences are exact in fp32, so that its error scales with
+// the log-ratio itself and two identical rows give a ratio of exactly 1.
+#include "sdv_device.cuh"
+#include "sdv_plan.h"
+
+namespace sdv {
+namespace {
+
+// Merge the `chunks` partials of one row in chunk order.
+__device__ __forceinline__ void merge_row(const float2* part, int chunks, float c, float& M,
+                                          float& S) {
+    M = -INFINITY;
+    S = 0.0f;
+    for (int i = 0; i < chunks; ++i) {
+        const float2 ps = part[i];
+        merge_stat(M, S, ps.x, ps.y, c);
+    }
+}
+
+__device__ __forceinline__ bool row_valid(float M, float S) {
+    return isfinite(M) && isfinite(S) && S > 0.0f;
+}
+
+// Natural-log LSE of l / T from (max, sum of 2^{(l - max) c}).
+__device__ __forceinline__ float row_lse(float M, float S, float c) {
+    return (M * c + log2f(S)) * kLn2;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int K = a.K, G = a.G;
+    const int KG = K * G;
+    float* ratio = reinterpret_cast<float*>(smem_raw);                                 // [K*G]
+    double* score = reinterpret_cast<double*>(smem_raw + ((static_cast<size_t>(KG) * 4 + 15) & ~size_t(15)));  // [K]
+    __shared__ unsigned s_bad;
+    __shared__ int s_len;
+    __shared__ int s_sel;
+
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const float T = a.temps ? a.temps[b] : a.temperature;
+    const float c = kLog2e / T;
+    if (tid == 0) {
+        s_bad = (isfinite(T) && T > 0.0f) ? 0u : kStatusBadTemp;
+        s_len = G;
+    }
+    __syncthreads();
+
+    const int64_t seq_p = static_cast<int64_t>(b) * K * (G + 1);   // first p row of b
+    const int64_t seq_q = static_cast<int64_t>(b) * K * G;         // first q row of b
+    const int nrow = 2 * G + 1;
+
+    // Acceptance ratio at every drafted token of every draft.
+    for (int idx = tid; idx < KG; idx += kSelectThreads) {
+        const int k = idx / G, j = idx - (idx / G) * G;
+        const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + j;
+        const int64_t rq = seq_q + static_cast<int64_t>(k) * G + j;
+        float mp, sp, mq, sq;
+        merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);
+        merge_row(a.part + (a.rows_p + rq) * a.chunks, a.chunks, c, mq, sq);
+        if (a.out_lse) {
+            float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
+            lse[j] = row_lse(mp, sp, c);
+            lse[G + 1 + j] = row_lse(mq, sq, c);
+        }
+        float r = 0.0f;
+        if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
+            atomicOr(&s_bad, kStatusBadRow);
+        } else {
+            const int32_t x = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
+            if (x < 0 || x >= a.V) {
+                atomicOr(&s_bad, kStatusBadDraft);
+            } else {
+                const float lp = load_logit(a.p, rp * a.V + x, BF16);
+                const float lq = load_logit(a.q, rq * a.V + x, BF16);
+                if (lq == -INFINITY) {
+                    r = 1.0f;                                   // q(x) = 0 <= p(x)
+                } else {
+                    const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
+                    r = d >= 0.0f ? 1.0f : ex2(d);              // q <= p accepts at once
+                }
+            }
+        }
+        ratio[idx] = r;
+    }
+    // The bonus rows (j = G): validity and LSE.
+    for (int k = tid; k < K; k += kSelectThreads) {
+        const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + G;
+        float mp, sp;
+        merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);
+        if (a.out_lse) a.out_lse[(static_cast<int64_t>(b) * K + k) * nrow + G] = row_lse(mp, sp, c);
+        if (!row_valid(mp, sp)) atomicOr(&s_bad, kStatusBadRow);
+    }
+    __syncthreads();
+
+    if (s_bad) {
+        if (tid == 0) {
+            a.out_sel[b] = -1;
+            a.out_len[b] = -1;
+            a.out_tok[b] = -1;
+            SeqTask t = {};
+            t.mode = 0;
+            a.tasks[b] = t;
+            atomicOr(a.status, s_bad);
+        }
+        return;
+    }
+
+    // Expected accepted streak of every draft (prefix products in fp64).
+    for (int k = tid; k < K; k += kSelectThreads) {
+        double prefix = 1.0, sc = 0.0;
+        for (int j = 0; j < G; ++j) {
+            prefix *= static_cast<double>(ratio[k * G + j]);
+            sc += prefix;
+        }
+        score[k] = sc;
+        if (a.out_scores) a.out_scores[static_cast<int64_t>(b) * K + k] = static_cast<float>(sc);
+    }
+    __syncthreads();
+
+    // Self-selection: first draft with the largest expected streak.
+    if (tid == 0) {
+        int best = 0;
+        for (int k = 1; k < K; ++k)
+            if (score[k] > score[best]) best = k;
+        s_sel = best;
+    }
+    __syncthreads();
+    const int sel = s_sel;
+
+    // Left-to-right acceptance of the selected draft: the first rejected j.
+    for (int j = tid; j < G; j += kSelectThreads) {
+        const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u, 0u),
+                                      a.seed_lo, a.seed_hi);
+        const float u = uniform24(r.x);
+        const float aj = ratio[sel * G + j];
+        const bool accepted = (aj >= 1.0f) || (u < aj);
+        if (!accepted) atomicMin(&s_len, j);
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        const int L = s_len;
+        a.out_sel[b] = sel;
+        a.out_len[b] = L;
+        const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(L), static_cast<uint32_t>(b), 0u, 0u),
+                                      a.seed_lo, a.seed_hi);
+        SeqTask t = {};
+        t.w = uniform24(r.y);
+        t.c = c;
+        t.row_p = seq_p + static_cast<int64_t>(sel) * (G + 1) + L;
+        float mp, sp;
+        merge_row(a.part + t.row_p * a.chunks, a.chunks, c, mp, sp);
+        t.mp = mp;
+        t.inv_sp = 1.0f / sp;
+        if (L < G) {
+            t.mode = 1;                                   // residual max(0, p - q)
+            t.row_q = seq_q + static_cast<int64_t>(sel) * G + L;
+            float mq, sq;
+            merge_row(a.part + (a.rows_p + t.row_q) * a.chunks, a.chunks, c, mq, sq);
+            t.mq = mq;
+            t.inv_sq = 1.0f / sq;
+        } else {
+            t.mode = 2;                                   // bonus token from p_gamma
+            t.row_q = -1;
+        }
+        a.tasks[b] = t;
+    }
+}
+
+}  // namespace
+
+cudaError_t setup_select(size_t smem) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
+}
+
+cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s) {
+    if (bf16)
+        select_kernel<true><<<a.B, kSelectThreads, smem, s>>>(a);
+    else
+        select_kernel<false><<<a.B, kSelectThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace sdv

@@ -1,0 +1,438 @@
+// sdv_api.cu -- the C ABI of libsdv (declared in include/sdv.h): contexts,
+// launch planning, argument checks, the three-kernel step, status reporting.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/sdv.h"
+#include "sdv_plan.h"
+
+using namespace sdv;
+
+struct sdv_ctx {
+    int B, K, G, V;
+    sdv_dtype dtype;
+    bool bf16;
+    cudaStream_t stream;
+    int device;
+    int nsm;
+    // row pass
+    int rp_grid;
+    int chunks;
+    int64_t nvec, chunk_vec, rows_p, rows_q, rows_total, items;
+    // select / sample
+    size_t sel_smem;
+    int cluster;
+    int64_t slice_vec;
+    size_t smp_smem;
+    // workspace
+    void* ws;
+    float2* part;
+    SeqTask* tasks;
+    unsigned* status;
+    // device staging of sdv_verify_host (allocated on first use)
+    void* hs_p;
+    void* hs_q;
+    int32_t* hs_drafts;
+    float* hs_temps;
+    int32_t* hs_out;
+    // kernel timing: 4 events per recorded step
+    bool prof_on;
+    std::vector<cudaEvent_t> prof_ev;
+    int prof_n;
+    char err[512];
+};
+
+namespace {
+
+sdv_status fail(sdv_ctx* ctx, sdv_status st, const char* fmt, ...) {
+    if (ctx) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(ctx->err, sizeof ctx->err, fmt, ap);
+        va_end(ap);
+    }
+    return st;
+}
+
+sdv_status cuda_fail(sdv_ctx* ctx, cudaError_t e, const char* what) {
+    return fail(ctx, SDV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t elt_size(sdv_dtype d) { return d == SDV_BF16 ? 2 : 4; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int kMaxProfSteps = 65536;
+
+// Chunking of the row pass: choose the number of chunks per row that
+// minimises (rounds of items over all warps) x (vectors per item + a small
+// per-item cost), with chunks of at least 64 vectors aligned to 8 vectors
+// (128 bytes).
+void plan_chunks(int64_t rows, int64_t nvec, int64_t nwarps, int* chunks_out, int64_t* cv_out) {
+    const int64_t min_cv = nvec < 64 ? nvec : 64;
+    int best_c = 1;
+    int64_t best_cv = nvec;
+    double best_cost = 1e300;
+    const int64_t max_c = nvec / min_cv;
+    for (int64_t c = 1; c <= max_c && c <= 4096; ++c) {
+        int64_t cv = (nvec + c - 1) / c;
+        cv = (cv + 7) / 8 * 8;
+        if (cv > nvec) cv = nvec;
+        const int64_t cc = (nvec + cv - 1) / cv;
+        const int64_t items = rows * cc;
+        const int64_t rounds = (items + nwarps - 1) / nwarps;
+        const double cost = static_cast<double>(rounds) * static_cast<double>(cv + 16);
+        if (cost < best_cost * (1.0 - 1e-9)) {
+            best_cost = cost;
+            best_c = static_cast<int>(cc);
+            best_cv = cv;
+        }
+    }
+    *chunks_out = best_c;
+    *cv_out = best_cv;
+}
+
+bool is_device_ptr(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace
+
+extern "C" {
+
+sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype dtype,
+                      void* stream) {
+    if (!out) return SDV_ERR_ARG;
+    *out = nullptr;
+    if (B < 1 || K < 1 || gamma < 1 || V < 1) return SDV_ERR_ARG;
+    if (dtype != SDV_BF16 && dtype != SDV_F32) return SDV_ERR_ARG;
+    const size_t elt = elt_size(dtype);
+    if ((static_cast<size_t>(V) * elt) % 16 != 0) return SDV_ERR_ARG;
+    if (static_cast<int64_t>(B) * K * (2 * gamma + 1) > (int64_t(1) << 40)) return SDV_ERR_ARG;
+
+    sdv_ctx* ctx = new (std::nothrow) sdv_ctx();
+    if (!ctx) return SDV_ERR_OOM;
+    ctx->B = B;
+    ctx->K = K;
+    ctx->G = gamma;
+    ctx->V = V;
+    ctx->dtype = dtype;
+    ctx->bf16 = dtype == SDV_BF16;
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    ctx->err[0] = 0;
+
+    cudaError_t e = cudaGetDevice(&ctx->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->nsm, cudaDevAttrMultiProcessorCount, ctx->device);
+    int bps = 0;
+    if (e == cudaSuccess) e = rowpass_occupancy(ctx->bf16, &bps);
+    if (e != cudaSuccess || bps < 1) {
+        sdv_destroy(ctx);
+        return SDV_ERR_CUDA;
+    }
+
+    // Row pass plan.
+    ctx->nvec = static_cast<int64_t>(V) * static_cast<int64_t>(elt) / 16;
+    ctx->rows_p = static_cast<int64_t>(B) * K * (gamma + 1);
+    ctx->rows_q = static_cast<int64_t>(B) * K * gamma;
+    ctx->rows_total = ctx->rows_p + ctx->rows_q;
+    const int64_t full_grid = static_cast<int64_t>(ctx->nsm) * bps;
+    const int64_t nwarps_full = full_grid * (kRowPassThreads / 32);
+    plan_chunks(ctx->rows_total, ctx->nvec, nwarps_full, &ctx->chunks, &ctx->chunk_vec);
+    ctx->items = ctx->rows_total * ctx->chunks;
+    const int64_t blocks_needed = (ctx->items + (kRowPassThreads / 32) - 1) / (kRowPassThreads / 32);
+    ctx->rp_grid = static_cast<int>(blocks_needed < full_grid ? blocks_needed : full_grid);
+
+    // Select plan.
+    ctx->sel_smem = align_up(static_cast<size_t>(K) * gamma * 4, 16) + static_cast<size_t>(K) * 8;
+    // Sample plan: up to 8 CTAs per sequence, each holding a slice of one or
+    // two rows in shared memory.
+    int cl = 8;
+    while (cl > 1 && cl > ctx->nvec) cl >>= 1;
+    ctx->cluster = cl;
+    ctx->slice_vec = (ctx->nvec + cl - 1) / cl;
+    ctx->smp_smem = static_cast<size_t>(2) * ctx->slice_vec * 16;
+    const size_t smem_cap = 200 * 1024;
+    if (ctx->sel_smem > smem_cap || ctx->smp_smem > smem_cap) {
+        sdv_destroy(ctx);
+        return SDV_ERR_ARG;
+    }
+    e = setup_select(ctx->sel_smem > 0 ? ctx->sel_smem : 16);
+    if (e == cudaSuccess) e = setup_sample(ctx->smp_smem);
+    if (e != cudaSuccess) {
+        sdv_destroy(ctx);
+        return SDV_ERR_CUDA;
+    }
+
+    // Workspace: partials, tasks, status word.
+    const size_t part_bytes = align_up(static_cast<size_t>(ctx->items) * sizeof(float2), 256);
+    const size_t task_bytes = align_up(static_cast<size_t>(B) * sizeof(SeqTask), 256);
+    const size_t total = part_bytes + task_bytes + 256;
+    e = cudaMalloc(&ctx->ws, total);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        ctx->ws = nullptr;
+        sdv_destroy(ctx);
+        return SDV_ERR_OOM;
+    }
+    char* w = static_cast<char*>(ctx->ws);
+    ctx->part = reinterpret_cast<float2*>(w);
+    ctx->tasks = reinterpret_cast<SeqTask*>(w + part_bytes);
+    ctx->status = reinterpret_cast<unsigned*>(w + part_bytes + task_bytes);
+    e = cudaMemsetAsync(ctx->status, 0, sizeof(unsigned), ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) {
+        sdv_destroy(ctx);
+        return SDV_ERR_CUDA;
+    }
+    *out = ctx;
+    return SDV_OK;
+}
+
+sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                         const int32_t* drafts, float temperature,
+                         const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
+                         int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
+                         float* out_lse) {
+    if (!ctx) return SDV_ERR_ARG;
+    ctx->err[0] = 0;
+    if (!p_logits || !q_logits || !drafts || !out_sel || !out_accept_len || !out_next_token)
+        return fail(ctx, SDV_ERR_ARG, "null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits)) & 15u)
+        return fail(ctx, SDV_ERR_ARG, "logit buffers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(drafts) | reinterpret_cast<uintptr_t>(out_sel) |
+         reinterpret_cast<uintptr_t>(out_accept_len) | reinterpret_cast<uintptr_t>(out_next_token) |
+         reinterpret_cast<uintptr_t>(temperature_per_seq) | reinterpret_cast<uintptr_t>(out_scores) |
+         reinterpret_cast<uintptr_t>(out_lse)) & 3u)
+        return fail(ctx, SDV_ERR_ARG, "int32 / float buffers must be 4-byte aligned");
+    if (!temperature_per_seq && !(std::isfinite(temperature) && temperature > 0.0f))
+        return fail(ctx, SDV_ERR_ARG, "temperature must be finite and > 0");
+    const void* ptrs[8] = {p_logits, q_logits, drafts, out_sel, out_accept_len, out_next_token,
+                           temperature_per_seq, out_scores};
+    for (const void* p : ptrs)
+        if (p && !is_device_ptr(p))
+            return fail(ctx, SDV_ERR_ARG, "argument is not a device pointer");
+    if (out_lse && !is_device_ptr(out_lse))
+        return fail(ctx, SDV_ERR_ARG, "out_lse is not a device pointer");
+
+    RowPassArgs ra;
+    ra.p = p_logits;
+    ra.q = q_logits;
+    ra.part = ctx->part;
+    ra.temps = temperature_per_seq;
+    ra.temperature = temperature;
+    ra.K = ctx->K;
+    ra.G = ctx->G;
+    ra.chunks = ctx->chunks;
+    ra.rows_p = ctx->rows_p;
+    ra.rows_total = ctx->rows_total;
+    ra.nvec = ctx->nvec;
+    ra.chunk_vec = ctx->chunk_vec;
+    ra.items = ctx->items;
+    cudaEvent_t* ev = nullptr;
+    if (ctx->prof_on && ctx->prof_n < kMaxProfSteps) {
+        const size_t need = static_cast<size_t>(ctx->prof_n + 1) * 4;
+        while (ctx->prof_ev.size() < need) {
+            cudaEvent_t x;
+            if (cudaEventCreate(&x) != cudaSuccess) return fail(ctx, SDV_ERR_CUDA, "event create");
+            ctx->prof_ev.push_back(x);
+        }
+        ev = &ctx->prof_ev[static_cast<size_t>(ctx->prof_n) * 4];
+        ++ctx->prof_n;
+    }
+    if (ev) cudaEventRecord(ev[0], ctx->stream);
+    cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->rp_grid, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "row pass launch");
+    if (ev) cudaEventRecord(ev[1], ctx->stream);
+
+    SelectArgs sa;
+    sa.p = p_logits;
+    sa.q = q_logits;
+    sa.drafts = drafts;
+    sa.part = ctx->part;
+    sa.temps = temperature_per_seq;
+    sa.temperature = temperature;
+    sa.B = ctx->B;
+    sa.K = ctx->K;
+    sa.G = ctx->G;
+    sa.V = ctx->V;
+    sa.chunks = ctx->chunks;
+    sa.rows_p = ctx->rows_p;
+    sa.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
+    sa.seed_hi = static_cast<uint32_t>(seed >> 32);
+    sa.out_sel = out_sel;
+    sa.out_len = out_accept_len;
+    sa.out_tok = out_next_token;
+    sa.out_scores = out_scores;
+    sa.out_lse = out_lse;
+    sa.tasks = ctx->tasks;
+    sa.status = ctx->status;
+    e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "select launch");
+    if (ev) cudaEventRecord(ev[2], ctx->stream);
+
+    SampleArgs ma;
+    ma.p = p_logits;
+    ma.q = q_logits;
+    ma.tasks = ctx->tasks;
+    ma.out_tok = out_next_token;
+    ma.status = ctx->status;
+    ma.nvec = ctx->nvec;
+    ma.slice_vec = ctx->slice_vec;
+    ma.cluster = ctx->cluster;
+    e = launch_sample(ma, ctx->bf16, ctx->B, ctx->cluster, ctx->smp_smem, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "sample launch");
+    if (ev) cudaEventRecord(ev[3], ctx->stream);
+    return SDV_OK;
+}
+
+sdv_status sdv_verify(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                      const int32_t* drafts, float temperature, uint64_t seed, int32_t* out_sel,
+                      int32_t* out_accept_len, int32_t* out_next_token) {
+    return sdv_verify_ex(ctx, p_logits, q_logits, drafts, temperature, nullptr, seed, out_sel,
+                         out_accept_len, out_next_token, nullptr, nullptr);
+}
+
+sdv_status sdv_sync(sdv_ctx* ctx) {
+    if (!ctx) return SDV_ERR_ARG;
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "stream synchronize");
+    unsigned h = 0;
+    e = cudaMemcpyAsync(&h, ctx->status, sizeof h, cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->status, 0, sizeof(unsigned), ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
+    if (h & kStatusTimeout)
+        return fail(ctx, SDV_ERR_CUDA, "a bounded device wait gave up (status 0x%x)", h);
+    if (h)
+        return fail(ctx, SDV_ERR_DEVICE_DATA, "device data error (status 0x%x:%s%s%s)", h,
+                    (h & kStatusBadDraft) ? " draft id out of range" : "",
+                    (h & kStatusBadRow) ? " non-finite or all -inf row" : "",
+                    (h & kStatusBadTemp) ? " bad per-sequence temperature" : "");
+    return SDV_OK;
+}
+
+sdv_status sdv_verify_host(sdv_ctx* ctx, const void* p_logits_host, const void* q_logits_host,
+                           const int32_t* drafts_host, float temperature,
+                           const float* temperature_per_seq_host, uint64_t seed,
+                           int32_t* out_sel_host, int32_t* out_accept_len_host,
+                           int32_t* out_next_token_host) {
+    if (!ctx) return SDV_ERR_ARG;
+    if (!p_logits_host || !q_logits_host || !drafts_host || !out_sel_host || !out_accept_len_host ||
+        !out_next_token_host)
+        return fail(ctx, SDV_ERR_ARG, "null pointer argument");
+    const size_t elt = elt_size(ctx->dtype);
+    const size_t pb = static_cast<size_t>(ctx->rows_p) * ctx->V * elt;
+    const size_t qb = static_cast<size_t>(ctx->rows_q) * ctx->V * elt;
+    const size_t db = static_cast<size_t>(ctx->rows_q) * sizeof(int32_t);
+    const size_t B = static_cast<size_t>(ctx->B);
+    cudaError_t e = cudaSuccess;
+    if (!ctx->hs_p) {
+        e = cudaMalloc(&ctx->hs_p, pb);
+        if (e == cudaSuccess) e = cudaMalloc(&ctx->hs_q, qb);
+        if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ctx->hs_drafts), db);
+        if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ctx->hs_temps), B * 4);
+        if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ctx->hs_out), 3 * B * 4);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(ctx->hs_p);
+            cudaFree(ctx->hs_q);
+            cudaFree(ctx->hs_drafts);
+            cudaFree(ctx->hs_temps);
+            cudaFree(ctx->hs_out);
+            ctx->hs_p = ctx->hs_q = nullptr;
+            ctx->hs_drafts = nullptr;
+            ctx->hs_temps = nullptr;
+            ctx->hs_out = nullptr;
+            return fail(ctx, SDV_ERR_OOM, "device staging allocation failed");
+        }
+    }
+    cudaStream_t s = ctx->stream;
+    e = cudaMemcpyAsync(ctx->hs_p, p_logits_host, pb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->hs_q, q_logits_host, qb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->hs_drafts, drafts_host, db, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && temperature_per_seq_host)
+        e = cudaMemcpyAsync(ctx->hs_temps, temperature_per_seq_host, B * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
+    sdv_status st = sdv_verify_ex(ctx, ctx->hs_p, ctx->hs_q, ctx->hs_drafts, temperature,
+                                  temperature_per_seq_host ? ctx->hs_temps : nullptr, seed,
+                                  ctx->hs_out, ctx->hs_out + B, ctx->hs_out + 2 * B, nullptr,
+                                  nullptr);
+    if (st != SDV_OK) return st;
+    e = cudaMemcpyAsync(out_sel_host, ctx->hs_out, B * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(out_accept_len_host, ctx->hs_out + B, B * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(out_next_token_host, ctx->hs_out + 2 * B, B * 4, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
+    return sdv_sync(ctx);
+}
+
+const char* sdv_last_error(const sdv_ctx* ctx) { return ctx ? ctx->err : "null context"; }
+
+void sdv_destroy(sdv_ctx* ctx) {
+    if (!ctx) return;
+    cudaStreamSynchronize(ctx->stream);
+    cudaFree(ctx->ws);
+    cudaFree(ctx->hs_p);
+    cudaFree(ctx->hs_q);
+    cudaFree(ctx->hs_drafts);
+    cudaFree(ctx->hs_temps);
+    cudaFree(ctx->hs_out);
+    for (cudaEvent_t x : ctx->prof_ev) cudaEventDestroy(x);
+    cudaGetLastError();
+    delete ctx;
+}
+
+sdv_status sdv_plan(const sdv_ctx* ctx, int* rowpass_ctas, int64_t* chunk_vectors,
+                    int* chunks_per_row, int* sample_cluster) {
+    if (!ctx) return SDV_ERR_ARG;
+    if (rowpass_ctas) *rowpass_ctas = ctx->rp_grid;
+    if (chunk_vectors) *chunk_vectors = ctx->chunk_vec;
+    if (chunks_per_row) *chunks_per_row = ctx->chunks;
+    if (sample_cluster) *sample_cluster = ctx->cluster;
+    return SDV_OK;
+}
+
+sdv_status sdv_profile_enable(sdv_ctx* ctx, int enable) {
+    if (!ctx) return SDV_ERR_ARG;
+    ctx->prof_on = enable != 0;
+    return SDV_OK;
+}
+
+sdv_status sdv_profile_read(sdv_ctx* ctx, float* ms_avg, int* steps) {
+    if (!ctx || !ms_avg) return SDV_ERR_ARG;
+    double sum[3] = {0.0, 0.0, 0.0};
+    const int n = ctx->prof_n;
+    for (int i = 0; i < n; ++i) {
+        const cudaEvent_t* ev = &ctx->prof_ev[static_cast<size_t>(i) * 4];
+        cudaError_t e = cudaEventSynchronize(ev[3]);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "event synchronize");
+        for (int k = 0; k < 3; ++k) {
+            float ms = 0.0f;
+            e = cudaEventElapsedTime(&ms, ev[k], ev[k + 1]);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "event elapsed time");
+            sum[k] += ms;
+        }
+    }
+    for (int k = 0; k < 3; ++k) ms_avg[k] = n ? static_cast<float>(sum[k] / n) : 0.0f;
+    if (steps) *steps = n;
+    ctx->prof_n = 0;
+    return SDV_OK;
+}
+
+sdv_status sdv_set_stream(sdv_ctx* ctx, void* stream) {
+    if (!ctx) return SDV_ERR_ARG;
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    return SDV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// sdv_plan.h -- launch plan and kernel argument blocks shared by the host
+// side of libsdv and its three kernels.  Internal; the public ABI is sdv.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sdv {
+
+// Bits of the device status word.
+enum : unsigned {
+    kStatusBadDraft = 1u,    // a draft id outside [0, V)
+    kStatusBadRow = 2u,      // a row with NaN / +inf, or only -inf
+    kStatusBadTemp = 4u,     // per-sequence temperature not finite and positive
+    kStatusTimeout = 8u,     // a bounded device wait gave up
+};
+
+// Task handed from the select/scan kernel to the sampling kernel, one per
+// sequence.  mode 0: nothing to draw (data error); 1: residual max(0, p - q)
+// of rows (row_p, row_q); 2: bonus draw from row_p alone.
+struct SeqTask {
+    int mode;
+    int pad;
+    int64_t row_p;      // row index within the p buffer
+    int64_t row_q;      // row index within the q buffer
+    float w;            // sampling uniform
+    float c;            // log2(e) / T
+    float mp, inv_sp;   // row max and 1 / sum 2^{(l - max) c} of the p row
+    float mq, inv_sq;   // same for the q row (residual only)
+};
+
+// Row pass (K1): rows are split into `chunks` fixed chunks of `chunk_vec`
+// 16-byte vectors (the last chunk of a row may be shorter); one warp reduces
+// one (row, chunk) item to a partial (max, sum of 2^{(l - max) c}).
+struct RowPassArgs {
+    const void* p;          // [rows_p][V]
+    const void* q;          // [rows_q][V]
+    float2* part;           // [rows_p + rows_q][chunks]
+    const float* temps;     // [B] or nullptr
+    float temperature;
+    int K, G;
+    int chunks;
+    int64_t rows_p, rows_total;
+    int64_t nvec;           // vectors per row
+    int64_t chunk_vec;      // vectors per chunk
+    int64_t items;          // rows_total * chunks
+};
+
+// Select / scan (K2): one CTA per sequence.
+struct SelectArgs {
+    const void* p;
+    const void* q;
+    const int32_t* drafts;
+    const float2* part;
+    const float* temps;
+    float temperature;
+    int B, K, G, V, chunks;
+    int64_t rows_p;
+    uint32_t seed_lo, seed_hi;
+    int32_t* out_sel;
+    int32_t* out_len;
+    int32_t* out_tok;       // written with -1 here on a data error
+    float* out_scores;      // [B][K] or nullptr
+    float* out_lse;         // [B][K][2G+1] or nullptr
+    SeqTask* tasks;
+    unsigned* status;
+};
+
+// Residual / bonus sampling (K3): a cluster of `cluster` CTAs per sequence,
+// each staging `slice_vec` vectors of the row(s) in shared memory.
+struct SampleArgs {
+    const void* p;
+    const void* q;
+    const SeqTask* tasks;
+    int32_t* out_tok;
+    unsigned* status;
+    int64_t nvec;
+    int64_t slice_vec;
+    int cluster;
+};
+
+// Launchers (defined next to their kernels).  `bf16` selects the element type
+// (bf16 when true, fp32 otherwise).  Each returns the launch's error code.
+cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s);
+cudaError_t launch_sample(const SampleArgs& a, bool bf16, int B, int cluster, size_t smem,
+                          cudaStream_t s);
+// Per-kernel set-up (shared-memory opt-in), once per device.
+cudaError_t setup_select(size_t smem);
+cudaError_t setup_sample(size_t smem);
+// Resident blocks per SM of the row-pass kernel.
+cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm);
+
+constexpr int kRowPassThreads = 256;
+constexpr int kSelectThreads = 256;
+constexpr int kSampleThreads = 256;
+
+}  // namespace sdv

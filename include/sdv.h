@@ -1,0 +1,168 @@
+/*
+ * sdv.h -- C ABI of libsdv: batched lossless draft verification with
+ * test-time self-selection, for speculative decoding with diffusion drafters,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * What one call computes, for every sequence b of a batch of B, given K
+ * candidate drafts of gamma tokens each:
+ *
+ *   1. Temperature softmax of every verifier row p(.|s, x_<j) (j = 0..gamma)
+ *      and drafter row q_j (j = 0..gamma-1) over the full vocabulary V.
+ *      ("SpecDiff-2: Scaling Diffusion Drafter Alignment For Faster
+ *      Speculative Decoding", section 2: the verifier scores all positions in
+ *      parallel and exposes q(.|s) and p(.|s).)
+ *   2. Per drafted token the acceptance ratio a = min(1, p(x)/q(x)), and per
+ *      draft the expected accepted streak S_k = sum_j prod_{i<=j} a_i
+ *      (same page, Figure 2 and section 3: position-wise acceptance and
+ *      accepted streaks).
+ *   3. Self-selection: sel = argmax_k S_k, ties to the lowest k (same page,
+ *      section 5.2: K drafts from one denoising pass are ranked by a
+ *      streak-oriented verifier score and the best is verified; the verifier
+ *      probabilities of the ranking are reused for acceptance).
+ *   4. The standard left-to-right acceptance rule on draft sel: token j is
+ *      accepted when q <= p, else when u_j < p/q; the first rejection ends the
+ *      scan (same page, section 2; "DiffuSpec: Unlocking Diffusion Language
+ *      Models for Speculative Decoding", section 3).
+ *   5. At the first rejection L < gamma, a replacement token drawn from the
+ *      normalised residual max(0, p_L - q_L) (same passages); when all gamma
+ *      tokens are accepted, a bonus token drawn from p_gamma.
+ *
+ * Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key
+ * (seed & 0xffffffff, seed >> 32) and counter (j, b, 0, 0); word 0 gives the
+ * acceptance uniform u_j, word 1 the sampling uniform w_j, each as
+ * (word >> 8) * 2^-24.  The uniforms do not depend on k.  Inverse-CDF draws
+ * return the first id v whose cumulative mass exceeds w * (total mass).
+ *
+ * Layout: every tensor is contiguous, row-major, on the device of the
+ * context unless stated otherwise.
+ *   p_logits  [B][K][gamma+1][V]  bf16 or fp32
+ *   q_logits  [B][K][gamma][V]    same dtype as p_logits
+ *   drafts    [B][K][gamma]       int32 token ids
+ *   out_sel, out_accept_len, out_next_token  [B] int32
+ * V * sizeof(element) must be a multiple of 16 bytes and both logit buffers
+ * 16-byte aligned (every row then starts on a 16-byte boundary).
+ *
+ * Ownership: the caller owns every tensor.  A context owns its workspace
+ * (allocated by sdv_create, freed by sdv_destroy) and borrows the stream.
+ *
+ * Errors: argument errors are returned synchronously and nothing is
+ * enqueued.  Data errors found on the device (a draft id outside [0, V), a row
+ * holding NaN or +inf or only -inf, a per-sequence temperature that is not a
+ * finite positive number) set the outputs of that sequence to -1 and are
+ * reported by the next sdv_sync.  A context is not thread-safe; use one
+ * context per stream.  Outputs are a pure function of (inputs, temperature,
+ * seed).
+ */
+#ifndef SDV_H
+#define SDV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sdv_ctx sdv_ctx;
+
+typedef enum {
+    SDV_OK = 0,
+    SDV_ERR_ARG = 1,          /* bad argument; nothing was enqueued              */
+    SDV_ERR_CUDA = 2,         /* a CUDA runtime call failed, or a device wait    */
+                              /* gave up after its iteration limit               */
+    SDV_ERR_OOM = 3,          /* workspace allocation failed                     */
+    SDV_ERR_DEVICE_DATA = 4   /* bad draft id / non-finite row / bad per-seq T   */
+} sdv_status;
+
+typedef enum { SDV_BF16 = 0, SDV_F32 = 1 } sdv_dtype;
+
+/*
+ * Create a context for batches of shape (B, K, gamma, V) on the current CUDA
+ * device, enqueuing on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  Requires B >= 1, K >= 1, gamma >= 1, V >= 1, V * elt % 16 == 0.
+ * Allocates the workspace (partial row statistics, per-sequence tasks, a
+ * status word: a few MB at most).  On error *out is NULL.
+ */
+sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V,
+                      sdv_dtype dtype, void* stream);
+
+/*
+ * Enqueue one verification step with one temperature for all sequences
+ * (temperature > 0, finite; it scales both p and q).  Returns after
+ * enqueuing; the outputs are valid once the stream has reached this point.
+ */
+sdv_status sdv_verify(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                      const int32_t* drafts, float temperature, uint64_t seed,
+                      int32_t* out_sel, int32_t* out_accept_len,
+                      int32_t* out_next_token);
+
+/*
+ * As sdv_verify, plus:
+ *   temperature_per_seq  device float [B] or NULL (NULL: use `temperature`)
+ *   out_scores           device float [B][K] expected streaks, or NULL
+ *   out_lse              device float [B][K][2 gamma + 1] row log-sum-exp of
+ *                        l / T (p rows j = 0..gamma, then q rows j = 0..gamma-1),
+ *                        or NULL
+ */
+sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                         const int32_t* drafts, float temperature,
+                         const float* temperature_per_seq, uint64_t seed,
+                         int32_t* out_sel, int32_t* out_accept_len,
+                         int32_t* out_next_token, float* out_scores,
+                         float* out_lse);
+
+/*
+ * End-to-end variant for callers whose data lives in HOST memory: copies the
+ * inputs to device buffers owned by the context (allocated on the first call,
+ * the size of one batch's inputs), runs sdv_verify_ex, copies the three
+ * outputs back and waits for the stream.  All pointers are host pointers
+ * (pinned memory gives full copy bandwidth); temperature_per_seq may be NULL.
+ * Returns the status of the step, as sdv_sync would.
+ */
+sdv_status sdv_verify_host(sdv_ctx* ctx, const void* p_logits_host,
+                           const void* q_logits_host, const int32_t* drafts_host,
+                           float temperature, const float* temperature_per_seq_host,
+                           uint64_t seed, int32_t* out_sel_host,
+                           int32_t* out_accept_len_host,
+                           int32_t* out_next_token_host);
+
+/*
+ * Wait for the context's stream and return the device-side status of every
+ * step enqueued since the previous sdv_sync (then cleared): SDV_OK,
+ * SDV_ERR_DEVICE_DATA or SDV_ERR_CUDA.
+ */
+sdv_status sdv_sync(sdv_ctx* ctx);
+
+/* Text of the last error seen by this context ("" if none).  The pointer is
+ * valid until the next call on the context. */
+const char* sdv_last_error(const sdv_ctx* ctx);
+
+/* Free the workspace and the context (NULL is a no-op).  Waits for the
+ * context's stream first. */
+void sdv_destroy(sdv_ctx* ctx);
+
+/* Launch plan of a context, for tests and benchmarks: CTAs of the row pass,
+ * 16-byte vectors per row chunk, chunks per row, CTAs per sequence (cluster
+ * size) of the sampling pass.  Any pointer may be NULL. */
+sdv_status sdv_plan(const sdv_ctx* ctx, int* rowpass_ctas, int64_t* chunk_vectors,
+                    int* chunks_per_row, int* sample_cluster);
+
+/* Replace the stream of a context (a cudaStream_t). */
+sdv_status sdv_set_stream(sdv_ctx* ctx, void* stream);
+
+/*
+ * Kernel timing.  While enabled, every step records CUDA events on the
+ * context's stream before the row pass and after each of its three kernels
+ * (row pass, select/scan, sample), for up to 65536 steps.  sdv_profile_read
+ * waits for the recorded steps, writes the mean device time in milliseconds
+ * of each kernel to ms_avg[0..2] and the number of steps to *steps, and
+ * clears the record.  Enabling with enable = 0 stops recording.
+ */
+sdv_status sdv_profile_enable(sdv_ctx* ctx, int enable);
+sdv_status sdv_profile_read(sdv_ctx* ctx, float* ms_avg, int* steps);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDV_H */

@@ -6,7 +6,8 @@
  * benchmark's CPU-baseline leg; never by the product path.  It shares no code
  * with the CUDA library.  Every step is written in the order the method states
  * it, with no blocking, fusion or reordering; the only parallelism is over
- * independent sequences.  See sdv_oracle.h for the passages followed.
+ * independent sequences, or over the independent rows of one sequence.  See
+ * sdv_oracle.h for the passages followed.
  */
 #include "sdv_oracle.h"
 
@@ -211,7 +212,7 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
                       const double* u, const double* w, int32_t* sel_out,
                       int32_t* len_out, int32_t* tok_out, double* lse_out,
                       double* scores_out, double* ratio_out, int32_t* band_out,
-                      double* resid_out)
+                      double* resid_out, int row_threads)
 {
     const int K = sh->K, G = sh->gamma, dtype = sh->dtype;
     const int64_t V = sh->V;
@@ -235,13 +236,19 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     if (!lse || !a || !S || !r) { free(lse); free(a); free(S); free(r); return -1; }
 
-    /* Temperature softmax of every p row (j = 0..G) and q row (j < G). */
-    for (int k = 0; k < K; ++k) {
-        for (int j = 0; j <= G; ++j)
-            lse[k * nrow + j] = sdvo_row_lse(p_row(p_logits, sh, b, k, j), dtype, V, T);
-        for (int j = 0; j < G; ++j)
-            lse[k * nrow + G + 1 + j] = sdvo_row_lse(q_row(q_logits, sh, b, k, j), dtype, V, T);
+    /* Temperature softmax of every p row (j = 0..G) and q row (j < G); the
+     * rows are independent, so they may be spread over threads. */
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(row_threads > 1 ? row_threads : 1) schedule(dynamic, 4) if (row_threads > 1)
+#endif
+    for (int i = 0; i < K * nrow; ++i) {
+        const int k = i / nrow, r = i % nrow;
+        if (r <= G)
+            lse[i] = sdvo_row_lse(p_row(p_logits, sh, b, k, r), dtype, V, T);
+        else
+            lse[i] = sdvo_row_lse(q_row(q_logits, sh, b, k, r - G - 1), dtype, V, T);
     }
+    (void)row_threads;
     for (int i = 0; i < K * nrow; ++i)
         if (!isfinite(lse[i])) err |= SDVO_BAD_ROW;
     if (lse_out) memcpy(lse_out, lse, sizeof(double) * (size_t)K * nrow);
@@ -334,9 +341,13 @@ static int run_batch(int B, int K, int gamma, int64_t V, int dtype,
     if (B < 0 || K < 1 || gamma < 0 || V < 1 || (dtype != SDVO_BF16 && dtype != SDVO_F32))
         return -1;
     const int nrow = 2 * gamma + 1;
-#ifdef _OPENMP
+    /* Threads go to independent sequences when there are enough of them,
+     * else to the independent rows of each sequence. */
     int nt = nthreads > 1 ? nthreads : 1;
-#pragma omp parallel for num_threads(nt) schedule(dynamic, 1) reduction(| : any)
+    const int seq_threads = B >= nt ? nt : 1;
+    const int row_threads = B >= nt ? 1 : nt;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(seq_threads) schedule(dynamic, 1) reduction(| : any) if (seq_threads > 1)
 #endif
     for (int b = 0; b < B; ++b) {
         double* u = (double*)malloc(sizeof(double) * (size_t)(gamma + 1));
@@ -356,12 +367,12 @@ static int run_batch(int B, int K, int gamma, int64_t V, int dtype,
                            scores ? scores + (int64_t)b * K : NULL,
                            ratio ? ratio + (int64_t)b * K * gamma : NULL,
                            band ? band + b : NULL,
-                           resid_mass ? resid_mass + b : NULL);
+                           resid_mass ? resid_mass + b : NULL, row_threads);
         if (err) err[b] = e;
         any |= e;
         free(u); free(w);
     }
-    (void)nthreads;
+    (void)seq_threads;
     return any;
 }
 

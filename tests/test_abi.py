@@ -1,0 +1,64 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point
+that include/sdv.h declares; argument checks that need no GPU behave as
+documented.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdv.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdv_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from draft_verification_sdv_gb300 import binding
+    return binding.load(build=True)
+
+
+def test_header_declares_the_api():
+    names = _declared_functions()
+    for required in ("sdv_create", "sdv_verify", "sdv_verify_ex", "sdv_verify_host",
+                     "sdv_sync", "sdv_last_error", "sdv_destroy"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from draft_verification_sdv_gb300 import binding
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in binding.SIGNATURES, "binding misses " + name
+
+
+def test_argument_errors_without_gpu(lib):
+    from draft_verification_sdv_gb300 import binding as bd
+    ctx = ctypes.c_void_p()
+    # shape / dtype / alignment checks return before any CUDA call
+    assert lib.sdv_create(None, 1, 1, 1, 32, bd.SDV_F32, None) == bd.SDV_ERR_ARG
+    for B, K, G, V, dt in [(0, 1, 4, 32, bd.SDV_F32), (1, 0, 4, 32, bd.SDV_F32),
+                           (1, 1, 0, 32, bd.SDV_F32), (1, 1, 4, 0, bd.SDV_F32),
+                           (1, 1, 4, 30, bd.SDV_BF16), (1, 1, 4, 5, bd.SDV_F32),
+                           (1, 1, 4, 32, 7)]:
+        assert lib.sdv_create(ctypes.byref(ctx), B, K, G, V, dt, None) == bd.SDV_ERR_ARG
+        assert ctx.value is None
+    assert lib.sdv_verify(None, None, None, None, 1.0, 0, None, None, None) == bd.SDV_ERR_ARG
+    assert lib.sdv_sync(None) == bd.SDV_ERR_ARG
+    assert lib.sdv_last_error(None) == b"null context"
+    lib.sdv_destroy(None)
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "draft_verification_sdv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "sdvo_" not in text and "sdv_oracle" not in text, f

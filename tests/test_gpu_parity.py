@@ -1,0 +1,316 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Bar (decisions are integers): selected draft, accepted length and emitted
+token bit-exact, except trials the oracle flags inside the 1e-5 boundary band
+(uniform within 1e-5 relative of an acceptance ratio or CDF boundary, or
+top-2 streak scores within 1e-5 relative), which are counted and reported.
+Row LSE and expected-streak scores within 1e-4 relative (LSE against
+max(1, |LSE|)).
+"""
+import numpy as np
+import pytest
+import torch
+
+from draft_verification_sdv_gb300 import binding as bd
+from draft_verification_sdv_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+LSE_RTOL = 1e-4
+SCORE_RTOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bd.load(build=True)
+
+
+def run_gpu(w: synth.Workload, seed=None, stream=None):
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream)
+    out = v(w.p_logits, w.q_logits, w.drafts, temperature=w.temperature,
+            seed=w.seed if seed is None else seed, temps=w.temps, scores=True, lse=True)
+    status = bd.sdv_sync(v.ctx)
+    res = {k: t.cpu().numpy() for k, t in out.items()}
+    res["status"] = status
+    res["plan"] = v.plan()
+    v.close()
+    return res
+
+
+def run_oracle(w: synth.Workload, seqs=None, seed=None):
+    import oracle
+    p, q, d, t = synth.to_oracle_arrays(w, seqs)
+    seed = w.seed if seed is None else seed
+    if seqs is None:
+        return oracle.verify(p, q, d, t, seed, nthreads=oracle.max_threads())
+    # sampled sequences keep their own b in the uniform keying
+    outs = [oracle.verify(p[i:i + 1], q[i:i + 1], d[i:i + 1], t[i:i + 1], seed, b0=b,
+                          nthreads=1) for i, b in enumerate(seqs)]
+    return {k: np.concatenate([o[k] for o in outs]) for k in outs[0]}
+
+
+def compare(gpu, orc, seqs=None, tag=""):
+    """Assert parity; return the number of boundary-band trials."""
+    seqs = list(range(len(orc["sel"]))) if seqs is None else list(seqs)
+    n_band = 0
+    for i, b in enumerate(seqs):
+        if orc["err"][i]:
+            assert gpu["sel"][b] == -1 and gpu["accept_len"][b] == -1 and gpu["next_token"][b] == -1
+            continue
+        lo, lg = orc["lse"][i], gpu["lse"][b]
+        bad = np.abs(lg - lo) > LSE_RTOL * np.maximum(1.0, np.abs(lo))
+        assert not bad.any(), "%s b=%d LSE mismatch %s vs %s" % (tag, b, lg[bad][:4], lo[bad][:4])
+        so, sg = orc["scores"][i], gpu["scores"][b]
+        assert np.all(np.abs(sg - so) <= SCORE_RTOL * np.abs(so) + 1e-6), \
+            "%s b=%d scores %s vs %s" % (tag, b, sg, so)
+        if orc["band"][i]:
+            n_band += 1
+            continue
+        got = (int(gpu["sel"][b]), int(gpu["accept_len"][b]), int(gpu["next_token"][b]))
+        exp = (int(orc["sel"][i]), int(orc["accept_len"][i]), int(orc["next_token"][i]))
+        assert got == exp, "%s b=%d (sel, L, token) gpu %s oracle %s" % (tag, b, got, exp)
+    return n_band
+
+
+def _small(B, K, G, V, dtype=torch.bfloat16, T=1.0, seed=0, temps=None, identical=(),
+           sigma=0.8, p_sigma=3.0, zipf=True):
+    return synth.generate(B, K, G, V, dtype=dtype, p_sigma=p_sigma, zipf=zipf,
+                          q_sigma=torch.full((B, K, G), sigma), identical=identical,
+                          temperature=T, temps=temps, seed=seed, device="cuda")
+
+
+# ---------------------------------------------------------------------------
+# small shapes: full oracle comparison
+# ---------------------------------------------------------------------------
+
+def test_tiny_exact_workload():
+    w = synth.workload(1, device="cuda")
+    gpu, orc = run_gpu(w), run_oracle(w)
+    assert gpu["status"] == bd.SDV_OK
+    assert compare(gpu, orc, tag="tiny") == 0
+
+
+def test_tiny_style_many_sequences_fp32():
+    # many independent trials of the tiny exactness shape (V = 32, fp32)
+    w = synth.generate(2048, 1, 4, 32, dtype=torch.float32, p_sigma=2.0, zipf=False,
+                       q_sigma=torch.ones((2048, 1, 4)), seed=11, device="cuda")
+    gpu, orc = run_gpu(w, seed=5), run_oracle(w, seed=5)
+    nb = compare(gpu, orc, tag="tiny-many")
+    assert nb <= 3, nb
+    # the residual path and the bonus path both occur
+    L = orc["accept_len"]
+    assert (L < 4).any() and (L == 4).any()
+
+
+@pytest.mark.parametrize("shape", [
+    (4, 3, 5, 5000, 0.7),        # several chunks per row, ragged last chunk
+    (3, 2, 3, 8, 1.0),           # one vector per row (bf16)
+    (2, 4, 7, 12344, 1.3),       # V*2 = 16 * 1543: odd vector count
+    (1, 1, 1, 152064, 1.0),      # gamma = 1
+    (5, 6, 2, 2048, 0.05),       # very low temperature: near one-hot rows
+    (2, 2, 4, 3000, 5.0),        # high temperature: near-uniform rows
+])
+def test_small_shapes(shape):
+    B, K, G, V, T = shape
+    w = _small(B, K, G, V, T=T, seed=B * 1000 + V)
+    gpu, orc = run_gpu(w, seed=7), run_oracle(w, seed=7)
+    assert gpu["status"] == bd.SDV_OK
+    assert compare(gpu, orc, tag=str(shape)) <= max(1, B // 100)
+
+
+def test_fp32_large_vocab():
+    w = _small(3, 2, 3, 40000, dtype=torch.float32, T=0.9, seed=3)
+    gpu, orc = run_gpu(w), run_oracle(w)
+    assert compare(gpu, orc, tag="fp32") == 0
+
+
+def test_single_stream_workload_full():
+    w = synth.workload(2, device="cuda")
+    gpu, orc = run_gpu(w), run_oracle(w)
+    assert compare(gpu, orc, tag="single-stream") == 0
+
+
+def test_self_selection_workload_full():
+    w = synth.workload(3, device="cuda")
+    gpu, orc = run_gpu(w), run_oracle(w)
+    nb = compare(gpu, orc, tag="self-selection")
+    assert nb <= 1
+    assert len(set(orc["sel"].tolist())) > 1, "selection never moves off draft 0"
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled sequences against the oracle, properties on all
+# ---------------------------------------------------------------------------
+
+def test_serving_workload_sampled():
+    w = synth.workload(4, device="cuda")
+    gpu = run_gpu(w)
+    assert gpu["status"] == bd.SDV_OK
+    G = w.gamma
+    ident = set(w.identical)
+    assert len(ident) == 19
+    for b in range(w.B):
+        assert 0 <= gpu["sel"][b] < w.K and 0 <= gpu["accept_len"][b] <= G
+        assert 0 <= gpu["next_token"][b] < w.V
+        if b in ident:                      # q == p: full acceptance, streak gamma, draft 0
+            assert gpu["accept_len"][b] == G and gpu["sel"][b] == 0
+            assert np.all(gpu["scores"][b] == G)
+    rng = np.random.default_rng(4)
+    seqs = sorted(set(rng.choice(w.B, 5, replace=False).tolist()) | {sorted(ident)[0]})
+    orc = run_oracle(w, seqs)
+    assert compare(gpu, orc, seqs, tag="serving") <= 1
+
+
+def test_large_window_workload_sampled():
+    w = synth.workload(5, device="cuda")
+    gpu = run_gpu(w)
+    assert gpu["status"] == bd.SDV_OK
+    assert ((gpu["accept_len"] >= 0) & (gpu["accept_len"] <= w.gamma)).all()
+    assert ((gpu["next_token"] >= 0) & (gpu["next_token"] < w.V)).all()
+    # the residual token carries residual mass: p > q at that id
+    for b in range(w.B):
+        L, k, x = int(gpu["accept_len"][b]), int(gpu["sel"][b]), int(gpu["next_token"][b])
+        if L < w.gamma:
+            lse = gpu["lse"][b, k]
+            T = w.temps_list()[b]
+            lp = float(w.p_logits[b, k, L, x]) / T - lse[L]
+            lq = float(w.q_logits[b, k, L, x]) / T - lse[w.gamma + 1 + L]
+            assert lp > lq - 1e-6
+    seqs = [0, 13, 31]
+    orc = run_oracle(w, seqs)
+    assert compare(gpu, orc, seqs, tag="large-window") <= 1
+    del w
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+def test_identical_rows_everywhere():
+    B, K, G, V = 6, 3, 4, 1000
+    w = _small(B, K, G, V, identical=range(B), seed=21)
+    gpu, orc = run_gpu(w), run_oracle(w)
+    assert (gpu["accept_len"] == G).all() and (gpu["sel"] == 0).all()
+    assert (gpu["scores"] == G).all()
+    assert compare(gpu, orc, tag="identical") == 0
+
+
+def test_minus_inf_logits():
+    """-inf entries carry no mass; q(x) = 0 accepts, p(x) = 0 < q(x) rejects."""
+    B, K, G, V = 4, 2, 3, 512
+    w = _small(B, K, G, V, seed=31)
+    p, q, d = w.p_logits, w.q_logits, w.drafts
+    ninf = float("-inf")
+    p[:, :, :, 300:] = ninf                  # masked tail of the verifier rows
+    q[:, :, :, 400:] = ninf
+    d[0, 0, 0] = 350                         # p(x) = 0, q(x) > 0: reject at j = 0
+    d[1, :, 1] = 450                         # q(x) = 0: accept at once
+    p[2, :, :, 0] = ninf                     # a -inf in the middle of a row
+    gpu, orc = run_gpu(w, seed=3), run_oracle(w, seed=3)
+    assert compare(gpu, orc, tag="-inf") == 0
+    # sequence 0 draft 0 has ratio 0 at j = 0: its score is 0
+    assert gpu["scores"][0, 0] == 0.0
+    assert (gpu["next_token"][gpu["next_token"] >= 0] < 300).all()
+
+
+def test_one_token_rows():
+    """Rows with a single finite entry: softmax is one-hot."""
+    B, K, G, V = 3, 2, 2, 256
+    w = _small(B, K, G, V, seed=41)
+    w.p_logits.fill_(float("-inf"))
+    w.q_logits.fill_(float("-inf"))
+    w.p_logits[..., 7] = 1.5
+    w.q_logits[..., 7] = -3.0
+    w.drafts.fill_(7)
+    gpu, orc = run_gpu(w), run_oracle(w)
+    assert (gpu["accept_len"] == G).all() and (gpu["next_token"] == 7).all()
+    assert compare(gpu, orc, tag="one-hot") == 0
+
+
+def test_data_errors_reported():
+    B, K, G, V = 4, 2, 3, 1024
+    w = _small(B, K, G, V, seed=51)
+    w.drafts[1, 1, 2] = V                          # draft id out of range
+    w.p_logits[2, 0, 1, 10] = float("nan")         # NaN in a row
+    temps = torch.tensor([1.0, 1.0, 1.0, -2.0], device="cuda")   # bad temperature
+    w.temps = temps
+    gpu = run_gpu(w)
+    assert gpu["status"] == bd.SDV_ERR_DEVICE_DATA
+    assert list(gpu["sel"][1:]) == [-1, -1, -1]
+    assert list(gpu["next_token"][1:]) == [-1, -1, -1]
+    orc = run_oracle(w)
+    compare(gpu, orc, tag="errors")
+    # status is cleared by sdv_sync: a clean step afterwards reports OK
+    w2 = _small(B, K, G, V, seed=52)
+    assert run_gpu(w2)["status"] == bd.SDV_OK
+
+
+def test_argument_errors():
+    w = _small(2, 2, 2, 64, seed=61)
+    v = bd.Verifier(2, 2, 2, 64)
+    out = {k: torch.empty(2, dtype=torch.int32, device="cuda") for k in ("sel", "accept_len", "next_token")}
+    st = bd.sdv_verify(v.ctx, w.p_logits, w.q_logits, w.drafts, 0.0, 0, out["sel"],
+                       out["accept_len"], out["next_token"])
+    assert st == bd.SDV_ERR_ARG and "temperature" in bd.sdv_last_error(v.ctx)
+    host = w.p_logits.cpu()
+    st = bd.load().sdv_verify(v.ctx, host.data_ptr(), w.q_logits.data_ptr(), w.drafts.data_ptr(),
+                              1.0, 0, out["sel"].data_ptr(), out["accept_len"].data_ptr(),
+                              out["next_token"].data_ptr())
+    assert st == bd.SDV_ERR_ARG and "device pointer" in bd.sdv_last_error(v.ctx)
+    raw = torch.empty(w.p_logits.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    st = bd.load().sdv_verify(v.ctx, raw.data_ptr() + 2, w.q_logits.data_ptr(), w.drafts.data_ptr(),
+                              1.0, 0, out["sel"].data_ptr(), out["accept_len"].data_ptr(),
+                              out["next_token"].data_ptr())
+    assert st == bd.SDV_ERR_ARG and "aligned" in bd.sdv_last_error(v.ctx)
+    assert bd.sdv_sync(v.ctx) == bd.SDV_OK
+    v.close()
+
+
+def test_deterministic_and_seeded():
+    w = _small(16, 4, 8, 20000, seed=71)
+    a, b2 = run_gpu(w, seed=9), run_gpu(w, seed=9)
+    for k in ("sel", "accept_len", "next_token", "scores", "lse"):
+        assert np.array_equal(a[k], b2[k]), k
+    c = run_gpu(w, seed=10)
+    assert np.array_equal(a["sel"], c["sel"]) and np.array_equal(a["scores"], c["scores"])
+    assert not np.array_equal(a["next_token"], c["next_token"]) or \
+        not np.array_equal(a["accept_len"], c["accept_len"])
+
+
+def test_per_sequence_temperature_matches_scalar():
+    B, K, G, V = 4, 2, 3, 4096
+    w = _small(B, K, G, V, T=0.8, seed=81)
+    scalar = run_gpu(w)
+    w.temps = torch.full((B,), 0.8, device="cuda")
+    per_seq = run_gpu(w)
+    for k in ("sel", "accept_len", "next_token", "scores", "lse"):
+        assert np.array_equal(scalar[k], per_seq[k]), k
+
+
+def test_host_entry_point_matches_device():
+    w = _small(8, 3, 6, 7000, seed=91)
+    dev = run_gpu(w, seed=4)
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype)
+    hp, hq = w.p_logits.cpu().pin_memory(), w.q_logits.cpu().pin_memory()
+    hd = w.drafts.cpu().pin_memory()
+    outs = [torch.empty(w.B, dtype=torch.int32).pin_memory() for _ in range(3)]
+    for _ in range(2):
+        st = bd.sdv_verify_host(v.ctx, hp, hq, hd, w.temperature, None, 4, *outs)
+        assert st == bd.SDV_OK
+        assert np.array_equal(outs[0].numpy(), dev["sel"])
+        assert np.array_equal(outs[1].numpy(), dev["accept_len"])
+        assert np.array_equal(outs[2].numpy(), dev["next_token"])
+    v.close()
+
+
+def test_side_stream():
+    w = _small(4, 2, 3, 3000, seed=101)
+    s = torch.cuda.Stream()
+    ref = run_gpu(w)
+    with torch.cuda.stream(s):
+        got = run_gpu(w, stream=s)
+    for k in ("sel", "accept_len", "next_token"):
+        assert np.array_equal(ref[k], got[k])
