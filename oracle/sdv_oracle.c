@@ -230,11 +230,16 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
         }
     if (err) return err;
 
+    const size_t nkg = (size_t)K * (G > 0 ? G : 1);
     double* lse = (double*)malloc(sizeof(double) * (size_t)K * nrow);
-    double* a = (double*)malloc(sizeof(double) * (size_t)K * (G > 0 ? G : 1));
-    double* S = (double*)malloc(sizeof(double) * (size_t)K);
+    double* a = (double*)malloc(sizeof(double) * nkg * 3);
+    double* S = (double*)malloc(sizeof(double) * (size_t)K * 3);
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     if (!lse || !a || !S || !r) { free(lse); free(a); free(S); free(r); return -1; }
+    double* a_lo = a + nkg;
+    double* a_hi = a + 2 * nkg;
+    double* S_lo = S + K;
+    double* S_hi = S + 2 * K;
 
     /* Temperature softmax of every p row (j = 0..G) and q row (j < G); the
      * rows are independent, so they may be spread over threads. */
@@ -255,28 +260,38 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
     if (err) goto done;
 
     /* Ratios a = min(1, p(x)/q(x)) at every drafted token, then the expected
-     * accepted streak of every draft. */
+     * accepted streak of every draft.  lo/hi: the same ratios with p/q moved
+     * by a relative 1e-5 (exact cases -- q(x) = 0, p(x) = 0, equal
+     * log-probabilities -- stay put); they only feed the boundary band. */
     for (int k = 0; k < K; ++k) {
         for (int j = 0; j < G; ++j) {
             int32_t x = drafts[((int64_t)b * K + k) * G + j];
             double lp = sdvo_logprob(p_row(p_logits, sh, b, k, j), dtype, x, T, lse[k * nrow + j]);
             double lq = sdvo_logprob(q_row(q_logits, sh, b, k, j), dtype, x, T, lse[k * nrow + G + 1 + j]);
             a[k * G + j] = sdvo_accept_ratio(lp, lq);
+            if (lq == -INFINITY || lp == -INFINITY || lp == lq) {
+                a_lo[k * G + j] = a_hi[k * G + j] = a[k * G + j];
+            } else {
+                double r = exp(lp - lq);
+                a_lo[k * G + j] = fmin(1.0, r * (1.0 - 1e-5));
+                a_hi[k * G + j] = fmin(1.0, r * (1.0 + 1e-5));
+            }
         }
         S[k] = sdvo_streak_score(a + (size_t)k * G, G);
+        S_lo[k] = sdvo_streak_score(a_lo + (size_t)k * G, G);
+        S_hi[k] = sdvo_streak_score(a_hi + (size_t)k * G, G);
     }
     if (scores_out) memcpy(scores_out, S, sizeof(double) * (size_t)K);
     if (ratio_out && G > 0) memcpy(ratio_out, a, sizeof(double) * (size_t)K * G);
 
-    /* Self-selection: the draft with the largest expected streak. */
+    /* Self-selection: the draft with the largest expected streak.  Boundary
+     * when the perturbed scores could reorder the first maximum. */
     int sel = sdvo_argmax_first(S, K);
     int band = 0;
-    {
-        double second = -INFINITY;
-        for (int k = 0; k < K; ++k)
-            if (k != sel && S[k] > second) second = S[k];
-        double gap = S[sel] - second;
-        if (K > 1 && gap > 0.0 && gap <= 1e-5 * S[sel]) band |= SDVO_BAND_SELECT;
+    for (int k = 0; k < K; ++k) {
+        if (k == sel) continue;
+        if ((k < sel && S_hi[k] >= S_lo[sel]) || (k > sel && S_hi[k] > S_lo[sel]))
+            band |= SDVO_BAND_SELECT;
     }
 
     /* Left-to-right acceptance of the selected draft. */

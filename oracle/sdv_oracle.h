@@ -44,7 +44,8 @@ extern "C" {
  * be decided differently by a correct fp32 implementation. */
 #define SDVO_BAND_ACCEPT 1   /* |u_j - a_j| <= 1e-5 a_j at a decided position  */
 #define SDVO_BAND_CDF 2      /* |t - C_v| <= 1e-5 R at the chosen v or v-1      */
-#define SDVO_BAND_SELECT 4   /* 0 < S_best - S_second <= 1e-5 S_best            */
+#define SDVO_BAND_SELECT 4   /* moving any p/q by 1e-5 (relative) could change  */
+                             /* the first maximum of the streak scores          */
 #define SDVO_BAND_RESID 8    /* residual mass R < 1e-3 (ill-conditioned draw)   */
 
 /* Status codes of sdvo_verify / sdvo_verify_uniforms (per sequence in err[]). */

@@ -336,6 +336,7 @@ def test_q_equals_p_invariant(oracle_lib):
     out = oracle_lib.verify(P, Q, D, 1.0, seed=9)
     assert (out["accept_len"] == G).all() and (out["sel"] == 0).all()
     assert (out["scores"] == G).all() and (out["ratio"] == 1.0).all()
+    assert not (out["band"] & oracle_lib.BAND_SELECT).any()      # exact ties are not boundary
     # bonus token: exact inverse CDF of p_gamma at w_gamma, by interval
     for b in range(B):
         _, w = oracle_lib.uniforms(9, b, G)
@@ -394,6 +395,22 @@ def test_chi_square_first_token_follows_verifier(oracle_lib):
     assert stats.chisquare(obs, exp_).pvalue > 1e-3
     alpha0 = np.minimum(p0, qm[0]).sum()
     assert abs(acc0 / n_total - alpha0) < 5 * np.sqrt(alpha0 * (1 - alpha0) / n_total)
+
+
+def test_selection_band(oracle_lib):
+    """A score that rounding could lift onto the best (or past it) marks the
+    selection as boundary; a clear winner or an exact tie of exact ratios does not."""
+    V, G = 4, 2
+    p = np.zeros((1, 3, G + 1, V), np.float32)
+    q = np.zeros((1, 3, G, V), np.float32)
+    d = np.zeros((1, 3, G), np.int32)
+    # drafts 1 and 2: exact ratio 1 everywhere (q == p); draft 0: ratio 1 - 1e-8
+    q[0, 0, 0, 0] = np.float32(1e-8 * 4 / 3)
+    out = oracle_lib.verify(p, q, d, 1.0, seed=0)
+    assert out["sel"][0] == 1 and out["band"][0] & oracle_lib.BAND_SELECT
+    q[0, 0, 0, 0] = 0.5                       # a clear gap: no band
+    out = oracle_lib.verify(p, q, d, 1.0, seed=0)
+    assert out["sel"][0] == 1 and not out["band"][0] & oracle_lib.BAND_SELECT
 
 
 def test_data_errors_flagged(oracle_lib):
