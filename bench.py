@@ -39,7 +39,7 @@ from draft_verification_sdv_gb300 import synth  # noqa: E402
 METRIC = "verified draft-tokens/s and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
 UNIT = "draft-tokens/s"
 DEFAULT_WORKLOAD = 5
-ROWPASS_SOURCES = ["k1_rowpass.cu", "sdv_device.cuh", "sdv_plan.h"]
+ROWPASS_SOURCES = ["k1_rowpass.cu", "sdv_device.cuh"]
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "rowpass_large-window.md")
 
 
@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["sdv", "reference"], default="sdv")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="shrink B of the workload (profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -208,7 +210,7 @@ def run_sdv(args, rank, world, local):
     from draft_verification_sdv_gb300 import binding as bd
     bd.load(build=True)
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = synth.workload(args.workload, device=dev, seed=args.workload + 1000 * rank)
+    w = synth.workload(args.workload, device=dev, seed=args.workload + 1000 * rank, B=args.batch)
     stream = torch.cuda.Stream(device=dev)
     v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream)
     out = None

@@ -22,15 +22,35 @@
 namespace sdv {
 namespace {
 
-// Merge the `chunks` partials of one row in chunk order.
+constexpr int kBatch = 16;   // chunk partials loaded per round
+
+// Merge the `chunks` partials of two rows in chunk order.  The loads of both
+// rows go out together, kBatch at a time, so the merge chains do not wait on
+// one load at a time.
+__device__ __forceinline__ void merge_rows2(const float2* pa, const float2* pb, int chunks, float c,
+                                            float& Ma, float& Sa, float& Mb, float& Sb) {
+    Ma = Mb = -INFINITY;
+    Sa = Sb = 0.0f;
+    for (int i0 = 0; i0 < chunks; i0 += kBatch) {
+        float2 va[kBatch], vb[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const bool in = i0 + u < chunks;
+            va[u] = in ? __ldcg(pa + i0 + u) : make_float2(-INFINITY, 0.0f);
+            vb[u] = in ? __ldcg(pb + i0 + u) : make_float2(-INFINITY, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            merge_stat(Ma, Sa, va[u].x, va[u].y, c);
+            merge_stat(Mb, Sb, vb[u].x, vb[u].y, c);
+        }
+    }
+}
+
 __device__ __forceinline__ void merge_row(const float2* part, int chunks, float c, float& M,
                                           float& S) {
-    M = -INFINITY;
-    S = 0.0f;
-    for (int i = 0; i < chunks; ++i) {
-        const float2 ps = part[i];
-        merge_stat(M, S, ps.x, ps.y, c);
-    }
+    float m2, s2;
+    merge_rows2(part, part, chunks, c, M, S, m2, s2);
 }
 
 __device__ __forceinline__ bool row_valid(float M, float S) {
@@ -47,8 +67,14 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int K = a.K, G = a.G;
     const int KG = K * G;
-    float* ratio = reinterpret_cast<float*>(smem_raw);                                 // [K*G]
-    double* score = reinterpret_cast<double*>(smem_raw + ((static_cast<size_t>(KG) * 4 + 15) & ~size_t(15)));  // [K]
+    // shared memory: merged row statistics (max, sum) of every p row [K][G+1]
+    // and q row [K][G], the ratios [K][G], the scores [K]
+    float2* pstat = reinterpret_cast<float2*>(smem_raw);
+    float2* qstat = pstat + K * (G + 1);
+    float* ratio = reinterpret_cast<float*>(qstat + KG);
+    double* score = reinterpret_cast<double*>(
+        smem_raw + ((static_cast<size_t>(K) * (2 * G + 1) * 8 + static_cast<size_t>(KG) * 4 + 15) &
+                    ~size_t(15)));
     __shared__ unsigned s_bad;
     __shared__ int s_len;
     __shared__ int s_sel;
@@ -72,9 +98,17 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const int k = idx / G, j = idx - (idx / G) * G;
         const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + j;
         const int64_t rq = seq_q + static_cast<int64_t>(k) * G + j;
+        // The drafted token and its two logits are inputs: fetch them first,
+        // then the row statistics.
+        const int32_t x = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
+        const bool x_ok = x >= 0 && x < a.V;
+        const float lp = x_ok ? load_logit(a.p, rp * a.V + x, BF16) : 0.0f;
+        const float lq = x_ok ? load_logit(a.q, rq * a.V + x, BF16) : 0.0f;
         float mp, sp, mq, sq;
-        merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);
-        merge_row(a.part + (a.rows_p + rq) * a.chunks, a.chunks, c, mq, sq);
+        merge_rows2(a.part + rp * a.chunks, a.part + (a.rows_p + rq) * a.chunks, a.chunks, c, mp, sp,
+                    mq, sq);
+        pstat[k * (G + 1) + j] = make_float2(mp, sp);
+        qstat[idx] = make_float2(mq, sq);
         if (a.out_lse) {
             float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
             lse[j] = row_lse(mp, sp, c);
@@ -83,20 +117,13 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         float r = 0.0f;
         if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
             atomicOr(&s_bad, kStatusBadRow);
+        } else if (!x_ok) {
+            atomicOr(&s_bad, kStatusBadDraft);
+        } else if (lq == -INFINITY) {
+            r = 1.0f;                                           // q(x) = 0 <= p(x)
         } else {
-            const int32_t x = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
-            if (x < 0 || x >= a.V) {
-                atomicOr(&s_bad, kStatusBadDraft);
-            } else {
-                const float lp = load_logit(a.p, rp * a.V + x, BF16);
-                const float lq = load_logit(a.q, rq * a.V + x, BF16);
-                if (lq == -INFINITY) {
-                    r = 1.0f;                                   // q(x) = 0 <= p(x)
-                } else {
-                    const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
-                    r = d >= 0.0f ? 1.0f : ex2(d);              // q <= p accepts at once
-                }
-            }
+            const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
+            r = d >= 0.0f ? 1.0f : ex2(d);                      // q <= p accepts at once
         }
         ratio[idx] = r;
     }
@@ -105,6 +132,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + G;
         float mp, sp;
         merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);
+        pstat[k * (G + 1) + G] = make_float2(mp, sp);
         if (a.out_lse) a.out_lse[(static_cast<int64_t>(b) * K + k) * nrow + G] = row_lse(mp, sp, c);
         if (!row_valid(mp, sp)) atomicOr(&s_bad, kStatusBadRow);
     }
@@ -166,17 +194,15 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         t.w = uniform24(r.y);
         t.c = c;
         t.row_p = seq_p + static_cast<int64_t>(sel) * (G + 1) + L;
-        float mp, sp;
-        merge_row(a.part + t.row_p * a.chunks, a.chunks, c, mp, sp);
-        t.mp = mp;
-        t.inv_sp = 1.0f / sp;
+        const float2 ps = pstat[sel * (G + 1) + L];
+        t.mp = ps.x;
+        t.inv_sp = 1.0f / ps.y;
         if (L < G) {
             t.mode = 1;                                   // residual max(0, p - q)
             t.row_q = seq_q + static_cast<int64_t>(sel) * G + L;
-            float mq, sq;
-            merge_row(a.part + (a.rows_p + t.row_q) * a.chunks, a.chunks, c, mq, sq);
-            t.mq = mq;
-            t.inv_sq = 1.0f / sq;
+            const float2 qs = qstat[sel * G + L];
+            t.mq = qs.x;
+            t.inv_sq = 1.0f / qs.y;
         } else {
             t.mode = 2;                                   // bonus token from p_gamma
             t.row_q = -1;

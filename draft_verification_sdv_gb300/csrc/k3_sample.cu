@@ -37,14 +37,28 @@ __device__ __forceinline__ float elem(const uint4& v, int e) {
     else return __uint_as_float(w[e]);
 }
 
-// Sampling weight of element e of vector i of the slice.
+// Sampling weights of the elements of vector i of the slice: p, or the
+// residual max(0, p - q).
 template <bool BF16>
-__device__ __forceinline__ float weight(const uint4* sp, const uint4* sq, int i, int e,
-                                        bool resid, const SeqTask& t) {
-    const float pv = ex2((elem<BF16>(sp[i], e) - t.mp) * t.c) * t.inv_sp;
-    if (!resid) return pv;
-    const float qv = ex2((elem<BF16>(sq[i], e) - t.mq) * t.c) * t.inv_sq;
-    return fmaxf(pv - qv, 0.0f);
+__device__ __forceinline__ void weights(const uint4* sp, const uint4* sq, int i, bool resid,
+                                        const SeqTask& t, float (&w)[Elems<BF16>::kPerVec]) {
+    constexpr int EPV = Elems<BF16>::kPerVec;
+    const uint4 pv = sp[i];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) w[e] = ex2((elem<BF16>(pv, e) - t.mp) * t.c) * t.inv_sp;
+    if (resid) {
+        const uint4 qv = sq[i];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+            w[e] = fmaxf(w[e] - ex2((elem<BF16>(qv, e) - t.mq) * t.c) * t.inv_sq, 0.0f);
+    }
+}
+
+// Sum of the weights of one vector (pairwise tree, fixed order).
+template <int N>
+__device__ __forceinline__ float tree_sum(const float (&w)[N]) {
+    if constexpr (N == 8) return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+    else return (w[0] + w[1]) + (w[2] + w[3]);
 }
 
 template <bool BF16>
@@ -56,6 +70,8 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
     __shared__ float s_total;                      // read by the whole cluster
     __shared__ float s_ok;                         // 1 if the slice arrived
     __shared__ int s_pick, s_last_thread, s_token;
+    __shared__ float s_tot[8];                     // slice totals of the cluster
+    __shared__ int s_all_ok;
 
     constexpr int EPV = Elems<BF16>::kPerVec;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -101,11 +117,14 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
 
     for (int pass = 0; pass < 2; ++pass) {
         const bool resid = (t.mode == 1) && (pass == 0);
+        // Per-vector sums are independent; the thread sum adds them in order.
         float tsum = 0.0f;
         if (have_data)
-            for (int i = tv0; i < tv1; ++i)
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) tsum += weight<BF16>(sp, sq, i, e, resid, t);
+            for (int i = tv0; i < tv1; ++i) {
+                float w[EPV];
+                weights<BF16>(sp, sq, i, resid, t, w);
+                tsum += tree_sum(w);
+            }
 
         // Block inclusive scan of the thread sums (fixed order).
         float x = tsum;
@@ -136,16 +155,22 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         if (tid == kSampleThreads - 1) s_total = incl;
         __syncthreads();
 
-        // Slice totals of the whole cluster, in rank order.
+        // Slice totals of the whole cluster, in rank order: thread r reads
+        // rank r's total through distributed shared memory.
         cluster_sync();
-        float R = 0.0f, target_excl = 0.0f;
-        bool all_ok = true;
-        int owner = -1, last_rank = -1;
-        float tot[16];
-        for (int r = 0; r < CL; ++r) {
-            tot[r] = ld_dsmem_f32(&s_total, static_cast<uint32_t>(r));
-            if (ld_dsmem_f32(&s_ok, static_cast<uint32_t>(r)) == 0.0f) all_ok = false;
+        if (tid == 0) s_all_ok = 1;
+        __syncthreads();
+        if (tid < CL) {
+            s_tot[tid] = ld_dsmem_f32(&s_total, static_cast<uint32_t>(tid));
+            if (ld_dsmem_f32(&s_ok, static_cast<uint32_t>(tid)) == 0.0f) s_all_ok = 0;
         }
+        __syncthreads();
+        float R = 0.0f, target_excl = 0.0f;
+        const bool all_ok = s_all_ok != 0;
+        int owner = -1, last_rank = -1;
+        float tot[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) tot[r] = r < CL ? s_tot[r] : 0.0f;
         for (int r = 0; r < CL; ++r) R += tot[r];
         // Residual mass zero on this row: every CTA sees the same R, so the
         // whole cluster takes the fallback pass to p together.
@@ -181,18 +206,31 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
             int pick = s_pick;
             if (pick == kSampleThreads) pick = s_last_thread;   // rounding fallback
             if (tid == pick) {
+                // Two levels: the vector whose running sum passes the target,
+                // then the element inside it.
                 const float excl = tid > 0 ? s_incl[tid - 1] : 0.0f;
                 const float tt = tl - excl;
                 float run = 0.0f;
                 int tok = -1, last_pos = -1;
-                for (int i = tv0; i < tv1 && tok < 0; ++i)
+                for (int i = tv0; i < tv1 && tok < 0; ++i) {
+                    float w[EPV];
+                    weights<BF16>(sp, sq, i, resid, t, w);
+                    const float vs = tree_sum(w);
+                    if (run + vs > tt) {
+                        float r2 = run;
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        const float wv = weight<BF16>(sp, sq, i, e, resid, t);
-                        run += wv;
-                        if (wv > 0.0f) last_pos = i * EPV + e;
-                        if (tok < 0 && run > tt) tok = i * EPV + e;
+                        for (int e = 0; e < EPV; ++e) {
+                            r2 += w[e];
+                            if (w[e] > 0.0f) last_pos = i * EPV + e;
+                            if (tok < 0 && r2 > tt) tok = i * EPV + e;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e)
+                            if (w[e] > 0.0f) last_pos = i * EPV + e;
                     }
+                    run += vs;
+                }
                 if (tok < 0) tok = last_pos;
                 if (tok >= 0) s_token = tok;
             }
@@ -203,9 +241,12 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
                     // The picked thread held no mass: take the last id with mass.
                     const int lt = s_last_thread;
                     const int l0 = min(lt * vpt, nv), l1 = min(l0 + vpt, nv);
-                    for (int i = l0; i < l1; ++i)
+                    for (int i = l0; i < l1; ++i) {
+                        float w[EPV];
+                        weights<BF16>(sp, sq, i, resid, t, w);
                         for (int e = 0; e < EPV; ++e)
-                            if (weight<BF16>(sp, sq, i, e, resid, t) > 0.0f) tok = i * EPV + e;
+                            if (w[e] > 0.0f) tok = i * EPV + e;
+                    }
                 }
                 a.out_tok[b] = tok >= 0 ? static_cast<int32_t>(sv0 * EPV + tok) : -1;
             }

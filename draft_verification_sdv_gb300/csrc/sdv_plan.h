@@ -92,7 +92,7 @@ cudaError_t setup_sample(size_t smem);
 cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm);
 
 constexpr int kRowPassThreads = 256;
-constexpr int kSelectThreads = 256;
-constexpr int kSampleThreads = 256;
+constexpr int kSelectThreads = 512;
+constexpr int kSampleThreads = 512;
 
 }  // namespace sdv

@@ -28,7 +28,8 @@ def lib():
     """Load (building on first use) the oracle shared library."""
     global _lib
     if _lib is None:
-        path = _build.build()
+        # SDV_ORACLE_LIB lets the mutation test load a deliberately broken copy.
+        path = os.environ.get("SDV_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         u32p = ctypes.POINTER(ctypes.c_uint32)
         dp = ctypes.POINTER(ctypes.c_double)
