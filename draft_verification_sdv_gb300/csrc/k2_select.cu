@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     float2* pstat = reinterpret_cast<float2*>(smem_raw);
     float2* qstat = pstat + K * (G + 1);
     float* ratio = reinterpret_cast<float*>(qstat + KG);
-    double* score = reinterpret_cast<double*>(
+    float* score = reinterpret_cast<float*>(
         smem_raw + ((static_cast<size_t>(K) * (2 * G + 1) * 8 + static_cast<size_t>(KG) * 4 + 15) &
                     ~size_t(15)));
     __shared__ unsigned s_bad;
@@ -151,15 +151,17 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         return;
     }
 
-    // Expected accepted streak of every draft (prefix products in fp64).
+    // Expected accepted streak of every draft (fp32 prefix products: GB300's
+    // fp64 rate is a small fraction of its fp32 rate, and fp32 keeps the
+    // score well inside the selection tolerance).
     for (int k = tid; k < K; k += kSelectThreads) {
-        double prefix = 1.0, sc = 0.0;
+        float prefix = 1.0f, sc = 0.0f;
         for (int j = 0; j < G; ++j) {
-            prefix *= static_cast<double>(ratio[k * G + j]);
+            prefix *= ratio[k * G + j];
             sc += prefix;
         }
         score[k] = sc;
-        if (a.out_scores) a.out_scores[static_cast<int64_t>(b) * K + k] = static_cast<float>(sc);
+        if (a.out_scores) a.out_scores[static_cast<int64_t>(b) * K + k] = sc;
     }
     __syncthreads();
 

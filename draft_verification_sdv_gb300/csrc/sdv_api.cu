@@ -154,7 +154,7 @@ sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype d
     // Select plan.
     ctx->sel_smem = align_up(static_cast<size_t>(K) * (2 * gamma + 1) * 8 +
                                  static_cast<size_t>(K) * gamma * 4, 16) +
-                    static_cast<size_t>(K) * 8;
+                    static_cast<size_t>(K) * 4;
     // Sample plan: up to 8 CTAs per sequence, each holding a slice of one or
     // two rows in shared memory.
     int cl = 8;
