@@ -19,10 +19,11 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsdv.so")
 
-SDV_OK, SDV_ERR_ARG, SDV_ERR_CUDA, SDV_ERR_OOM, SDV_ERR_DEVICE_DATA = 0, 1, 2, 3, 4
+SDV_OK, SDV_ERR_ARG, SDV_ERR_CUDA, SDV_ERR_OOM, SDV_ERR_DEVICE_DATA, SDV_ERR_SCRATCH = 0, 1, 2, 3, 4, 5
 SDV_BF16, SDV_F32 = 0, 1
 STATUS_NAMES = {0: "SDV_OK", 1: "SDV_ERR_ARG", 2: "SDV_ERR_CUDA", 3: "SDV_ERR_OOM",
-                4: "SDV_ERR_DEVICE_DATA"}
+                4: "SDV_ERR_DEVICE_DATA", 5: "SDV_ERR_SCRATCH"}
+STATIC_SCRATCH_BYTES = 8 << 20
 
 # Every entry point of include/sdv.h, with its ctypes signature.
 _VP, _I, _I64, _U64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
@@ -39,6 +40,7 @@ SIGNATURES = {
     "sdv_set_stream": (_I, [_VP, _VP]),
     "sdv_profile_enable": (_I, [_VP, _I]),
     "sdv_profile_read": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_I)]),
+    "sdv_verify_static": (_I, [_I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
 }
 
 _lib = None
@@ -188,6 +190,19 @@ def sdv_profile_read(ctx):
     if st != SDV_OK:
         raise SdvError(st, sdv_last_error(ctx))
     return [float(x) for x in ms], n.value
+
+
+def sdv_verify_static(B, K, gamma, V, dtype, stream, p_logits, q_logits, drafts, temperature,
+                      temperature_per_seq, seed, out_sel, out_accept_len, out_next_token) -> int:
+    """Allocation-free step (no context): scratch lives in a static device array."""
+    return load().sdv_verify_static(
+        B, K, gamma, V, _dtype_code(dtype), ctypes.c_void_p(_stream_handle(stream)),
+        _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
+        _dev_ptr(drafts, torch.int32, "drafts"), float(temperature),
+        _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
+        _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
+        _dev_ptr(out_next_token, torch.int32, "out_next_token"))
 
 
 def sdv_set_stream(ctx, stream) -> int:

@@ -1,0 +1,224 @@
+// sdv_static.cu -- sdv_verify_static: the verification step for callers that
+// cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc at all: code running inside a CUDA
+// graph capture that forbids allocation, a host process whose device memory is
+// owned entirely by another allocator (a serving engine's pool), or a plug-in
+// loaded into such a process.  For them this entry point runs the same three
+// kernels as sdv_verify_ex (row pass, select/scan, sample), but their scratch
+// -- the row-pass partials, the per-sequence tasks and the status word --
+// lives in one file-scope static device array of kStaticScratchBytes, which
+// every GPU that loads this library holds until the process exits.  The
+// caller still owns and passes every input and output.
+//
+// Set-up: the first call on a device (with that device current) resolves the
+// device address of the array with cudaGetSymbolAddress; make that first call
+// before any stream capture.  No call allocates: no cudaMalloc, no cudaFree,
+// no allocating library routine.
+//
+// Every call shares the one array and leaves its contents behind; the status
+// word is cleared at the start of each call and everything else is written
+// before it is read.  Calls that overlap on the GPU (two streams, two host
+// threads) race on the array and must be serialised by the caller.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/sdv.h"
+#include "sdv_plan.h"
+
+using namespace sdv;
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+struct StaticDevice {
+    bool ready;
+    void* scratch;        // device address of g_static_scratch on this device
+    int nsm;
+    int rowpass_blocks[2];   // resident row-pass CTAs per SM: [fp32, bf16]
+    int smem_optin;          // largest dynamic shared memory a block may opt into
+};
+
+StaticDevice g_devices[kMaxDevices];
+std::mutex g_setup_mutex;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Once per device, with that device current.
+cudaError_t setup_device(int dev, StaticDevice** out) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    StaticDevice& d = g_devices[dev];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        int nsm = 0, optin = 0, bps_f32 = 0, bps_bf16 = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = rowpass_occupancy(false, &bps_f32);
+        if (e == cudaSuccess) e = rowpass_occupancy(true, &bps_bf16);
+        if (e != cudaSuccess) return e;
+        if (bps_f32 < 1 || bps_bf16 < 1 || optin <= 4096) return cudaErrorInvalidConfiguration;
+        d.scratch = ptr;
+        d.nsm = nsm;
+        d.smem_optin = optin;
+        d.rowpass_blocks[0] = bps_f32;
+        d.rowpass_blocks[1] = bps_bf16;
+        d.ready = true;
+    }
+    *out = &d;
+    return cudaSuccess;
+}
+
+// Chunks per row for the row pass: the same cost model as a context's plan,
+// limited to the chunk counts whose partials fit `max_items`.
+bool plan_static(int64_t rows, int64_t nvec, int64_t nwarps, int64_t max_items, int* chunks,
+                 int64_t* chunk_vec) {
+    const int64_t min_cv = nvec < 64 ? nvec : 64;
+    const int64_t max_c = nvec / min_cv;
+    double best = -1.0;
+    for (int64_t c = 1; c <= max_c && c <= 4096; ++c) {
+        int64_t cv = (nvec + c - 1) / c;
+        cv = (cv + 7) / 8 * 8;
+        if (cv > nvec) cv = nvec;
+        const int64_t cc = (nvec + cv - 1) / cv;
+        const int64_t items = rows * cc;
+        if (items > max_items) continue;
+        const int64_t rounds = (items + nwarps - 1) / nwarps;
+        const double cost = static_cast<double>(rounds) * static_cast<double>(cv + 16);
+        if (best < 0.0 || cost < best * (1.0 - 1e-9)) {
+            best = cost;
+            *chunks = static_cast<int>(cc);
+            *chunk_vec = cv;
+        }
+    }
+    return best >= 0.0;
+}
+
+}  // namespace
+
+extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtype dtype,
+                                        void* stream, const void* p_logits,
+                                        const void* q_logits, const int32_t* drafts,
+                                        float temperature, const float* temperature_per_seq,
+                                        uint64_t seed, int32_t* out_sel,
+                                        int32_t* out_accept_len, int32_t* out_next_token) {
+    if (B < 1 || K < 1 || gamma < 1 || V < 1) return SDV_ERR_ARG;
+    if (dtype != SDV_BF16 && dtype != SDV_F32) return SDV_ERR_ARG;
+    const int64_t elt = dtype == SDV_BF16 ? 2 : 4;
+    if ((static_cast<int64_t>(V) * elt) % 16 != 0) return SDV_ERR_ARG;
+    if (!p_logits || !q_logits || !drafts || !out_sel || !out_accept_len || !out_next_token)
+        return SDV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits)) & 15u)
+        return SDV_ERR_ARG;
+    if (!temperature_per_seq && !(std::isfinite(temperature) && temperature > 0.0f))
+        return SDV_ERR_ARG;
+
+    // Scratch layout in the static array: partials, tasks, status word.
+    const int64_t nvec = static_cast<int64_t>(V) * elt / 16;
+    const int64_t rows_p = static_cast<int64_t>(B) * K * (gamma + 1);
+    const int64_t rows_total = rows_p + static_cast<int64_t>(B) * K * gamma;
+    const size_t task_bytes = round_up(static_cast<size_t>(B) * sizeof(SeqTask), 256);
+    // Partials (rounded up to 256 bytes), tasks and the status word must fit.
+    if (task_bytes + 512 >= kStaticScratchBytes) return SDV_ERR_SCRATCH;
+    const int64_t max_items =
+        static_cast<int64_t>((kStaticScratchBytes - task_bytes - 512) / sizeof(float2));
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDV_ERR_CUDA;
+    StaticDevice* sd = nullptr;
+    if (setup_device(dev, &sd) != cudaSuccess) return SDV_ERR_CUDA;
+
+    const int bps = sd->rowpass_blocks[dtype == SDV_BF16 ? 1 : 0];
+    const int64_t nwarps = static_cast<int64_t>(sd->nsm) * bps * (kRowPassThreads / 32);
+    int chunks = 0;
+    int64_t chunk_vec = 0;
+    if (!plan_static(rows_total, nvec, nwarps, max_items, &chunks, &chunk_vec)) return SDV_ERR_SCRATCH;
+    const int64_t items = rows_total * chunks;
+    const size_t part_bytes = round_up(static_cast<size_t>(items) * sizeof(float2), 256);
+    unsigned char* base = static_cast<unsigned char*>(sd->scratch);
+    float2* part = reinterpret_cast<float2*>(base);
+    SeqTask* tasks = reinterpret_cast<SeqTask*>(base + part_bytes);
+    unsigned* status = reinterpret_cast<unsigned*>(base + part_bytes + task_bytes);
+
+    int cl = 8;
+    while (cl > 1 && cl > nvec) cl >>= 1;
+    const int64_t slice_vec = (nvec + cl - 1) / cl;
+    const size_t sel_smem = round_up(static_cast<size_t>(K) * (2 * gamma + 1) * 8 +
+                                         static_cast<size_t>(K) * gamma * 4, 16) +
+                            static_cast<size_t>(K) * 4;
+    const size_t smp_smem = static_cast<size_t>(2) * slice_vec * 16;
+    if (sel_smem > static_cast<size_t>(sd->smem_optin) - 4096 ||
+        smp_smem > static_cast<size_t>(sd->smem_optin) - 4096)
+        return SDV_ERR_ARG;
+    // Let both kernels take up to the device's opt-in limit (raising the
+    // limit never disturbs a launch that asks for less).
+    if (setup_select(static_cast<size_t>(sd->smem_optin) - 4096) != cudaSuccess ||
+        setup_sample(static_cast<size_t>(sd->smem_optin) - 4096) != cudaSuccess)
+        return SDV_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return SDV_ERR_CUDA;
+
+    RowPassArgs ra;
+    ra.p = p_logits;
+    ra.q = q_logits;
+    ra.part = part;
+    ra.temps = temperature_per_seq;
+    ra.temperature = temperature;
+    ra.K = K;
+    ra.G = gamma;
+    ra.chunks = chunks;
+    ra.rows_p = rows_p;
+    ra.rows_total = rows_total;
+    ra.nvec = nvec;
+    ra.chunk_vec = chunk_vec;
+    ra.items = items;
+    const int64_t full_grid = static_cast<int64_t>(sd->nsm) * bps;
+    const int64_t blocks_needed = (items + (kRowPassThreads / 32) - 1) / (kRowPassThreads / 32);
+    const int grid = static_cast<int>(blocks_needed < full_grid ? blocks_needed : full_grid);
+    if (launch_rowpass(ra, dtype == SDV_BF16, grid, s) != cudaSuccess) return SDV_ERR_CUDA;
+
+    SelectArgs sa;
+    sa.p = p_logits;
+    sa.q = q_logits;
+    sa.drafts = drafts;
+    sa.part = part;
+    sa.temps = temperature_per_seq;
+    sa.temperature = temperature;
+    sa.B = B;
+    sa.K = K;
+    sa.G = gamma;
+    sa.V = V;
+    sa.chunks = chunks;
+    sa.rows_p = rows_p;
+    sa.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
+    sa.seed_hi = static_cast<uint32_t>(seed >> 32);
+    sa.out_sel = out_sel;
+    sa.out_len = out_accept_len;
+    sa.out_tok = out_next_token;
+    sa.out_scores = nullptr;
+    sa.out_lse = nullptr;
+    sa.tasks = tasks;
+    sa.status = status;
+    if (launch_select(sa, dtype == SDV_BF16, sel_smem, s) != cudaSuccess) return SDV_ERR_CUDA;
+
+    SampleArgs ma;
+    ma.p = p_logits;
+    ma.q = q_logits;
+    ma.tasks = tasks;
+    ma.out_tok = out_next_token;
+    ma.status = status;
+    ma.nvec = nvec;
+    ma.slice_vec = slice_vec;
+    ma.cluster = cl;
+    if (launch_sample(ma, dtype == SDV_BF16, B, cl, smp_smem, s) != cudaSuccess) return SDV_ERR_CUDA;
+    return SDV_OK;
+}

@@ -71,7 +71,9 @@ typedef enum {
     SDV_ERR_CUDA = 2,         /* a CUDA runtime call failed, or a device wait    */
                               /* gave up after its iteration limit               */
     SDV_ERR_OOM = 3,          /* workspace allocation failed                     */
-    SDV_ERR_DEVICE_DATA = 4   /* bad draft id / non-finite row / bad per-seq T   */
+    SDV_ERR_DEVICE_DATA = 4,  /* bad draft id / non-finite row / bad per-seq T   */
+    SDV_ERR_SCRATCH = 5       /* sdv_verify_static: the shape needs more scratch */
+                              /* than SDV_STATIC_SCRATCH_BYTES                   */
 } sdv_status;
 
 typedef enum { SDV_BF16 = 0, SDV_F32 = 1 } sdv_dtype;
@@ -160,6 +162,50 @@ sdv_status sdv_set_stream(sdv_ctx* ctx, void* stream);
  */
 sdv_status sdv_profile_enable(sdv_ctx* ctx, int enable);
 sdv_status sdv_profile_read(sdv_ctx* ctx, float* ms_avg, int* steps);
+
+/*
+ * sdv_verify_static -- the step of sdv_verify_ex for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry point:
+ * it exists for deployment, not for the method.
+ *
+ * Who needs it: code that must not call cudaMalloc -- work recorded into a
+ * CUDA graph or run where allocation is forbidden, a process whose device
+ * memory belongs entirely to another allocator (a serving engine's pool), a
+ * plug-in loaded into such a process.  sdv_create allocates a workspace; this
+ * call does not.  It takes no context and allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library routine.
+ *
+ * Scratch: the row-pass partials, per-sequence tasks and status word live in
+ * one static device array of SDV_STATIC_SCRATCH_BYTES (8 MiB), which every GPU
+ * that loads libsdv holds until the process exits.  A shape whose scratch does
+ * not fit is rejected with SDV_ERR_SCRATCH before anything is enqueued (as a
+ * guide: partials take 8 bytes per row chunk, at least one chunk per row, so
+ * B*K*(2*gamma+1) must stay below about one million rows).
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * device address of the array (cudaGetSymbolAddress) and the device's limits.
+ * Make that first call before any stream capture.
+ *
+ * Arguments: as sdv_verify_ex, with the shape (B, K, gamma, V, dtype) and the
+ * stream (a cudaStream_t, NULL = legacy default stream) passed on every call;
+ * all tensors are caller-owned device memory.  Outputs are the same values
+ * sdv_verify_ex writes.  Argument errors return SDV_ERR_ARG and nothing is
+ * enqueued.  The call only enqueues; there is no sdv_sync for it: a sequence
+ * with bad data (draft id out of range, non-finite row, bad per-sequence
+ * temperature) gets -1 in all three outputs.
+ *
+ * Sharing: every call uses the same array and leaves its contents behind (the
+ * status word is cleared at the start of each call; the rest is written before
+ * it is read).  Calls that overlap on the GPU -- on two streams or from two
+ * host threads -- race on the array; the caller must serialise them.
+ */
+#define SDV_STATIC_SCRATCH_BYTES (8u << 20)
+sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtype dtype, void* stream,
+                             const void* p_logits, const void* q_logits,
+                             const int32_t* drafts, float temperature,
+                             const float* temperature_per_seq, uint64_t seed,
+                             int32_t* out_sel, int32_t* out_accept_len,
+                             int32_t* out_next_token);
 
 #ifdef __cplusplus
 }
