@@ -10,8 +10,10 @@
 // `chunk_vec` 16-byte vectors.  One warp reduces one (row, chunk) item to
 // (m, s) = (max l, sum 2^{(l - m) c}), c = log2(e) / T, with a fixed lane
 // mapping and a fixed reduction tree, so two rows with the same bytes and the
-// same temperature give bit-identical partials whatever their position.  A
-// persistent grid of warps takes items round-robin.
+// same temperature give bit-identical partials whatever their position.  The
+// grid holds one CTA per eight items and runs in many waves: the hardware
+// hands each freed slot the next CTA, which keeps every SM streaming until
+// the end (measured faster than a persistent grid with a static order).
 //
 // The kernel is HBM-bandwidth bound: per element one 2-byte load, one
 // exponential on the special-function unit and a handful of fp32 operations.
@@ -81,13 +83,15 @@ __device__ __forceinline__ float vec_sum(const uint4& v, float m, float c) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassArgs a) {
+    // Let the select kernel launch now: it waits for this grid before it
+    // reads any partial.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kRowPassThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kRowPassThreads) >> 5;
+    const int64_t item = (static_cast<int64_t>(blockIdx.x) * kRowPassThreads + threadIdx.x) >> 5;
     const int64_t rows_per_seq_p = static_cast<int64_t>(a.K) * (a.G + 1);
     const int64_t rows_per_seq_q = static_cast<int64_t>(a.K) * a.G;
 
-    for (int64_t item = warp; item < a.items; item += nwarps) {
+    if (item < a.items) {
         const int64_t row = item / a.chunks;
         const int64_t chunk = item - row * a.chunks;
         const int64_t v0 = chunk * a.chunk_vec;
@@ -147,7 +151,11 @@ cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm) {
                       blocks_per_sm, rowpass_kernel<false>, kRowPassThreads, 0);
 }
 
-cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, int grid, cudaStream_t s) {
+cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, cudaStream_t s) {
+    constexpr int64_t per_cta = kRowPassThreads / 32;
+    const int64_t g = (a.items + per_cta - 1) / per_cta;
+    if (g < 1 || g > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const int grid = static_cast<int>(g);
     if (bf16)
         rowpass_kernel<true><<<grid, kRowPassThreads, 0, s>>>(a);
     else

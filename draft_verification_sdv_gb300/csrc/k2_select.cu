@@ -93,17 +93,38 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     const int64_t seq_q = static_cast<int64_t>(b) * K * G;         // first q row of b
     const int nrow = 2 * G + 1;
 
+    // The drafted token of this thread's first pair and its two logits are
+    // inputs of the step, not results of the row pass: fetch them before
+    // waiting for the row pass to finish.
+    int32_t x0 = 0;
+    float lp0 = 0.0f, lq0 = 0.0f;
+    if (tid < KG) {
+        const int k = tid / G, j = tid - (tid / G) * G;
+        x0 = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
+        if (x0 >= 0 && x0 < a.V) {
+            lp0 = load_logit(a.p, (seq_p + static_cast<int64_t>(k) * (G + 1) + j) * a.V + x0, BF16);
+            lq0 = load_logit(a.q, (seq_q + static_cast<int64_t>(k) * G + j) * a.V + x0, BF16);
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Let the sample kernel launch: it waits for this grid before reading.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // Acceptance ratio at every drafted token of every draft.
     for (int idx = tid; idx < KG; idx += kSelectThreads) {
         const int k = idx / G, j = idx - (idx / G) * G;
         const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + j;
         const int64_t rq = seq_q + static_cast<int64_t>(k) * G + j;
-        // The drafted token and its two logits are inputs: fetch them first,
-        // then the row statistics.
-        const int32_t x = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
+        int32_t x = x0;
+        float lp = lp0, lq = lq0;
+        if (idx != tid) {
+            x = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
+            if (x >= 0 && x < a.V) {
+                lp = load_logit(a.p, rp * a.V + x, BF16);
+                lq = load_logit(a.q, rq * a.V + x, BF16);
+            }
+        }
         const bool x_ok = x >= 0 && x < a.V;
-        const float lp = x_ok ? load_logit(a.p, rp * a.V + x, BF16) : 0.0f;
-        const float lq = x_ok ? load_logit(a.q, rq * a.V + x, BF16) : 0.0f;
         float mp, sp, mq, sq;
         merge_rows2(a.part + rp * a.chunks, a.part + (a.rows_p + rq) * a.chunks, a.chunks, c, mp, sp,
                     mq, sq);
@@ -223,12 +244,19 @@ cudaError_t setup_select(size_t smem) {
                                 static_cast<int>(smem));
 }
 
-cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s) {
-    if (bf16)
-        select_kernel<true><<<a.B, kSelectThreads, smem, s>>>(a);
-    else
-        select_kernel<false><<<a.B, kSelectThreads, smem, s>>>(a);
-    return cudaGetLastError();
+cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B));
+    cfg.blockDim = dim3(kSelectThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (bf16) return cudaLaunchKernelEx(&cfg, select_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, select_kernel<false>, a);
 }
 
 }  // namespace sdv

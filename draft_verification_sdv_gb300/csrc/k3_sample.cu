@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
     const uint32_t rank = cluster_rank();
     const int CL = a.cluster;
     const int64_t b = blockIdx.x / CL;
+    // The tasks are written by the select kernel: wait for it to finish.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const SeqTask t = a.tasks[b];
     const int64_t sv0 = static_cast<int64_t>(rank) * a.slice_vec;
     const int64_t sv1 = sv0 + a.slice_vec < a.nvec ? sv0 + a.slice_vec : a.nvec;
@@ -269,19 +271,21 @@ cudaError_t setup_sample(size_t smem) {
 }
 
 cudaError_t launch_sample(const SampleArgs& a, bool bf16, int B, int cluster, size_t smem,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(B * cluster));
     cfg.blockDim = dim3(kSampleThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     if (bf16) return cudaLaunchKernelEx(&cfg, sample_kernel<true>, a);
     return cudaLaunchKernelEx(&cfg, sample_kernel<false>, a);
 }

@@ -68,34 +68,6 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kMaxProfSteps = 65536;
 
-// Chunking of the row pass: choose the number of chunks per row that
-// minimises (rounds of items over all warps) x (vectors per item + a small
-// per-item cost), with chunks of at least 64 vectors aligned to 8 vectors
-// (128 bytes).
-void plan_chunks(int64_t rows, int64_t nvec, int64_t nwarps, int* chunks_out, int64_t* cv_out) {
-    const int64_t min_cv = nvec < 64 ? nvec : 64;
-    int best_c = 1;
-    int64_t best_cv = nvec;
-    double best_cost = 1e300;
-    const int64_t max_c = nvec / min_cv;
-    for (int64_t c = 1; c <= max_c && c <= 4096; ++c) {
-        int64_t cv = (nvec + c - 1) / c;
-        cv = (cv + 7) / 8 * 8;
-        if (cv > nvec) cv = nvec;
-        const int64_t cc = (nvec + cv - 1) / cv;
-        const int64_t items = rows * cc;
-        const int64_t rounds = (items + nwarps - 1) / nwarps;
-        const double cost = static_cast<double>(rounds) * static_cast<double>(cv + 16);
-        if (cost < best_cost * (1.0 - 1e-9)) {
-            best_cost = cost;
-            best_c = static_cast<int>(cc);
-            best_cv = cv;
-        }
-    }
-    *chunks_out = best_c;
-    *cv_out = best_cv;
-}
-
 bool is_device_ptr(const void* p) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -117,7 +89,7 @@ sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype d
     if (dtype != SDV_BF16 && dtype != SDV_F32) return SDV_ERR_ARG;
     const size_t elt = elt_size(dtype);
     if ((static_cast<size_t>(V) * elt) % 16 != 0) return SDV_ERR_ARG;
-    if (static_cast<int64_t>(B) * K * (2 * gamma + 1) > (int64_t(1) << 40)) return SDV_ERR_ARG;
+    if (static_cast<int64_t>(B) * K * (2 * gamma + 1) > (int64_t(1) << 27)) return SDV_ERR_ARG;
 
     sdv_ctx* ctx = new (std::nothrow) sdv_ctx();
     if (!ctx) return SDV_ERR_OOM;
@@ -144,12 +116,10 @@ sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype d
     ctx->rows_p = static_cast<int64_t>(B) * K * (gamma + 1);
     ctx->rows_q = static_cast<int64_t>(B) * K * gamma;
     ctx->rows_total = ctx->rows_p + ctx->rows_q;
-    const int64_t full_grid = static_cast<int64_t>(ctx->nsm) * bps;
-    const int64_t nwarps_full = full_grid * (kRowPassThreads / 32);
-    plan_chunks(ctx->rows_total, ctx->nvec, nwarps_full, &ctx->chunks, &ctx->chunk_vec);
+    const int64_t resident_warps = static_cast<int64_t>(ctx->nsm) * bps * (kRowPassThreads / 32);
+    plan_rowpass_chunks(ctx->rows_total, ctx->nvec, resident_warps, 0, &ctx->chunks, &ctx->chunk_vec);
     ctx->items = ctx->rows_total * ctx->chunks;
-    const int64_t blocks_needed = (ctx->items + (kRowPassThreads / 32) - 1) / (kRowPassThreads / 32);
-    ctx->rp_grid = static_cast<int>(blocks_needed < full_grid ? blocks_needed : full_grid);
+    ctx->rp_grid = static_cast<int>((ctx->items + (kRowPassThreads / 32) - 1) / (kRowPassThreads / 32));
 
     // Select plan.
     ctx->sel_smem = align_up(static_cast<size_t>(K) * (2 * gamma + 1) * 8 +
@@ -251,7 +221,7 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
         ++ctx->prof_n;
     }
     if (ev) cudaEventRecord(ev[0], ctx->stream);
-    cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->rp_grid, ctx->stream);
+    cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "row pass launch");
     if (ev) cudaEventRecord(ev[1], ctx->stream);
 
@@ -277,7 +247,7 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     sa.out_lse = out_lse;
     sa.tasks = ctx->tasks;
     sa.status = ctx->status;
-    e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream);
+    e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "select launch");
     if (ev) cudaEventRecord(ev[2], ctx->stream);
 
@@ -290,7 +260,7 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     ma.nvec = ctx->nvec;
     ma.slice_vec = ctx->slice_vec;
     ma.cluster = ctx->cluster;
-    e = launch_sample(ma, ctx->bf16, ctx->B, ctx->cluster, ctx->smp_smem, ctx->stream);
+    e = launch_sample(ma, ctx->bf16, ctx->B, ctx->cluster, ctx->smp_smem, ctx->stream, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "sample launch");
     if (ev) cudaEventRecord(ev[3], ctx->stream);
     return SDV_OK;

@@ -31,7 +31,8 @@ struct SeqTask {
 
 // Row pass (K1): rows are split into `chunks` fixed chunks of `chunk_vec`
 // 16-byte vectors (the last chunk of a row may be shorter); one warp reduces
-// one (row, chunk) item to a partial (max, sum of 2^{(l - max) c}).
+// one (row, chunk) item to a partial (max, sum of 2^{(l - max) c}).  Launched
+// with one CTA per kRowPassThreads / 32 items.
 struct RowPassArgs {
     const void* p;          // [rows_p][V]
     const void* q;          // [rows_q][V]
@@ -81,10 +82,14 @@ struct SampleArgs {
 
 // Launchers (defined next to their kernels).  `bf16` selects the element type
 // (bf16 when true, fp32 otherwise).  Each returns the launch's error code.
-cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, int grid, cudaStream_t s);
-cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s);
+// The select and sample kernels are launched as programmatic dependents of
+// the kernel before them on the stream: they may start while it finishes and
+// wait (griddepcontrol.wait) before reading its results; `pdl` = false
+// launches them as ordinary stream-ordered kernels.
+cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_sample(const SampleArgs& a, bool bf16, int B, int cluster, size_t smem,
-                          cudaStream_t s);
+                          cudaStream_t s, bool pdl);
 // Per-kernel set-up (shared-memory opt-in), once per device.
 cudaError_t setup_select(size_t smem);
 cudaError_t setup_sample(size_t smem);
@@ -92,6 +97,34 @@ cudaError_t setup_sample(size_t smem);
 cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm);
 
 constexpr int kRowPassThreads = 256;
+
+// Row-pass chunking.  One warp reduces one (row, chunk) item and the grid is
+// one CTA per kRowPassThreads / 32 items, scheduled by the hardware in many
+// waves (that balances SMs whose bandwidth differs; a persistent grid with a
+// static item order does not).  Chunks target kChunkTargetVec vectors
+// (76 KB of bf16), are split further until there are at least
+// kMinItemWaves waves of resident warps, stay >= 64 vectors, and are rounded
+// to 8 vectors (128 bytes).  Chunks are fixed per row, so rows with the same
+// bytes give bit-identical partials wherever they sit.
+constexpr int64_t kChunkTargetVec = 4752;
+constexpr int64_t kMinItemWaves = 4;
+
+inline void plan_rowpass_chunks(int64_t rows, int64_t nvec, int64_t resident_warps,
+                                int64_t max_items, int* chunks, int64_t* chunk_vec) {
+    int64_t c = (nvec + kChunkTargetVec - 1) / kChunkTargetVec;
+    const int64_t want = (kMinItemWaves * resident_warps + rows - 1) / rows;
+    if (want > c) c = want;
+    const int64_t cmax = nvec >= 64 ? nvec / 64 : 1;
+    if (c > cmax) c = cmax;
+    if (c < 1) c = 1;
+    if (max_items > 0 && rows * c > max_items) c = max_items / rows;
+    if (c < 1) c = 1;
+    int64_t cv = (nvec + c - 1) / c;
+    cv = (cv + 7) / 8 * 8;
+    if (cv > nvec) cv = nvec;
+    *chunk_vec = cv;
+    *chunks = static_cast<int>((nvec + cv - 1) / cv);
+}
 constexpr int kSelectThreads = 512;
 constexpr int kSampleThreads = 512;
 

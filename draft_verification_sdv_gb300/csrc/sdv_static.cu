@@ -77,31 +77,6 @@ cudaError_t setup_device(int dev, StaticDevice** out) {
     return cudaSuccess;
 }
 
-// Chunks per row for the row pass: the same cost model as a context's plan,
-// limited to the chunk counts whose partials fit `max_items`.
-bool plan_static(int64_t rows, int64_t nvec, int64_t nwarps, int64_t max_items, int* chunks,
-                 int64_t* chunk_vec) {
-    const int64_t min_cv = nvec < 64 ? nvec : 64;
-    const int64_t max_c = nvec / min_cv;
-    double best = -1.0;
-    for (int64_t c = 1; c <= max_c && c <= 4096; ++c) {
-        int64_t cv = (nvec + c - 1) / c;
-        cv = (cv + 7) / 8 * 8;
-        if (cv > nvec) cv = nvec;
-        const int64_t cc = (nvec + cv - 1) / cv;
-        const int64_t items = rows * cc;
-        if (items > max_items) continue;
-        const int64_t rounds = (items + nwarps - 1) / nwarps;
-        const double cost = static_cast<double>(rounds) * static_cast<double>(cv + 16);
-        if (best < 0.0 || cost < best * (1.0 - 1e-9)) {
-            best = cost;
-            *chunks = static_cast<int>(cc);
-            *chunk_vec = cv;
-        }
-    }
-    return best >= 0.0;
-}
-
 }  // namespace
 
 extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtype dtype,
@@ -137,11 +112,13 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     if (setup_device(dev, &sd) != cudaSuccess) return SDV_ERR_CUDA;
 
     const int bps = sd->rowpass_blocks[dtype == SDV_BF16 ? 1 : 0];
-    const int64_t nwarps = static_cast<int64_t>(sd->nsm) * bps * (kRowPassThreads / 32);
+    const int64_t resident_warps = static_cast<int64_t>(sd->nsm) * bps * (kRowPassThreads / 32);
+    if (rows_total > max_items) return SDV_ERR_SCRATCH;
     int chunks = 0;
     int64_t chunk_vec = 0;
-    if (!plan_static(rows_total, nvec, nwarps, max_items, &chunks, &chunk_vec)) return SDV_ERR_SCRATCH;
+    plan_rowpass_chunks(rows_total, nvec, resident_warps, max_items, &chunks, &chunk_vec);
     const int64_t items = rows_total * chunks;
+    if (items > max_items) return SDV_ERR_SCRATCH;
     const size_t part_bytes = round_up(static_cast<size_t>(items) * sizeof(float2), 256);
     unsigned char* base = static_cast<unsigned char*>(sd->scratch);
     float2* part = reinterpret_cast<float2*>(base);
@@ -181,10 +158,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     ra.nvec = nvec;
     ra.chunk_vec = chunk_vec;
     ra.items = items;
-    const int64_t full_grid = static_cast<int64_t>(sd->nsm) * bps;
-    const int64_t blocks_needed = (items + (kRowPassThreads / 32) - 1) / (kRowPassThreads / 32);
-    const int grid = static_cast<int>(blocks_needed < full_grid ? blocks_needed : full_grid);
-    if (launch_rowpass(ra, dtype == SDV_BF16, grid, s) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_rowpass(ra, dtype == SDV_BF16, s) != cudaSuccess) return SDV_ERR_CUDA;
 
     SelectArgs sa;
     sa.p = p_logits;
@@ -208,7 +182,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     sa.out_lse = nullptr;
     sa.tasks = tasks;
     sa.status = status;
-    if (launch_select(sa, dtype == SDV_BF16, sel_smem, s) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_select(sa, dtype == SDV_BF16, sel_smem, s, true) != cudaSuccess) return SDV_ERR_CUDA;
 
     SampleArgs ma;
     ma.p = p_logits;
@@ -219,6 +193,6 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     ma.nvec = nvec;
     ma.slice_vec = slice_vec;
     ma.cluster = cl;
-    if (launch_sample(ma, dtype == SDV_BF16, B, cl, smp_smem, s) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_sample(ma, dtype == SDV_BF16, B, cl, smp_smem, s, true) != cudaSuccess) return SDV_ERR_CUDA;
     return SDV_OK;
 }
