@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["sdv", "reference"], default="sdv")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--shared-q", action="store_true",
+                    help="drafts from one pass's marginals: q is [B, gamma, V] (large-window shape)")
     ap.add_argument("--batch", type=int, default=None,
                     help="shrink B of the workload (profiling captures only)")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -195,7 +197,7 @@ def step_bytes(w: synth.Workload, accept_len) -> dict:
     """Algorithmic bytes of one step: every logit row once, the re-read rows
     of the draw (two for a residual, one for a bonus), drafts, outputs."""
     elt = 2 if w.dtype == torch.bfloat16 else 4
-    rows = w.B * w.K * (2 * w.gamma + 1)
+    rows = w.B * w.K * (w.gamma + 1) + (w.B if w.shared_q else w.B * w.K) * w.gamma
     reread = sum(2 if int(L) < w.gamma else 1 for L in accept_len)
     k1 = elt * w.V * rows
     total = k1 + elt * w.V * reread + w.B * w.K * w.gamma * 4 + w.B * 12
@@ -210,9 +212,12 @@ def run_sdv(args, rank, world, local):
     from draft_verification_sdv_gb300 import binding as bd
     bd.load(build=True)
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = synth.workload(args.workload, device=dev, seed=args.workload + 1000 * rank, B=args.batch)
+    if args.shared_q:
+        w = synth.workload_shared(B=args.batch or 32, device=dev, seed=55 + 1000 * rank)
+    else:
+        w = synth.workload(args.workload, device=dev, seed=args.workload + 1000 * rank, B=args.batch)
     stream = torch.cuda.Stream(device=dev)
-    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream)
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q)
     out = None
 
     def step():
@@ -292,6 +297,7 @@ def run_sdv(args, rank, world, local):
         "input_dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded logits and drafts; no model weights)",
         "config": {"workload": w.name, "B": w.B, "K": w.K, "gamma": w.gamma, "V": w.V,
+                   "q_layout": "[B,gamma,V] shared by the K drafts" if w.shared_q else "[B,K,gamma,V]",
                    "temperatures": "per-sequence {0.6, 1.0}" if w.temps is not None else w.temperature,
                    "l2": "inputs %.2f GB > L2 (126 MB): no flush" % (sb["k1"] / 1e9),
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "1 GPU"},

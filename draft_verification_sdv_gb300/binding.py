@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(HERE, "libsdv.so")
 
 SDV_OK, SDV_ERR_ARG, SDV_ERR_CUDA, SDV_ERR_OOM, SDV_ERR_DEVICE_DATA, SDV_ERR_SCRATCH = 0, 1, 2, 3, 4, 5
 SDV_BF16, SDV_F32 = 0, 1
+SDV_FLAG_SHARED_Q = 1
 STATUS_NAMES = {0: "SDV_OK", 1: "SDV_ERR_ARG", 2: "SDV_ERR_CUDA", 3: "SDV_ERR_OOM",
                 4: "SDV_ERR_DEVICE_DATA", 5: "SDV_ERR_SCRATCH"}
 STATIC_SCRATCH_BYTES = 8 << 20
@@ -29,6 +30,7 @@ STATIC_SCRATCH_BYTES = 8 << 20
 _VP, _I, _I64, _U64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
 SIGNATURES = {
     "sdv_create": (_I, [ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _VP]),
+    "sdv_create_ex": (_I, [ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _VP, ctypes.c_uint]),
     "sdv_verify": (_I, [_VP, _VP, _VP, _VP, _F, _U64, _VP, _VP, _VP]),
     "sdv_verify_ex": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP, _VP]),
     "sdv_verify_host": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
@@ -113,10 +115,10 @@ def _stream_handle(stream) -> Optional[int]:
 
 
 def sdv_create(B: int, K: int, gamma: int, V: int, dtype: torch.dtype = torch.bfloat16,
-               stream=None) -> ctypes.c_void_p:
+               stream=None, flags: int = 0) -> ctypes.c_void_p:
     ctx = ctypes.c_void_p()
-    st = load().sdv_create(ctypes.byref(ctx), B, K, gamma, V, _dtype_code(dtype),
-                           ctypes.c_void_p(_stream_handle(stream)))
+    st = load().sdv_create_ex(ctypes.byref(ctx), B, K, gamma, V, _dtype_code(dtype),
+                              ctypes.c_void_p(_stream_handle(stream)), int(flags))
     if st != SDV_OK:
         raise SdvError(st, "sdv_create(B=%d, K=%d, gamma=%d, V=%d)" % (B, K, gamma, V))
     return ctx
@@ -217,20 +219,23 @@ class Verifier:
     """
 
     def __init__(self, B: int, K: int, gamma: int, V: int, dtype=torch.bfloat16,
-                 device=None, stream=None):
+                 device=None, stream=None, shared_q: bool = False):
         self.B, self.K, self.gamma, self.V, self.dtype = B, K, gamma, V, dtype
+        self.shared_q = shared_q
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
             else torch.device(device)
         with torch.cuda.device(self.device):
             self.stream = stream
-            self.ctx = sdv_create(B, K, gamma, V, dtype, stream)
+            self.ctx = sdv_create(B, K, gamma, V, dtype, stream,
+                                  SDV_FLAG_SHARED_Q if shared_q else 0)
 
     def __call__(self, p_logits, q_logits, drafts, temperature: float = 1.0, seed: int = 0,
                  temps: Optional[torch.Tensor] = None, scores: bool = False, lse: bool = False,
                  out: Optional[dict] = None) -> dict:
         B, K, G, V = self.B, self.K, self.gamma, self.V
-        if tuple(p_logits.shape) != (B, K, G + 1, V) or tuple(q_logits.shape) != (B, K, G, V):
-            raise ValueError("logits must be [B,K,gamma+1,V] and [B,K,gamma,V]")
+        q_shape = (B, G, V) if self.shared_q else (B, K, G, V)
+        if tuple(p_logits.shape) != (B, K, G + 1, V) or tuple(q_logits.shape) != q_shape:
+            raise ValueError("logits must be [B,K,gamma+1,V] and %s" % (list(q_shape),))
         if tuple(drafts.shape) != (B, K, G):
             raise ValueError("drafts must be [B,K,gamma]")
         if p_logits.dtype != self.dtype or q_logits.dtype != self.dtype:

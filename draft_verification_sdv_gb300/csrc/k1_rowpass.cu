@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassA
     const int lane = threadIdx.x & 31;
     const int64_t item = (static_cast<int64_t>(blockIdx.x) * kRowPassThreads + threadIdx.x) >> 5;
     const int64_t rows_per_seq_p = static_cast<int64_t>(a.K) * (a.G + 1);
-    const int64_t rows_per_seq_q = static_cast<int64_t>(a.K) * a.G;
+    const int64_t rows_per_seq_q = (a.flags & kFlagSharedQ) ? a.G : static_cast<int64_t>(a.K) * a.G;
 
     if (item < a.items) {
         const int64_t row = item / a.chunks;

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     __syncthreads();
 
     const int64_t seq_p = static_cast<int64_t>(b) * K * (G + 1);   // first p row of b
-    const int64_t seq_q = static_cast<int64_t>(b) * K * G;         // first q row of b
+    const int64_t seq_d = static_cast<int64_t>(b) * K * G;         // first draft of b
     const int nrow = 2 * G + 1;
 
     // The drafted token of this thread's first pair and its two logits are
@@ -100,10 +100,10 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     float lp0 = 0.0f, lq0 = 0.0f;
     if (tid < KG) {
         const int k = tid / G, j = tid - (tid / G) * G;
-        x0 = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
+        x0 = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
         if (x0 >= 0 && x0 < a.V) {
             lp0 = load_logit(a.p, (seq_p + static_cast<int64_t>(k) * (G + 1) + j) * a.V + x0, BF16);
-            lq0 = load_logit(a.q, (seq_q + static_cast<int64_t>(k) * G + j) * a.V + x0, BF16);
+            lq0 = load_logit(a.q, q_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
         }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -114,11 +114,11 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     for (int idx = tid; idx < KG; idx += kSelectThreads) {
         const int k = idx / G, j = idx - (idx / G) * G;
         const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + j;
-        const int64_t rq = seq_q + static_cast<int64_t>(k) * G + j;
+        const int64_t rq = q_row_index(a.flags, b, k, j, K, G);
         int32_t x = x0;
         float lp = lp0, lq = lq0;
         if (idx != tid) {
-            x = a.drafts[seq_q + static_cast<int64_t>(k) * G + j];
+            x = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
             if (x >= 0 && x < a.V) {
                 lp = load_logit(a.p, rp * a.V + x, BF16);
                 lq = load_logit(a.q, rq * a.V + x, BF16);
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         t.inv_sp = 1.0f / ps.y;
         if (L < G) {
             t.mode = 1;                                   // residual max(0, p - q)
-            t.row_q = seq_q + static_cast<int64_t>(sel) * G + L;
+            t.row_q = q_row_index(a.flags, b, sel, L, K, G);
             const float2 qs = qstat[sel * G + L];
             t.mq = qs.x;
             t.inv_sq = 1.0f / qs.y;

@@ -14,6 +14,7 @@ using namespace sdv;
 
 struct sdv_ctx {
     int B, K, G, V;
+    unsigned flags;
     sdv_dtype dtype;
     bool bf16;
     cudaStream_t stream;
@@ -83,8 +84,14 @@ extern "C" {
 
 sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype dtype,
                       void* stream) {
+    return sdv_create_ex(out, B, K, gamma, V, dtype, stream, 0u);
+}
+
+sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype dtype,
+                         void* stream, unsigned flags) {
     if (!out) return SDV_ERR_ARG;
     *out = nullptr;
+    if (flags & ~static_cast<unsigned>(SDV_FLAG_SHARED_Q)) return SDV_ERR_ARG;
     if (B < 1 || K < 1 || gamma < 1 || V < 1) return SDV_ERR_ARG;
     if (dtype != SDV_BF16 && dtype != SDV_F32) return SDV_ERR_ARG;
     const size_t elt = elt_size(dtype);
@@ -98,6 +105,7 @@ sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype d
     ctx->G = gamma;
     ctx->V = V;
     ctx->dtype = dtype;
+    ctx->flags = flags;
     ctx->bf16 = dtype == SDV_BF16;
     ctx->stream = static_cast<cudaStream_t>(stream);
     ctx->err[0] = 0;
@@ -114,7 +122,8 @@ sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtype d
     // Row pass plan.
     ctx->nvec = static_cast<int64_t>(V) * static_cast<int64_t>(elt) / 16;
     ctx->rows_p = static_cast<int64_t>(B) * K * (gamma + 1);
-    ctx->rows_q = static_cast<int64_t>(B) * K * gamma;
+    ctx->rows_q = (flags & SDV_FLAG_SHARED_Q) ? static_cast<int64_t>(B) * gamma
+                                              : static_cast<int64_t>(B) * K * gamma;
     ctx->rows_total = ctx->rows_p + ctx->rows_q;
     const int64_t resident_warps = static_cast<int64_t>(ctx->nsm) * bps * (kRowPassThreads / 32);
     plan_rowpass_chunks(ctx->rows_total, ctx->nvec, resident_warps, 0, &ctx->chunks, &ctx->chunk_vec);
@@ -204,6 +213,7 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     ra.K = ctx->K;
     ra.G = ctx->G;
     ra.chunks = ctx->chunks;
+    ra.flags = ctx->flags;
     ra.rows_p = ctx->rows_p;
     ra.rows_total = ctx->rows_total;
     ra.nvec = ctx->nvec;
@@ -237,6 +247,7 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     sa.G = ctx->G;
     sa.V = ctx->V;
     sa.chunks = ctx->chunks;
+    sa.flags = ctx->flags;
     sa.rows_p = ctx->rows_p;
     sa.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
     sa.seed_hi = static_cast<uint32_t>(seed >> 32);
@@ -304,7 +315,7 @@ sdv_status sdv_verify_host(sdv_ctx* ctx, const void* p_logits_host, const void* 
     const size_t elt = elt_size(ctx->dtype);
     const size_t pb = static_cast<size_t>(ctx->rows_p) * ctx->V * elt;
     const size_t qb = static_cast<size_t>(ctx->rows_q) * ctx->V * elt;
-    const size_t db = static_cast<size_t>(ctx->rows_q) * sizeof(int32_t);
+    const size_t db = static_cast<size_t>(ctx->B) * ctx->K * ctx->G * sizeof(int32_t);
     const size_t B = static_cast<size_t>(ctx->B);
     cudaError_t e = cudaSuccess;
     if (!ctx->hs_p) {

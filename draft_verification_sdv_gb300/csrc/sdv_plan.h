@@ -7,6 +7,18 @@
 
 namespace sdv {
 
+// Layout flags of a context (the public SDV_FLAG_* values).
+enum : unsigned {
+    kFlagSharedQ = 1u,       // q is [B][G][V]: one marginal row per (b, j), shared by all k
+};
+
+// Row index of the drafter row of (b, k, j) within the q buffer.
+__host__ __device__ __forceinline__ int64_t q_row_index(unsigned flags, int b, int k, int j, int K,
+                                                        int G) {
+    return (flags & kFlagSharedQ) ? static_cast<int64_t>(b) * G + j
+                                  : (static_cast<int64_t>(b) * K + k) * G + j;
+}
+
 // Bits of the device status word.
 enum : unsigned {
     kStatusBadDraft = 1u,    // a draft id outside [0, V)
@@ -41,6 +53,7 @@ struct RowPassArgs {
     float temperature;
     int K, G;
     int chunks;
+    unsigned flags;
     int64_t rows_p, rows_total;
     int64_t nvec;           // vectors per row
     int64_t chunk_vec;      // vectors per chunk
@@ -56,6 +69,7 @@ struct SelectArgs {
     const float* temps;
     float temperature;
     int B, K, G, V, chunks;
+    unsigned flags;
     int64_t rows_p;
     uint32_t seed_lo, seed_hi;
     int32_t* out_sel;

@@ -153,6 +153,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     ra.K = K;
     ra.G = gamma;
     ra.chunks = chunks;
+    ra.flags = 0u;
     ra.rows_p = rows_p;
     ra.rows_total = rows_total;
     ra.nvec = nvec;
@@ -172,6 +173,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     sa.G = gamma;
     sa.V = V;
     sa.chunks = chunks;
+    sa.flags = 0u;
     sa.rows_p = rows_p;
     sa.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
     sa.seed_hi = static_cast<uint32_t>(seed >> 32);

@@ -45,6 +45,7 @@ class Workload:
     temps: Optional[torch.Tensor]     # [B] float32 per-sequence temperatures, or None
     seed: int = 0                     # Philox seed of the verification step
     identical: Sequence[int] = field(default_factory=list)  # b with q == p[:gamma]
+    shared_q: bool = False            # q_logits is [B, gamma, V], shared by the K drafts
 
     def temps_list(self):
         if self.temps is None:
@@ -130,6 +131,68 @@ def generate(B: int, K: int, gamma: int, V: int, *, dtype=torch.bfloat16,
                     identical=[int(b) for b in identical])
 
 
+def generate_shared(B: int, K: int, gamma: int, V: int, *, dtype=torch.bfloat16,
+                    p_sigma: float = 3.0, zipf: bool = True,
+                    q_sigma: Optional[torch.Tensor] = None, prefix_sigma: float = 0.5,
+                    temperature: float = 1.0, temps: Optional[torch.Tensor] = None,
+                    seed: int = 0, device="cpu", name: str = "shared-marginal",
+                    chunk_rows: int = 256, verify_seed: int = 0) -> Workload:
+    """Drafts from one denoising pass: the drafter exposes one marginal row per
+    position, q[b, j] = base[b, j] + N(0, q_sigma[b, j]^2), and the K drafts are
+    K independent samples from those marginals.  The verifier row at j = 0 sees
+    only the prefix s, so it is the same row base[b, 0] for every draft; rows at
+    j >= 1 see different draft prefixes: base[b, j] + N(0, prefix_sigma^2)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    G1 = gamma + 1
+    prior = _zipf_prior(V, device) if zipf else None
+    if q_sigma is None:
+        q_sigma = torch.ones((B, gamma), dtype=torch.float32)
+    q_sigma = q_sigma.to(device=device, dtype=torch.float32)
+    if temps is not None:
+        temps = temps.to(device=device, dtype=torch.float32)
+    t_seq = temps if temps is not None else torch.full((B,), float(temperature), device=device)
+    p = torch.empty((B, K, G1, V), dtype=dtype, device=device)
+    q = torch.empty((B, gamma, V), dtype=dtype, device=device)
+    drafts = torch.empty((B, K, gamma), dtype=torch.int64, device=device)
+    for b in range(B):
+        for j0 in range(0, G1, max(1, chunk_rows // max(K, 1))):
+            j1 = min(G1, j0 + max(1, chunk_rows // max(K, 1)))
+            base = torch.randn((j1 - j0, V), generator=gen, device=device, dtype=torch.float32)
+            base.mul_(p_sigma)
+            if prior is not None:
+                base.add_(prior)
+            rows = base.unsqueeze(0).expand(K, -1, -1).clone()
+            noise = torch.randn(rows.shape, generator=gen, device=device, dtype=torch.float32)
+            jj = torch.arange(j0, j1, device=device)
+            rows += noise * prefix_sigma * (jj > 0).to(torch.float32)[None, :, None]
+            p[b, :, j0:j1] = rows.to(dtype)
+            for j in range(j0, min(j1, gamma)):
+                qrow = base[j - j0] + torch.randn((V,), generator=gen, device=device) * q_sigma[b, j]
+                qstore = qrow.to(dtype)
+                q[b, j] = qstore
+                logits = (qstore.to(torch.float32) / t_seq[b]).expand(K, V)
+                drafts[b, :, j] = _gumbel_argmax(logits, torch.ones((), device=device), gen)
+    return Workload(name=name, B=B, K=K, gamma=gamma, V=V, dtype=dtype, p_logits=p,
+                    q_logits=q, drafts=drafts.to(torch.int32), temperature=float(temperature),
+                    temps=temps, seed=int(verify_seed), shared_q=True)
+
+
+def workload_shared(B: int = 32, K: int = 16, gamma: int = 32, V: int = QWEN_VOCAB,
+                    device="cpu", seed: int = 55) -> Workload:
+    """The large-window shape with drafts from one pass's marginals: drafter
+    noise rising from 0.3 to 2.0 across the window, per-sequence temperatures
+    in {0.6, 1.0}, verifier rows of different draft prefixes 0.5 apart."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10_000 + seed)
+    sj = 0.3 + 1.7 * torch.arange(gamma, dtype=torch.float32) / max(gamma - 1, 1)
+    coin = torch.rand((B,), generator=g) < 0.5
+    temps = torch.where(coin, torch.tensor(0.6), torch.tensor(1.0))
+    return generate_shared(B, K, gamma, V, q_sigma=sj.expand(B, gamma).clone(), temps=temps,
+                           seed=seed, device=device,
+                           name="large-window shared-marginal B%d K%d g%d V%d bf16" % (B, K, gamma, V))
+
+
 # --------------------------------------------------------------------------
 # The five workloads (tiny exactness case, single stream, self-selection
 # sweep, serving batch, large-window stress), each seeded by its index.
@@ -206,6 +269,8 @@ def to_oracle_arrays(w: Workload, seqs: Optional[Sequence[int]] = None):
         q = q.view(torch.int16).numpy().view(np.uint16)
     else:
         p, q = p.numpy(), q.numpy()
+    if w.shared_q:          # the oracle takes the full layout: q broadcast over k
+        q = np.ascontiguousarray(np.broadcast_to(q[:, None], (q.shape[0], w.K) + q.shape[1:]))
     d = w.drafts[sl].detach().cpu().numpy().astype(np.int32)
     t = np.asarray(w.temps_list(), dtype=np.float64)
     if seqs is not None:

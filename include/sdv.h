@@ -36,7 +36,8 @@
  * Layout: every tensor is contiguous, row-major, on the device of the
  * context unless stated otherwise.
  *   p_logits  [B][K][gamma+1][V]  bf16 or fp32
- *   q_logits  [B][K][gamma][V]    same dtype as p_logits
+ *   q_logits  [B][K][gamma][V]    same dtype as p_logits ([B][gamma][V] with
+ *                                 SDV_FLAG_SHARED_Q, see sdv_create_ex)
  *   drafts    [B][K][gamma]       int32 token ids
  *   out_sel, out_accept_len, out_next_token  [B] int32
  * V * sizeof(element) must be a multiple of 16 bytes and both logit buffers
@@ -87,6 +88,23 @@ typedef enum { SDV_BF16 = 0, SDV_F32 = 1 } sdv_dtype;
  */
 sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V,
                       sdv_dtype dtype, void* stream);
+
+/*
+ * Layout flags for sdv_create_ex.
+ *
+ * SDV_FLAG_SHARED_Q: the K drafts of a sequence are sampled from the
+ * position-wise marginals of one denoising pass ("SpecDiff-2: Scaling
+ * Diffusion Drafter Alignment For Faster Speculative Decoding", section 5.2),
+ * so the drafter rows do not depend on k: q_logits is [B][gamma][V] and row
+ * (b, j) serves every draft k.  Each marginal row is read once, which cuts the
+ * drafter bytes K-fold.  Results equal those of the full layout with q
+ * broadcast over k.
+ */
+#define SDV_FLAG_SHARED_Q 1u
+
+/* sdv_create with layout flags (0 = the full [B][K][gamma][V] q layout). */
+sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V,
+                         sdv_dtype dtype, void* stream, unsigned flags);
 
 /*
  * Enqueue one verification step with one temperature for all sequences

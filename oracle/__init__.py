@@ -59,6 +59,16 @@ def lib():
         L.sdvo_verify_uniforms.restype = ctypes.c_int
         L.sdvo_verify.argtypes = common + [ctypes.c_uint64, ctypes.c_int32] + outs
         L.sdvo_verify.restype = ctypes.c_int
+        L.sdvo_verify_greedy_uniforms.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int64, ctypes.c_int, vp, vp, vp, vp,
+                                                  vp] + outs
+        L.sdvo_verify_greedy_uniforms.restype = ctypes.c_int
+        L.sdvo_verify_greedy.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                         ctypes.c_int, vp, vp, vp, ctypes.c_uint64,
+                                         ctypes.c_int32] + outs
+        L.sdvo_verify_greedy.restype = ctypes.c_int
+        L.sdvo_accept_ratio_greedy.argtypes = [ctypes.c_double]
+        L.sdvo_accept_ratio_greedy.restype = ctypes.c_double
         L.sdvo_max_threads.argtypes = []
         L.sdvo_max_threads.restype = ctypes.c_int
         _lib = L
@@ -190,6 +200,45 @@ def verify_uniforms(p_logits, q_logits, drafts, temps, u, w, nthreads=1):
     if G == 0:
         out["ratio"] = out["ratio"][..., :0]
     return out
+
+
+def _greedy_common(p_logits, drafts, temps):
+    p_logits = np.ascontiguousarray(p_logits)
+    _, dt = _row_dtype(p_logits[..., :1].reshape(-1)[:1])
+    B, K, G1, V = p_logits.shape
+    G = G1 - 1
+    drafts = np.ascontiguousarray(drafts, dtype=np.int32)
+    if drafts.shape != (B, K, G):
+        raise ValueError("drafts must be [B, K, gamma]")
+    temps = np.broadcast_to(np.asarray(temps, dtype=np.float64), (B,)).copy()
+    out = dict(
+        sel=np.full(B, -1, np.int32), accept_len=np.full(B, -1, np.int32),
+        next_token=np.full(B, -1, np.int32), lse=np.zeros((B, K, 2 * G + 1)),
+        scores=np.zeros((B, K)), ratio=np.zeros((B, K, max(G, 1))),
+        band=np.zeros(B, np.int32), err=np.zeros(B, np.int32), resid_mass=np.zeros(B))
+    return p_logits, drafts, temps, dt, (B, K, G, V), out
+
+
+def verify_greedy(p_logits, drafts, temps, seed, b0=0, nthreads=1):
+    """Greedy acceptance (no drafter rows), Philox uniforms as verify()."""
+    p, d, t, dt, (B, K, G, V), out = _greedy_common(p_logits, drafts, temps)
+    lib().sdvo_verify_greedy(B, K, G, V, dt, _ptr(p), _ptr(d), _ptr(t), int(seed), int(b0),
+                             *_outs(out, nthreads))
+    return out
+
+
+def verify_greedy_uniforms(p_logits, drafts, temps, u, w, nthreads=1):
+    """Greedy acceptance with explicit uniforms u [B,gamma], w [B,gamma+1]."""
+    p, d, t, dt, (B, K, G, V), out = _greedy_common(p_logits, drafts, temps)
+    u = np.ascontiguousarray(np.broadcast_to(np.asarray(u, np.float64), (B, G)))
+    w = np.ascontiguousarray(np.broadcast_to(np.asarray(w, np.float64), (B, G + 1)))
+    lib().sdvo_verify_greedy_uniforms(B, K, G, V, dt, _ptr(p), _ptr(d), _ptr(t), _ptr(u),
+                                      _ptr(w), *_outs(out, nthreads))
+    return out
+
+
+def accept_ratio_greedy(lp):
+    return lib().sdvo_accept_ratio_greedy(float(lp))
 
 
 def max_threads():

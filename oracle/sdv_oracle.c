@@ -125,6 +125,13 @@ double sdvo_accept_ratio(double lp, double lq)
     return exp(lp - lq);                   /* else accept with prob p/q        */
 }
 
+double sdvo_accept_ratio_greedy(double lp)
+{
+    if (lp == -INFINITY) return 0.0;       /* p(x) = 0: never accept          */
+    if (lp >= 0.0) return 1.0;
+    return exp(lp);                        /* accept with probability p(x)     */
+}
+
 double sdvo_streak_score(const double* a, int gamma)
 {
     double score = 0.0, prefix = 1.0;
@@ -212,7 +219,7 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
                       const double* u, const double* w, int32_t* sel_out,
                       int32_t* len_out, int32_t* tok_out, double* lse_out,
                       double* scores_out, double* ratio_out, int32_t* band_out,
-                      double* resid_out, int row_threads)
+                      double* resid_out, int row_threads, int greedy)
 {
     const int K = sh->K, G = sh->gamma, dtype = sh->dtype;
     const int64_t V = sh->V;
@@ -250,12 +257,14 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
         const int k = i / nrow, r = i % nrow;
         if (r <= G)
             lse[i] = sdvo_row_lse(p_row(p_logits, sh, b, k, r), dtype, V, T);
-        else
+        else if (!greedy)
             lse[i] = sdvo_row_lse(q_row(q_logits, sh, b, k, r - G - 1), dtype, V, T);
+        else
+            lse[i] = NAN;                 /* greedy acceptance reads no q row */
     }
     (void)row_threads;
     for (int i = 0; i < K * nrow; ++i)
-        if (!isfinite(lse[i])) err |= SDVO_BAD_ROW;
+        if (!isfinite(lse[i]) && !(greedy && i % nrow > G)) err |= SDVO_BAD_ROW;
     if (lse_out) memcpy(lse_out, lse, sizeof(double) * (size_t)K * nrow);
     if (err) goto done;
 
@@ -267,6 +276,18 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
         for (int j = 0; j < G; ++j) {
             int32_t x = drafts[((int64_t)b * K + k) * G + j];
             double lp = sdvo_logprob(p_row(p_logits, sh, b, k, j), dtype, x, T, lse[k * nrow + j]);
+            if (greedy) {
+                /* greedy acceptance: the ratio is p(x) itself */
+                a[k * G + j] = sdvo_accept_ratio_greedy(lp);
+                if (lp == -INFINITY || lp >= 0.0) {
+                    a_lo[k * G + j] = a_hi[k * G + j] = a[k * G + j];
+                } else {
+                    double r = exp(lp);
+                    a_lo[k * G + j] = fmin(1.0, r * (1.0 - 1e-5));
+                    a_hi[k * G + j] = fmin(1.0, r * (1.0 + 1e-5));
+                }
+                continue;
+            }
             double lq = sdvo_logprob(q_row(q_logits, sh, b, k, j), dtype, x, T, lse[k * nrow + G + 1 + j]);
             a[k * G + j] = sdvo_accept_ratio(lp, lq);
             if (lq == -INFINITY || lp == -INFINITY || lp == lq) {
@@ -306,7 +327,20 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
     double R = 0.0, t = 0.0, c_prev = 0.0, c_v = 0.0;
     const void* prow = p_row(p_logits, sh, b, sel, L);
     double lse_p = lse[sel * nrow + L];
-    if (L < G) {
+    if (L < G && greedy) {
+        /* greedy: draw from p with the rejected token zeroed out */
+        const int32_t xr = drafts[((int64_t)b * K + sel) * G + L];
+        for (int64_t v = 0; v < V; ++v)
+            r[v] = v == xr ? 0.0 : exp(sdvo_logit(prow, dtype, v) / T - lse_p);
+        tok = sdvo_inverse_cdf(r, V, w[L], &R, &t, &c_prev, &c_v);
+        if (resid_out) *resid_out = R;
+        if (R < 1e-3) band |= SDVO_BAND_RESID;
+        if (tok < 0) {
+            for (int64_t v = 0; v < V; ++v)
+                r[v] = exp(sdvo_logit(prow, dtype, v) / T - lse_p);
+            tok = sdvo_inverse_cdf(r, V, w[L], &R, &t, &c_prev, &c_v);
+        }
+    } else if (L < G) {
         const void* qrow = q_row(q_logits, sh, b, sel, L);
         double lse_q = lse[sel * nrow + G + 1 + L];
         for (int64_t v = 0; v < V; ++v) {
@@ -342,7 +376,7 @@ done:
     return err;
 }
 
-static int run_batch(int B, int K, int gamma, int64_t V, int dtype,
+static int run_batch(int B, int K, int gamma, int64_t V, int dtype, int greedy,
                      const void* p_logits, const void* q_logits,
                      const int32_t* drafts, const double* temps,
                      const double* u_in, const double* w_in, int use_philox,
@@ -382,7 +416,7 @@ static int run_batch(int B, int K, int gamma, int64_t V, int dtype,
                            scores ? scores + (int64_t)b * K : NULL,
                            ratio ? ratio + (int64_t)b * K * gamma : NULL,
                            band ? band + b : NULL,
-                           resid_mass ? resid_mass + b : NULL, row_threads);
+                           resid_mass ? resid_mass + b : NULL, row_threads, greedy);
         if (err) err[b] = e;
         any |= e;
         free(u); free(w);
@@ -400,7 +434,20 @@ int sdvo_verify_uniforms(int B, int K, int gamma, int64_t V, int dtype,
                          int32_t* band, int32_t* err, double* resid_mass,
                          int nthreads)
 {
-    return run_batch(B, K, gamma, V, dtype, p_logits, q_logits, drafts, temps, u, w, 0, 0, 0,
+    return run_batch(B, K, gamma, V, dtype, 0, p_logits, q_logits, drafts, temps, u, w, 0, 0, 0,
+                     sel, accept_len, next_token, lse, scores, ratio, band, err, resid_mass,
+                     nthreads);
+}
+
+int sdvo_verify_greedy_uniforms(int B, int K, int gamma, int64_t V, int dtype,
+                                const void* p_logits, const int32_t* drafts,
+                                const double* temps, const double* u, const double* w,
+                                int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                                double* lse, double* scores, double* ratio,
+                                int32_t* band, int32_t* err, double* resid_mass,
+                                int nthreads)
+{
+    return run_batch(B, K, gamma, V, dtype, 1, p_logits, NULL, drafts, temps, u, w, 0, 0, 0,
                      sel, accept_len, next_token, lse, scores, ratio, band, err, resid_mass,
                      nthreads);
 }
@@ -414,7 +461,20 @@ int sdvo_verify(int B, int K, int gamma, int64_t V, int dtype,
                 int32_t* band, int32_t* err, double* resid_mass,
                 int nthreads)
 {
-    return run_batch(B, K, gamma, V, dtype, p_logits, q_logits, drafts, temps, NULL, NULL, 1,
+    return run_batch(B, K, gamma, V, dtype, 0, p_logits, q_logits, drafts, temps, NULL, NULL, 1,
+                     seed, b0, sel, accept_len, next_token, lse, scores, ratio, band, err,
+                     resid_mass, nthreads);
+}
+
+int sdvo_verify_greedy(int B, int K, int gamma, int64_t V, int dtype,
+                       const void* p_logits, const int32_t* drafts,
+                       const double* temps, uint64_t seed, int32_t b0,
+                       int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                       double* lse, double* scores, double* ratio,
+                       int32_t* band, int32_t* err, double* resid_mass,
+                       int nthreads)
+{
+    return run_batch(B, K, gamma, V, dtype, 1, p_logits, NULL, drafts, temps, NULL, NULL, 1,
                      seed, b0, sel, accept_len, next_token, lse, scores, ratio, band, err,
                      resid_mass, nthreads);
 }

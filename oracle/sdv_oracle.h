@@ -82,6 +82,11 @@ double sdvo_logprob(const void* row, int dtype, int64_t x, double T, double lse)
  * (lq = -inf) counts as q <= p, so a = 1; p(x) = 0 < q(x) gives a = 0. */
 double sdvo_accept_ratio(double lp, double lq);
 
+/* Greedy acceptance ratio from the verifier alone: a = p(x) (the drafted
+ * token's verifier probability; "SpecDiff-2: Scaling Diffusion Drafter
+ * Alignment For Faster Speculative Decoding", section 5.2 and appendix B.4). */
+double sdvo_accept_ratio_greedy(double lp);
+
 /* Expected accepted streak S = sum_{j<gamma} prod_{i<=j} a_i. */
 double sdvo_streak_score(const double* a, int gamma);
 
@@ -128,6 +133,26 @@ int sdvo_verify(int B, int K, int gamma, int64_t V, int dtype,
                 double* lse, double* scores, double* ratio,
                 int32_t* band, int32_t* err, double* resid_mass,
                 int nthreads);
+
+/* Greedy acceptance (same page, section 5.2 and appendix B.4): no drafter
+ * rows.  a_j = p_j(x_j); S_k and the selection as above; accept iff
+ * u_j < p_j(x_j); at the first rejection L draw from p_L with x_L zeroed out
+ * (renormalised); if all are accepted, the bonus token from p_gamma.  The
+ * q entries of lse[] are NaN. */
+int sdvo_verify_greedy_uniforms(int B, int K, int gamma, int64_t V, int dtype,
+                                const void* p_logits, const int32_t* drafts,
+                                const double* temps, const double* u, const double* w,
+                                int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                                double* lse, double* scores, double* ratio,
+                                int32_t* band, int32_t* err, double* resid_mass,
+                                int nthreads);
+int sdvo_verify_greedy(int B, int K, int gamma, int64_t V, int dtype,
+                       const void* p_logits, const int32_t* drafts,
+                       const double* temps, uint64_t seed, int32_t b0,
+                       int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                       double* lse, double* scores, double* ratio,
+                       int32_t* band, int32_t* err, double* resid_mass,
+                       int nthreads);
 
 /* Number of threads the build can run (1 without OpenMP). */
 int sdvo_max_threads(void);

@@ -29,7 +29,7 @@ def _lib():
 
 
 def run_gpu(w: synth.Workload, seed=None, stream=None):
-    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream)
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q)
     out = v(w.p_logits, w.q_logits, w.drafts, temperature=w.temperature,
             seed=w.seed if seed is None else seed, temps=w.temps, scores=True, lse=True)
     status = bd.sdv_sync(v.ctx)
@@ -338,3 +338,42 @@ def test_side_stream():
         got = run_gpu(w, stream=s)
     for k in ("sel", "accept_len", "next_token"):
         assert np.array_equal(ref[k], got[k])
+
+
+# ---------------------------------------------------------------------------
+# shared drafter marginals (q is [B, gamma, V], one row per position)
+# ---------------------------------------------------------------------------
+
+def test_shared_marginals_small():
+    w = synth.generate_shared(6, 4, 5, 3000, q_sigma=torch.full((6, 5), 0.8), temperature=0.9,
+                              seed=111, device="cuda")
+    gpu, orc = run_gpu(w, seed=3), run_oracle(w, seed=3)
+    assert gpu["status"] == bd.SDV_OK
+    assert compare(gpu, orc, tag="shared") <= 1
+
+
+def test_shared_marginals_equal_full_layout_bitwise():
+    """The shared layout gives bit-identical outputs to the full layout with
+    the marginal rows copied to every draft."""
+    w = synth.generate_shared(4, 3, 6, 20000, temps=torch.tensor([0.6, 1.0, 1.3, 0.8]), seed=112,
+                              device="cuda")
+    shared = run_gpu(w, seed=5)
+    full = synth.Workload(name="full", B=w.B, K=w.K, gamma=w.gamma, V=w.V, dtype=w.dtype,
+                          p_logits=w.p_logits,
+                          q_logits=w.q_logits[:, None].expand(w.B, w.K, w.gamma, w.V).contiguous(),
+                          drafts=w.drafts, temperature=w.temperature, temps=w.temps, seed=w.seed)
+    ref = run_gpu(full, seed=5)
+    for k in ("sel", "accept_len", "next_token", "scores", "lse"):
+        assert np.array_equal(shared[k], ref[k]), k
+
+
+def test_shared_marginals_large_window_sampled():
+    w = synth.workload_shared(device="cuda")
+    gpu = run_gpu(w)
+    assert gpu["status"] == bd.SDV_OK
+    assert ((gpu["accept_len"] >= 0) & (gpu["accept_len"] <= w.gamma)).all()
+    seqs = [3, 30]
+    orc = run_oracle(w, seqs)
+    assert compare(gpu, orc, seqs, tag="shared large-window") <= 1
+    del w
+    torch.cuda.empty_cache()

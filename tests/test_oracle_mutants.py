@@ -40,6 +40,12 @@ MUTANTS = [
      "lse[i] = sdvo_row_lse(p_row(p_logits, sh, b, k, r - G - 1), dtype, V, T);", 1),
     ("residual_drops_temperature", "double pv = exp(sdvo_logit(prow, dtype, v) / T - lse_p);",
      "double pv = exp(sdvo_logit(prow, dtype, v) - lse_p);", 1),
+    ("greedy_ratio_squared", "    return exp(lp);                        /* accept with probability p(x)     */",
+     "    return exp(2.0 * lp);", 1),
+    ("greedy_keeps_rejected_token", "r[v] = v == xr ? 0.0 : exp(sdvo_logit(prow, dtype, v) / T - lse_p);",
+     "r[v] = exp(sdvo_logit(prow, dtype, v) / T - lse_p);", 1),
+    ("greedy_zeroes_wrong_token", "const int32_t xr = drafts[((int64_t)b * K + sel) * G + L];",
+     "const int32_t xr = drafts[((int64_t)b * K + sel) * G + (L + 1) % G];", 1),
 ]
 
 
@@ -57,6 +63,7 @@ def test_pins_catch_mutant(name, old, new, count, tmp_path):
                     str(c), "-lm"], check=True, capture_output=True)
     env = dict(os.environ, SDV_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_greedy_pins.py")],
                        env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-1500:])
