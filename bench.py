@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["sdv", "reference"], default="sdv")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--greedy", action="store_true",
+                    help="greedy acceptance: verifier rows only, no drafter rows")
     ap.add_argument("--shared-q", action="store_true",
                     help="drafts from one pass's marginals: q is [B, gamma, V] (large-window shape)")
     ap.add_argument("--batch", type=int, default=None,
@@ -193,12 +195,14 @@ def traffic_per_row():
         return None
 
 
-def step_bytes(w: synth.Workload, accept_len) -> dict:
+def step_bytes(w: synth.Workload, accept_len, greedy: bool = False) -> dict:
     """Algorithmic bytes of one step: every logit row once, the re-read rows
-    of the draw (two for a residual, one for a bonus), drafts, outputs."""
+    of the draw (two for a residual, one for a bonus or a greedy replacement),
+    drafts, outputs."""
     elt = 2 if w.dtype == torch.bfloat16 else 4
-    rows = w.B * w.K * (w.gamma + 1) + (w.B if w.shared_q else w.B * w.K) * w.gamma
-    reread = sum(2 if int(L) < w.gamma else 1 for L in accept_len)
+    q_rows = 0 if greedy else (w.B if w.shared_q else w.B * w.K) * w.gamma
+    rows = w.B * w.K * (w.gamma + 1) + q_rows
+    reread = sum(2 if int(L) < w.gamma and not greedy else 1 for L in accept_len)
     k1 = elt * w.V * rows
     total = k1 + elt * w.V * reread + w.B * w.K * w.gamma * 4 + w.B * 12
     return {"rows": rows, "k1": k1, "total": total, "reread_rows": reread}
@@ -217,7 +221,11 @@ def run_sdv(args, rank, world, local):
     else:
         w = synth.workload(args.workload, device=dev, seed=args.workload + 1000 * rank, B=args.batch)
     stream = torch.cuda.Stream(device=dev)
-    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q)
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q,
+                    greedy=args.greedy)
+    if args.greedy:
+        w.q_logits = None
+        torch.cuda.empty_cache()
     out = None
 
     def step():
@@ -265,7 +273,7 @@ def run_sdv(args, rank, world, local):
     tokens_per_step = w.B * w.K * w.gamma
     value = world * tokens_per_step * args.steps / (ms_max / 1e3)
     ms_step = ms_max / args.steps
-    sb = step_bytes(w, accept_len)
+    sb = step_bytes(w, accept_len, greedy=args.greedy)
     peak, peak_kind = measured_peaks()
     k1_gbs = sb["k1"] / (ms_kernels[0] * 1e-3) / 1e9 if ms_kernels[0] > 0 else None
     step_gbs = sb["total"] / (ms_step * 1e-3) / 1e9
@@ -297,7 +305,8 @@ def run_sdv(args, rank, world, local):
         "input_dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded logits and drafts; no model weights)",
         "config": {"workload": w.name, "B": w.B, "K": w.K, "gamma": w.gamma, "V": w.V,
-                   "q_layout": "[B,gamma,V] shared by the K drafts" if w.shared_q else "[B,K,gamma,V]",
+                   "q_layout": ("none (greedy acceptance)" if args.greedy else
+                                "[B,gamma,V] shared by the K drafts" if w.shared_q else "[B,K,gamma,V]"),
                    "temperatures": "per-sequence {0.6, 1.0}" if w.temps is not None else w.temperature,
                    "l2": "inputs %.2f GB > L2 (126 MB): no flush" % (sb["k1"] / 1e9),
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "1 GPU"},
@@ -315,9 +324,11 @@ def run_sdv(args, rank, world, local):
     # host memory each step, outputs read back.
     if not args.no_e2e:
         hp = torch.empty(w.p_logits.shape, dtype=w.dtype, pin_memory=True)
-        hq = torch.empty(w.q_logits.shape, dtype=w.dtype, pin_memory=True)
         hp.copy_(w.p_logits)
-        hq.copy_(w.q_logits)
+        hq = None
+        if w.q_logits is not None:
+            hq = torch.empty(w.q_logits.shape, dtype=w.dtype, pin_memory=True)
+            hq.copy_(w.q_logits)
         hd = w.drafts.cpu().pin_memory()
         ht = w.temps.cpu().pin_memory() if w.temps is not None else None
         outs = [torch.empty(w.B, dtype=torch.int32).pin_memory() for _ in range(3)]
@@ -330,15 +341,15 @@ def run_sdv(args, rank, world, local):
             assert st == bd.SDV_OK, bd.sdv_last_error(v.ctx)
         te = time.perf_counter() - te0
         te = max_over_ranks(te, world)
-        h2d = hp.numel() * hp.element_size() + hq.numel() * hq.element_size() + hd.numel() * 4 + \
-            (ht.numel() * 4 if ht is not None else 0)
+        h2d = hp.numel() * hp.element_size() + (hq.numel() * hq.element_size() if hq is not None else 0) + \
+            hd.numel() * 4 + (ht.numel() * 4 if ht is not None else 0)
         result["e2e"] = {"value": world * tokens_per_step * args.e2e_steps / te, "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 3 * w.B * 4,
                          "steps": args.e2e_steps, "ms_per_step": te * 1e3 / args.e2e_steps}
         del hp, hq
 
     # The oracle as it stands on the host cores, bounded sample (rank 0, N = 1).
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.greedy:
         result["cpu_baseline"] = cpu_baseline(w)
     v.close()
     return result

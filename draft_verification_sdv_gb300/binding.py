@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(HERE, "libsdv.so")
 SDV_OK, SDV_ERR_ARG, SDV_ERR_CUDA, SDV_ERR_OOM, SDV_ERR_DEVICE_DATA, SDV_ERR_SCRATCH = 0, 1, 2, 3, 4, 5
 SDV_BF16, SDV_F32 = 0, 1
 SDV_FLAG_SHARED_Q = 1
+SDV_FLAG_GREEDY = 2
 STATUS_NAMES = {0: "SDV_OK", 1: "SDV_ERR_ARG", 2: "SDV_ERR_CUDA", 3: "SDV_ERR_OOM",
                 4: "SDV_ERR_DEVICE_DATA", 5: "SDV_ERR_SCRATCH"}
 STATIC_SCRATCH_BYTES = 8 << 20
@@ -219,26 +220,30 @@ class Verifier:
     """
 
     def __init__(self, B: int, K: int, gamma: int, V: int, dtype=torch.bfloat16,
-                 device=None, stream=None, shared_q: bool = False):
+                 device=None, stream=None, shared_q: bool = False, greedy: bool = False):
         self.B, self.K, self.gamma, self.V, self.dtype = B, K, gamma, V, dtype
         self.shared_q = shared_q
+        self.greedy = greedy
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
             else torch.device(device)
         with torch.cuda.device(self.device):
             self.stream = stream
             self.ctx = sdv_create(B, K, gamma, V, dtype, stream,
-                                  SDV_FLAG_SHARED_Q if shared_q else 0)
+                                  (SDV_FLAG_SHARED_Q if shared_q else 0) |
+                                  (SDV_FLAG_GREEDY if greedy else 0))
 
     def __call__(self, p_logits, q_logits, drafts, temperature: float = 1.0, seed: int = 0,
                  temps: Optional[torch.Tensor] = None, scores: bool = False, lse: bool = False,
                  out: Optional[dict] = None) -> dict:
         B, K, G, V = self.B, self.K, self.gamma, self.V
         q_shape = (B, G, V) if self.shared_q else (B, K, G, V)
-        if tuple(p_logits.shape) != (B, K, G + 1, V) or tuple(q_logits.shape) != q_shape:
-            raise ValueError("logits must be [B,K,gamma+1,V] and %s" % (list(q_shape),))
+        if tuple(p_logits.shape) != (B, K, G + 1, V):
+            raise ValueError("p_logits must be [B,K,gamma+1,V]")
+        if not self.greedy and (q_logits is None or tuple(q_logits.shape) != q_shape):
+            raise ValueError("q_logits must be %s" % (list(q_shape),))
         if tuple(drafts.shape) != (B, K, G):
             raise ValueError("drafts must be [B,K,gamma]")
-        if p_logits.dtype != self.dtype or q_logits.dtype != self.dtype:
+        if p_logits.dtype != self.dtype or (q_logits is not None and q_logits.dtype != self.dtype):
             raise TypeError("logits must be %s" % self.dtype)
         dev = p_logits.device
         if out is None:
@@ -250,7 +255,8 @@ class Verifier:
             if scores:
                 out["scores"] = torch.empty((B, K), dtype=torch.float32, device=dev)
             if lse:
-                out["lse"] = torch.empty((B, K, 2 * G + 1), dtype=torch.float32, device=dev)
+                out["lse"] = torch.empty((B, K, G + 1 if self.greedy else 2 * G + 1),
+                                         dtype=torch.float32, device=dev)
         st = sdv_verify_ex(self.ctx, p_logits, q_logits, drafts, temperature, temps, seed,
                            out["sel"], out["accept_len"], out["next_token"], out.get("scores"),
                            out.get("lse"))

@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
+    const bool greedy = (a.flags & kFlagGreedy) != 0;   // no drafter rows
     const float T = a.temps ? a.temps[b] : a.temperature;
     const float c = kLog2e / T;
     if (tid == 0) {
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
 
     const int64_t seq_p = static_cast<int64_t>(b) * K * (G + 1);   // first p row of b
     const int64_t seq_d = static_cast<int64_t>(b) * K * G;         // first draft of b
-    const int nrow = 2 * G + 1;
+    const int nrow = greedy ? G + 1 : 2 * G + 1;        // LSE entries per draft
 
     // The drafted token of this thread's first pair and its two logits are
     // inputs of the step, not results of the row pass: fetch them before
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         x0 = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
         if (x0 >= 0 && x0 < a.V) {
             lp0 = load_logit(a.p, (seq_p + static_cast<int64_t>(k) * (G + 1) + j) * a.V + x0, BF16);
-            lq0 = load_logit(a.q, q_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
+            if (!greedy) lq0 = load_logit(a.q, q_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
         }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -114,32 +115,41 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     for (int idx = tid; idx < KG; idx += kSelectThreads) {
         const int k = idx / G, j = idx - (idx / G) * G;
         const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + j;
-        const int64_t rq = q_row_index(a.flags, b, k, j, K, G);
+        const int64_t rq = greedy ? 0 : q_row_index(a.flags, b, k, j, K, G);
         int32_t x = x0;
         float lp = lp0, lq = lq0;
         if (idx != tid) {
             x = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
             if (x >= 0 && x < a.V) {
                 lp = load_logit(a.p, rp * a.V + x, BF16);
-                lq = load_logit(a.q, rq * a.V + x, BF16);
+                if (!greedy) lq = load_logit(a.q, rq * a.V + x, BF16);
             }
         }
         const bool x_ok = x >= 0 && x < a.V;
-        float mp, sp, mq, sq;
-        merge_rows2(a.part + rp * a.chunks, a.part + (a.rows_p + rq) * a.chunks, a.chunks, c, mp, sp,
-                    mq, sq);
+        float mp, sp, mq = 0.0f, sq = 1.0f;
+        const float2* prow_part = a.part + rp * a.chunks;
+        merge_rows2(prow_part, greedy ? prow_part : a.part + (a.rows_p + rq) * a.chunks, a.chunks, c,
+                    mp, sp, mq, sq);
+        if (greedy) {
+            mq = 0.0f;
+            sq = 1.0f;
+        }
         pstat[k * (G + 1) + j] = make_float2(mp, sp);
         qstat[idx] = make_float2(mq, sq);
         if (a.out_lse) {
             float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
             lse[j] = row_lse(mp, sp, c);
-            lse[G + 1 + j] = row_lse(mq, sq, c);
+            if (!greedy) lse[G + 1 + j] = row_lse(mq, sq, c);
         }
         float r = 0.0f;
         if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
             atomicOr(&s_bad, kStatusBadRow);
         } else if (!x_ok) {
             atomicOr(&s_bad, kStatusBadDraft);
+        } else if (greedy) {
+            // greedy acceptance: the ratio is the verifier probability p(x)
+            const float d = (lp - mp) * c - log2f(sp);
+            r = d >= 0.0f ? 1.0f : ex2(d);
         } else if (lq == -INFINITY) {
             r = 1.0f;                                           // q(x) = 0 <= p(x)
         } else {
@@ -220,7 +230,11 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const float2 ps = pstat[sel * (G + 1) + L];
         t.mp = ps.x;
         t.inv_sp = 1.0f / ps.y;
-        if (L < G) {
+        if (L < G && greedy) {
+            t.mode = 3;                                   // p with the rejected token zeroed
+            t.zero_id = a.drafts[seq_d + static_cast<int64_t>(sel) * G + L];
+            t.row_q = -1;
+        } else if (L < G) {
             t.mode = 1;                                   // residual max(0, p - q)
             t.row_q = q_row_index(a.flags, b, sel, L, K, G);
             const float2 qs = qstat[sel * G + L];

@@ -38,14 +38,17 @@ __device__ __forceinline__ float elem(const uint4& v, int e) {
 }
 
 // Sampling weights of the elements of vector i of the slice: p, or the
-// residual max(0, p - q).
+// residual max(0, p - q); the element at slice position zero_pos (if any)
+// gets weight 0 (greedy replacement: the rejected token is excluded).
 template <bool BF16>
 __device__ __forceinline__ void weights(const uint4* sp, const uint4* sq, int i, bool resid,
-                                        const SeqTask& t, float (&w)[Elems<BF16>::kPerVec]) {
+                                        int zero_pos, const SeqTask& t,
+                                        float (&w)[Elems<BF16>::kPerVec]) {
     constexpr int EPV = Elems<BF16>::kPerVec;
     const uint4 pv = sp[i];
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) w[e] = ex2((elem<BF16>(pv, e) - t.mp) * t.c) * t.inv_sp;
+    for (int e = 0; e < EPV; ++e)
+        w[e] = i * EPV + e == zero_pos ? 0.0f : ex2((elem<BF16>(pv, e) - t.mp) * t.c) * t.inv_sp;
     if (resid) {
         const uint4 qv = sq[i];
 #pragma unroll
@@ -119,12 +122,16 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
 
     for (int pass = 0; pass < 2; ++pass) {
         const bool resid = (t.mode == 1) && (pass == 0);
+        // greedy replacement: the rejected token's position within this slice
+        const int zero_pos = (t.mode == 3 && pass == 0)
+                                 ? static_cast<int>(static_cast<int64_t>(t.zero_id) - sv0 * EPV)
+                                 : -1;
         // Per-vector sums are independent; the thread sum adds them in order.
         float tsum = 0.0f;
         if (have_data)
             for (int i = tv0; i < tv1; ++i) {
                 float w[EPV];
-                weights<BF16>(sp, sq, i, resid, t, w);
+                weights<BF16>(sp, sq, i, resid, zero_pos, t, w);
                 tsum += tree_sum(w);
             }
 
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         for (int r = 0; r < CL; ++r) R += tot[r];
         // Residual mass zero on this row: every CTA sees the same R, so the
         // whole cluster takes the fallback pass to p together.
-        if (pass == 0 && t.mode == 1 && R == 0.0f && all_ok) {
+        if (pass == 0 && (t.mode == 1 || t.mode == 3) && R == 0.0f && all_ok) {
             cluster_sync();
             continue;
         }
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
                 int tok = -1, last_pos = -1;
                 for (int i = tv0; i < tv1 && tok < 0; ++i) {
                     float w[EPV];
-                    weights<BF16>(sp, sq, i, resid, t, w);
+                    weights<BF16>(sp, sq, i, resid, zero_pos, t, w);
                     const float vs = tree_sum(w);
                     if (run + vs > tt) {
                         float r2 = run;
@@ -245,7 +252,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
                     const int l0 = min(lt * vpt, nv), l1 = min(l0 + vpt, nv);
                     for (int i = l0; i < l1; ++i) {
                         float w[EPV];
-                        weights<BF16>(sp, sq, i, resid, t, w);
+                        weights<BF16>(sp, sq, i, resid, zero_pos, t, w);
                         for (int e = 0; e < EPV; ++e)
                             if (w[e] > 0.0f) tok = i * EPV + e;
                     }

@@ -91,7 +91,8 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
                          void* stream, unsigned flags) {
     if (!out) return SDV_ERR_ARG;
     *out = nullptr;
-    if (flags & ~static_cast<unsigned>(SDV_FLAG_SHARED_Q)) return SDV_ERR_ARG;
+    if (flags & ~static_cast<unsigned>(SDV_FLAG_SHARED_Q | SDV_FLAG_GREEDY)) return SDV_ERR_ARG;
+    if ((flags & SDV_FLAG_SHARED_Q) && (flags & SDV_FLAG_GREEDY)) return SDV_ERR_ARG;
     if (B < 1 || K < 1 || gamma < 1 || V < 1) return SDV_ERR_ARG;
     if (dtype != SDV_BF16 && dtype != SDV_F32) return SDV_ERR_ARG;
     const size_t elt = elt_size(dtype);
@@ -122,8 +123,9 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
     // Row pass plan.
     ctx->nvec = static_cast<int64_t>(V) * static_cast<int64_t>(elt) / 16;
     ctx->rows_p = static_cast<int64_t>(B) * K * (gamma + 1);
-    ctx->rows_q = (flags & SDV_FLAG_SHARED_Q) ? static_cast<int64_t>(B) * gamma
-                                              : static_cast<int64_t>(B) * K * gamma;
+    ctx->rows_q = (flags & SDV_FLAG_GREEDY)     ? 0
+                  : (flags & SDV_FLAG_SHARED_Q) ? static_cast<int64_t>(B) * gamma
+                                                : static_cast<int64_t>(B) * K * gamma;
     ctx->rows_total = ctx->rows_p + ctx->rows_q;
     const int64_t resident_warps = static_cast<int64_t>(ctx->nsm) * bps * (kRowPassThreads / 32);
     plan_rowpass_chunks(ctx->rows_total, ctx->nvec, resident_warps, 0, &ctx->chunks, &ctx->chunk_vec);
@@ -185,7 +187,9 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
                          float* out_lse) {
     if (!ctx) return SDV_ERR_ARG;
     ctx->err[0] = 0;
-    if (!p_logits || !q_logits || !drafts || !out_sel || !out_accept_len || !out_next_token)
+    const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
+    if (!p_logits || (!q_logits && !greedy) || !drafts || !out_sel || !out_accept_len ||
+        !out_next_token)
         return fail(ctx, SDV_ERR_ARG, "null pointer argument");
     if ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits)) & 15u)
         return fail(ctx, SDV_ERR_ARG, "logit buffers must be 16-byte aligned");
@@ -309,8 +313,9 @@ sdv_status sdv_verify_host(sdv_ctx* ctx, const void* p_logits_host, const void* 
                            int32_t* out_sel_host, int32_t* out_accept_len_host,
                            int32_t* out_next_token_host) {
     if (!ctx) return SDV_ERR_ARG;
-    if (!p_logits_host || !q_logits_host || !drafts_host || !out_sel_host || !out_accept_len_host ||
-        !out_next_token_host)
+    const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
+    if (!p_logits_host || (!q_logits_host && !greedy) || !drafts_host || !out_sel_host ||
+        !out_accept_len_host || !out_next_token_host)
         return fail(ctx, SDV_ERR_ARG, "null pointer argument");
     const size_t elt = elt_size(ctx->dtype);
     const size_t pb = static_cast<size_t>(ctx->rows_p) * ctx->V * elt;
@@ -320,7 +325,7 @@ sdv_status sdv_verify_host(sdv_ctx* ctx, const void* p_logits_host, const void* 
     cudaError_t e = cudaSuccess;
     if (!ctx->hs_p) {
         e = cudaMalloc(&ctx->hs_p, pb);
-        if (e == cudaSuccess) e = cudaMalloc(&ctx->hs_q, qb);
+        if (e == cudaSuccess && qb > 0) e = cudaMalloc(&ctx->hs_q, qb);
         if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ctx->hs_drafts), db);
         if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ctx->hs_temps), B * 4);
         if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&ctx->hs_out), 3 * B * 4);
@@ -340,7 +345,8 @@ sdv_status sdv_verify_host(sdv_ctx* ctx, const void* p_logits_host, const void* 
     }
     cudaStream_t s = ctx->stream;
     e = cudaMemcpyAsync(ctx->hs_p, p_logits_host, pb, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->hs_q, q_logits_host, qb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && qb > 0)
+        e = cudaMemcpyAsync(ctx->hs_q, q_logits_host, qb, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->hs_drafts, drafts_host, db, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && temperature_per_seq_host)
         e = cudaMemcpyAsync(ctx->hs_temps, temperature_per_seq_host, B * 4, cudaMemcpyHostToDevice, s);

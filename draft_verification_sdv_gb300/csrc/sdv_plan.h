@@ -10,6 +10,7 @@ namespace sdv {
 // Layout flags of a context (the public SDV_FLAG_* values).
 enum : unsigned {
     kFlagSharedQ = 1u,       // q is [B][G][V]: one marginal row per (b, j), shared by all k
+    kFlagGreedy = 2u,        // greedy acceptance: no drafter rows at all
 };
 
 // Row index of the drafter row of (b, k, j) within the q buffer.
@@ -27,12 +28,13 @@ enum : unsigned {
     kStatusTimeout = 8u,     // a bounded device wait gave up
 };
 
-// Task handed from the select/scan kernel to the sampling kernel, one per
-// sequence.  mode 0: nothing to draw (data error); 1: residual max(0, p - q)
-// of rows (row_p, row_q); 2: bonus draw from row_p alone.
+// The draw to make for one sequence, decided by the selection and scan.
+// mode 0: nothing to draw (data error); 1: residual max(0, p - q) of rows
+// (row_p, row_q); 2: bonus draw from row_p alone; 3: greedy replacement, row_p
+// with the token zero_id zeroed out.
 struct SeqTask {
     int mode;
-    int pad;
+    int zero_id;
     int64_t row_p;      // row index within the p buffer
     int64_t row_q;      // row index within the q buffer
     float w;            // sampling uniform

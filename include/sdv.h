@@ -102,6 +102,19 @@ sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V,
  */
 #define SDV_FLAG_SHARED_Q 1u
 
+/*
+ * SDV_FLAG_GREEDY: greedy acceptance, which verifies the selected draft
+ * without drafting probabilities (same page, section 5.2 and appendix B.4;
+ * usable with drafters of another tokenizer).  No drafter rows are read:
+ * q_logits may be NULL.  a_j = p_j(x_j), the streak score is
+ * S_k = sum_j prod_{i<=j} p_i(x_i), token j is accepted when u_j < p_j(x_j),
+ * and at the first rejection L the replacement is drawn from p_L with x_L
+ * zeroed out (renormalised); with every token accepted, the bonus token comes
+ * from p_gamma.  out_lse is then [B][K][gamma+1].  Cannot be combined with
+ * SDV_FLAG_SHARED_Q.
+ */
+#define SDV_FLAG_GREEDY 2u
+
 /* sdv_create with layout flags (0 = the full [B][K][gamma][V] q layout). */
 sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V,
                          sdv_dtype dtype, void* stream, unsigned flags);

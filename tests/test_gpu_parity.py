@@ -28,9 +28,10 @@ def _lib():
     bd.load(build=True)
 
 
-def run_gpu(w: synth.Workload, seed=None, stream=None):
-    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q)
-    out = v(w.p_logits, w.q_logits, w.drafts, temperature=w.temperature,
+def run_gpu(w: synth.Workload, seed=None, stream=None, greedy=False):
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q,
+                    greedy=greedy)
+    out = v(w.p_logits, None if greedy else w.q_logits, w.drafts, temperature=w.temperature,
             seed=w.seed if seed is None else seed, temps=w.temps, scores=True, lse=True)
     status = bd.sdv_sync(v.ctx)
     res = {k: t.cpu().numpy() for k, t in out.items()}
@@ -40,10 +41,16 @@ def run_gpu(w: synth.Workload, seed=None, stream=None):
     return res
 
 
-def run_oracle(w: synth.Workload, seqs=None, seed=None):
+def run_oracle(w: synth.Workload, seqs=None, seed=None, greedy=False):
     import oracle
     p, q, d, t = synth.to_oracle_arrays(w, seqs)
     seed = w.seed if seed is None else seed
+    if greedy:
+        if seqs is None:
+            return oracle.verify_greedy(p, d, t, seed, nthreads=oracle.max_threads())
+        outs = [oracle.verify_greedy(p[i:i + 1], d[i:i + 1], t[i:i + 1], seed, b0=b, nthreads=1)
+                for i, b in enumerate(seqs)]
+        return {k: np.concatenate([o[k] for o in outs]) for k in outs[0]}
     if seqs is None:
         return oracle.verify(p, q, d, t, seed, nthreads=oracle.max_threads())
     # sampled sequences keep their own b in the uniform keying
@@ -65,7 +72,8 @@ def compare(gpu, orc, seqs=None, tag=""):
         if orc["err"][i]:
             assert gpu["sel"][b] == -1 and gpu["accept_len"][b] == -1 and gpu["next_token"][b] == -1
             continue
-        lo, lg = orc["lse"][i], gpu["lse"][b]
+        lg = gpu["lse"][b]
+        lo = orc["lse"][i][..., :lg.shape[-1]]      # greedy mode has no q rows
         bad = np.abs(lg - lo) > LSE_RTOL * np.maximum(1.0, np.abs(lo))
         assert not bad.any(), "%s b=%d LSE mismatch %s vs %s" % (tag, b, lg[bad][:4], lo[bad][:4])
         so, sg = orc["scores"][i], gpu["scores"][b]
@@ -377,3 +385,44 @@ def test_shared_marginals_large_window_sampled():
     assert compare(gpu, orc, seqs, tag="shared large-window") <= 1
     del w
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# greedy acceptance (no drafter rows)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape", [
+    (6, 4, 5, 3000, 0.9, torch.bfloat16),
+    (512, 1, 4, 32, 1.0, torch.float32),       # many tiny-exact-style trials
+    (3, 2, 7, 12344, 1.3, torch.bfloat16),
+])
+def test_greedy_small_shapes(shape):
+    B, K, G, V, T, dt = shape
+    w = _small(B, K, G, V, dtype=dt, T=T, seed=B * 7 + V, p_sigma=2.0 if dt == torch.float32 else 3.0,
+               zipf=dt != torch.float32)
+    gpu, orc = run_gpu(w, seed=9, greedy=True), run_oracle(w, seed=9, greedy=True)
+    assert gpu["status"] == bd.SDV_OK
+    assert gpu["lse"].shape == (B, K, G + 1)
+    assert compare(gpu, orc, tag="greedy %s" % (shape,)) <= max(1, B // 100)
+    # the rejected token is never its own replacement
+    d = w.drafts.cpu().numpy()
+    for b in range(B):
+        L, k = int(gpu["accept_len"][b]), int(gpu["sel"][b])
+        if L < G:
+            assert gpu["next_token"][b] != d[b, k, L]
+
+
+def test_greedy_large_window_sampled():
+    w = synth.workload(5, device="cuda")
+    gpu = run_gpu(w, greedy=True)
+    assert gpu["status"] == bd.SDV_OK
+    seqs = [5, 21]
+    orc = run_oracle(w, seqs, greedy=True)
+    assert compare(gpu, orc, seqs, tag="greedy large-window") <= 1
+    del w
+    torch.cuda.empty_cache()
+
+
+def test_greedy_rejects_shared_q_combination():
+    with pytest.raises(bd.SdvError):
+        bd.Verifier(2, 2, 2, 64, shared_q=True, greedy=True)
