@@ -69,6 +69,13 @@ def lib():
         L.sdvo_verify_greedy.restype = ctypes.c_int
         L.sdvo_accept_ratio_greedy.argtypes = [ctypes.c_double]
         L.sdvo_accept_ratio_greedy.restype = ctypes.c_double
+        L.sdvo_cps_prune_row.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
+                                         ctypes.c_double, ctypes.c_int, vp, vp, dp, dp]
+        L.sdvo_cps_prune_row.restype = ctypes.c_int
+        L.sdvo_cps.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int, vp, vp,
+                               ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
+                               vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
+        L.sdvo_cps.restype = ctypes.c_int
         L.sdvo_max_threads.argtypes = []
         L.sdvo_max_threads.restype = ctypes.c_int
         _lib = L
@@ -239,6 +246,43 @@ def verify_greedy_uniforms(p_logits, drafts, temps, u, w, nthreads=1):
 
 def accept_ratio_greedy(lp):
     return lib().sdvo_accept_ratio_greedy(float(lp))
+
+
+CPS_BAND_MASS, CPS_BAND_BEAM = 1, 2
+
+
+def cps_prune_row(row, T, tau, mmax):
+    """Candidates of one drafter row: (ids, natural-log probs, mass without
+    the last kept token, mass with it)."""
+    row, dt = _row_dtype(row)
+    ids = np.full(mmax, -1, np.int32)
+    lp = np.full(mmax, -np.inf)
+    mb, ma = ctypes.c_double(), ctypes.c_double()
+    n = lib().sdvo_cps_prune_row(_ptr(row), dt, row.shape[-1], float(T), float(tau), int(mmax),
+                                 _ptr(ids), _ptr(lp), ctypes.byref(mb), ctypes.byref(ma))
+    return ids[:n], lp[:n], mb.value, ma.value
+
+
+def cps(q, temps, tau, mmax, beam, eos_id=-1, nthreads=1):
+    """Causal-consistency path search over drafter marginals q [B, gamma, V]
+    (uint16 bf16 words or float32).  Returns a dict: cand_ids, cand_logp,
+    ncand, lat_len, paths, path_logp, npaths, band."""
+    q = np.ascontiguousarray(q)
+    _, dt = _row_dtype(q[..., :1].reshape(-1)[:1])
+    B, G, V = q.shape
+    temps = np.broadcast_to(np.asarray(temps, dtype=np.float64), (B,)).copy()
+    out = dict(cand_ids=np.full((B, G, mmax), -1, np.int32), cand_logp=np.zeros((B, G, mmax)),
+               ncand=np.zeros((B, G), np.int32), lat_len=np.zeros(B, np.int32),
+               paths=np.full((B, beam, G), -1, np.int32), path_logp=np.zeros((B, beam)),
+               npaths=np.zeros(B, np.int32), band=np.zeros(B, np.int32))
+    st = lib().sdvo_cps(B, G, V, dt, _ptr(q), _ptr(temps), float(tau), int(mmax), int(beam),
+                        int(eos_id), _ptr(out["cand_ids"]), _ptr(out["cand_logp"]),
+                        _ptr(out["ncand"]), _ptr(out["lat_len"]), _ptr(out["paths"]),
+                        _ptr(out["path_logp"]), _ptr(out["npaths"]), _ptr(out["band"]),
+                        int(nthreads))
+    if st != 0:
+        raise RuntimeError("oracle cps failed")
+    return out
 
 
 def max_threads():

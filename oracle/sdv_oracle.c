@@ -487,3 +487,192 @@ int sdvo_max_threads(void)
     return 1;
 #endif
 }
+
+
+/* ------------------------------------------------------------------------ */
+/* Causal-consistency path search: candidate pruning and the beam.  Pinned  */
+/* by brute force: the kept set is the smallest most-likely set reaching    */
+/* tau, and the beam equals the exact top paths of the whole lattice.       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    double z;     /* l / T (orders like the probability) */
+    int64_t v;
+} cps_entry_t;
+
+static int cps_cmp(const void* a, const void* b)
+{
+    const cps_entry_t* x = (const cps_entry_t*)a;
+    const cps_entry_t* y = (const cps_entry_t*)b;
+    if (x->z > y->z) return -1;
+    if (x->z < y->z) return 1;
+    return x->v < y->v ? -1 : (x->v > y->v ? 1 : 0);
+}
+
+int sdvo_cps_prune_row(const void* row, int dtype, int64_t V, double T, double tau, int mmax,
+                       int32_t* ids, double* logp, double* mass_before, double* mass_after)
+{
+    double lse = sdvo_row_lse(row, dtype, V, T);
+    cps_entry_t* e = (cps_entry_t*)malloc(sizeof(cps_entry_t) * (size_t)V);
+    if (!e) return -1;
+    for (int64_t v = 0; v < V; ++v) {
+        e[v].z = sdvo_logit(row, dtype, v) / T;
+        e[v].v = v;
+    }
+    qsort(e, (size_t)V, sizeof(cps_entry_t), cps_cmp);
+    double mass = 0.0, before = 0.0;
+    int n = 0;
+    while (n < mmax && n < V) {
+        double lp = e[n].z - lse;
+        ids[n] = (int32_t)e[n].v;
+        logp[n] = lp;
+        before = mass;
+        mass += exp(lp);
+        ++n;
+        if (mass >= tau) break;
+    }
+    if (mass_before) *mass_before = before;
+    if (mass_after) *mass_after = mass;
+    free(e);
+    return n;
+}
+
+/* One beam entry: score and the candidate rank chosen at every position. */
+typedef struct {
+    double score;
+    int32_t* ranks;
+} cps_beam_t;
+
+/* order: score desc, then candidate ranks lexicographically asc */
+static int cps_beam_before(const double sa, const int32_t* ra, const double sb, const int32_t* rb,
+                           int len)
+{
+    if (sa > sb) return 1;
+    if (sa < sb) return 0;
+    for (int i = 0; i < len; ++i) {
+        if (ra[i] < rb[i]) return 1;
+        if (ra[i] > rb[i]) return 0;
+    }
+    return 0;
+}
+
+static int cps_one(int b, int gamma, int64_t V, int dtype, const void* q, double T, double tau,
+                   int mmax, int beam, int32_t eos_id, int32_t* cand_ids, double* cand_logp,
+                   int32_t* ncand, int32_t* lat_len, int32_t* paths, double* path_logp,
+                   int32_t* npaths, int32_t* band_out)
+{
+    size_t elt = dtype == SDVO_BF16 ? 2 : 4;
+    int band = 0;
+    int32_t* ci = cand_ids + (int64_t)b * gamma * mmax;
+    double* cl = cand_logp + (int64_t)b * gamma * mmax;
+    int32_t* nc = ncand + (int64_t)b * gamma;
+    for (int i = 0; i < gamma * mmax; ++i) { ci[i] = -1; cl[i] = -INFINITY; }
+    /* Prune every position; the lattice ends at the first position whose
+     * most likely token is EOS, which is kept alone as the last token. */
+    int Lc = gamma;
+    for (int j = 0; j < gamma; ++j) {
+        const void* row = (const char*)q + (size_t)(((int64_t)b * gamma + j) * V) * elt;
+        double mb = 0.0, ma = 0.0;
+        int n = sdvo_cps_prune_row(row, dtype, V, T, tau, mmax, ci + j * mmax, cl + j * mmax, &mb, &ma);
+        if (n < 0) return -1;
+        nc[j] = n;
+        if (j < Lc && n < mmax && (fabs(ma - tau) <= 1e-5 || fabs(mb - tau) <= 1e-5))
+            band |= SDVO_CPS_BAND_MASS;
+        if (j < Lc && eos_id >= 0 && ci[j * mmax] == eos_id) {
+            Lc = j + 1;
+            nc[j] = 1;
+            for (int i = 1; i < mmax; ++i) { ci[j * mmax + i] = -1; cl[j * mmax + i] = -INFINITY; }
+        }
+    }
+    for (int j = Lc; j < gamma; ++j) {
+        nc[j] = 0;
+        for (int i = 0; i < mmax; ++i) { ci[j * mmax + i] = -1; cl[j * mmax + i] = -INFINITY; }
+    }
+    lat_len[b] = Lc;
+
+    /* Beam search, left to right, keeping the `beam` best prefixes.  The
+     * candidates of a step are scored one by one and kept in a sorted list of
+     * at most `beam + 1` entries (one extra to see the first left out). */
+    const int W = beam;
+    cps_beam_t* cur = (cps_beam_t*)calloc((size_t)W + 1, sizeof(cps_beam_t));
+    cps_beam_t* nxt = (cps_beam_t*)calloc((size_t)W + 1, sizeof(cps_beam_t));
+    int32_t* store = (int32_t*)calloc((size_t)(2 * (W + 1)) * (gamma > 0 ? gamma : 1), sizeof(int32_t));
+    int32_t* tmp = (int32_t*)calloc((size_t)(gamma > 0 ? gamma : 1), sizeof(int32_t));
+    if (!cur || !nxt || !store || !tmp) { free(cur); free(nxt); free(store); free(tmp); return -1; }
+    for (int i = 0; i <= W; ++i) {
+        cur[i].ranks = store + (size_t)i * gamma;
+        nxt[i].ranks = store + (size_t)(W + 1 + i) * gamma;
+    }
+    int ncur = 1;
+    cur[0].score = 0.0;
+    double left_out = -INFINITY;           /* best score left out at the last step */
+    int have_left_out = 0;
+    for (int j = 0; j < Lc; ++j) {
+        int nn = 0;
+        for (int w = 0; w < ncur; ++w) {
+            for (int r = 0; r < nc[j]; ++r) {
+                double sc = cur[w].score + cl[j * mmax + r];
+                for (int i = 0; i < j; ++i) tmp[i] = cur[w].ranks[i];
+                tmp[j] = r;
+                /* insert into nxt (sorted, at most W + 1 entries) */
+                int pos = nn;
+                while (pos > 0 && cps_beam_before(sc, tmp, nxt[pos - 1].score, nxt[pos - 1].ranks, j + 1))
+                    --pos;
+                if (pos > W) continue;
+                int last = nn < W + 1 ? nn : W;
+                int32_t* spare = nxt[last].ranks;
+                for (int i = last; i > pos; --i) nxt[i] = nxt[i - 1];
+                nxt[pos].ranks = spare;
+                nxt[pos].score = sc;
+                for (int i = 0; i <= j; ++i) nxt[pos].ranks[i] = tmp[i];
+                if (nn < W + 1) ++nn;
+            }
+        }
+        have_left_out = nn > W;
+        left_out = have_left_out ? nxt[W].score : -INFINITY;
+        ncur = nn < W ? nn : W;
+        cps_beam_t* t = cur; cur = nxt; nxt = t;
+    }
+    /* band: adjacent kept paths, or the last kept and the first left out,
+     * within 1e-5 but not equal */
+    for (int w = 0; w + 1 < ncur; ++w) {
+        double gap = cur[w].score - cur[w + 1].score;
+        if (gap > 0.0 && gap <= 1e-5 * (1.0 + fabs(cur[w].score))) band |= SDVO_CPS_BAND_BEAM;
+    }
+    if (have_left_out && ncur > 0) {
+        double gap = cur[ncur - 1].score - left_out;
+        if (gap > 0.0 && gap <= 1e-5 * (1.0 + fabs(left_out))) band |= SDVO_CPS_BAND_BEAM;
+    }
+    int32_t* pb = paths + (int64_t)b * W * gamma;
+    double* sb = path_logp + (int64_t)b * W;
+    for (int w = 0; w < W; ++w) {
+        sb[w] = -INFINITY;
+        for (int j = 0; j < gamma; ++j) pb[w * gamma + j] = -1;
+    }
+    for (int w = 0; w < ncur; ++w) {
+        sb[w] = cur[w].score;
+        for (int j = 0; j < Lc; ++j) pb[w * gamma + j] = ci[j * mmax + cur[w].ranks[j]];
+    }
+    npaths[b] = ncur;
+    if (band_out) band_out[b] = band;
+    free(cur); free(nxt); free(store); free(tmp);
+    return 0;
+}
+
+int sdvo_cps(int B, int gamma, int64_t V, int dtype, const void* q, const double* temps,
+             double tau, int mmax, int beam, int32_t eos_id,
+             int32_t* cand_ids, double* cand_logp, int32_t* ncand, int32_t* lat_len,
+             int32_t* paths, double* path_logp, int32_t* npaths, int32_t* band, int nthreads)
+{
+    if (B < 1 || gamma < 1 || V < 1 || mmax < 1 || beam < 1) return -1;
+    int any = 0;
+#ifdef _OPENMP
+    int nt = nthreads > 1 ? nthreads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1) reduction(| : any) if (nt > 1)
+#endif
+    for (int b = 0; b < B; ++b)
+        any |= cps_one(b, gamma, V, dtype, q, temps[b], tau, mmax, beam, eos_id, cand_ids,
+                       cand_logp, ncand, lat_len, paths, path_logp, npaths, band);
+    (void)nthreads;
+    return any;
+}

@@ -154,6 +154,38 @@ int sdvo_verify_greedy(int B, int K, int gamma, int64_t V, int dtype,
                        int32_t* band, int32_t* err, double* resid_mass,
                        int nthreads);
 
+/* ------------------------------------------------------------------------ */
+/* Causal-consistency path search ("DiffuSpec: Unlocking Diffusion Language   */
+/* Models for Speculative Decoding", section 4.2; settings of section 5.3).   */
+/* ------------------------------------------------------------------------ */
+
+/* Band flags of a CPS result (one word per sequence). */
+#define SDVO_CPS_BAND_MASS 1   /* a cumulative mass within 1e-5 of tau at a cut  */
+#define SDVO_CPS_BAND_BEAM 2   /* two distinct paths within 1e-5 around the top W */
+
+/* Candidates of one drafter row: softmax(l / T), tokens in order of
+ * (probability desc, id asc); keep the shortest prefix whose mass reaches tau,
+ * at most mmax tokens.  Writes ids and natural-log probabilities, returns the
+ * count (>= 1); *mass_before / *mass_after get the mass without / with the
+ * last kept token (for the band check). */
+int sdvo_cps_prune_row(const void* row, int dtype, int64_t V, double T, double tau, int mmax,
+                       int32_t* ids, double* logp, double* mass_before, double* mass_after);
+
+/* Pruning of every row of q [B][gamma][V], the lattice cut at the first
+ * position whose most likely token is eos_id (kept as the last token; eos_id <
+ * 0: no cut), and a left-to-right beam of width `beam` over the lattice,
+ * scoring a path by the sum of its log-probabilities (drafter confidence).
+ * Ties go to the path whose candidate ranks come first lexicographically.
+ * With this separable score the beam returns the exact `beam` best paths.
+ * Outputs: cand_ids / cand_logp [B][gamma][mmax] (-1 / -inf past the count),
+ * ncand [B][gamma] (0 past the lattice), lat_len [B], paths [B][beam][gamma]
+ * (-1 past the lattice), path_logp [B][beam] (-inf for missing paths),
+ * npaths [B], band [B] (may be NULL). */
+int sdvo_cps(int B, int gamma, int64_t V, int dtype, const void* q, const double* temps,
+             double tau, int mmax, int beam, int32_t eos_id,
+             int32_t* cand_ids, double* cand_logp, int32_t* ncand, int32_t* lat_len,
+             int32_t* paths, double* path_logp, int32_t* npaths, int32_t* band, int nthreads);
+
 /* Number of threads the build can run (1 without OpenMP). */
 int sdvo_max_threads(void);
 

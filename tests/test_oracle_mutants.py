@@ -46,6 +46,14 @@ MUTANTS = [
      "r[v] = exp(sdvo_logit(prow, dtype, v) / T - lse_p);", 1),
     ("greedy_zeroes_wrong_token", "const int32_t xr = drafts[((int64_t)b * K + sel) * G + L];",
      "const int32_t xr = drafts[((int64_t)b * K + sel) * G + (L + 1) % G];", 1),
+    ("cps_ties_to_higher_id", "return x->v < y->v ? -1 : (x->v > y->v ? 1 : 0);",
+     "return x->v > y->v ? -1 : (x->v < y->v ? 1 : 0);", 1),
+    ("cps_prune_ignores_temperature", "e[v].z = sdvo_logit(row, dtype, v) / T;",
+     "e[v].z = sdvo_logit(row, dtype, v);", 1),
+    ("cps_eos_dropped", "            Lc = j + 1;", "            Lc = j;", 1),
+    ("cps_score_not_accumulated", "double sc = cur[w].score + cl[j * mmax + r];",
+     "double sc = cl[j * mmax + r];", 1),
+    ("cps_beam_one_short", "ncur = nn < W ? nn : W;", "ncur = nn < W ? nn : (W > 1 ? W - 1 : 1);", 1),
 ]
 
 
@@ -64,6 +72,7 @@ def test_pins_catch_mutant(name, old, new, count, tmp_path):
     env = dict(os.environ, SDV_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_greedy_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_greedy_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_cps_pins.py")],
                        env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-1500:])
