@@ -513,6 +513,13 @@ int sdvo_cps_prune_row(const void* row, int dtype, int64_t V, double T, double t
                        int32_t* ids, double* logp, double* mass_before, double* mass_after)
 {
     double lse = sdvo_row_lse(row, dtype, V, T);
+    if (!isfinite(lse)) {
+        /* NaN / +inf logits, or no token of positive probability: the row
+         * offers no candidates */
+        if (mass_before) *mass_before = 0.0;
+        if (mass_after) *mass_after = 0.0;
+        return 0;
+    }
     cps_entry_t* e = (cps_entry_t*)malloc(sizeof(cps_entry_t) * (size_t)V);
     if (!e) return -1;
     for (int64_t v = 0; v < V; ++v) {
@@ -523,6 +530,7 @@ int sdvo_cps_prune_row(const void* row, int dtype, int64_t V, double T, double t
     double mass = 0.0, before = 0.0;
     int n = 0;
     while (n < mmax && n < V) {
+        if (e[n].z == -INFINITY) break;       /* probability zero: never a candidate */
         double lp = e[n].z - lse;
         ids[n] = (int32_t)e[n].v;
         logp[n] = lp;
@@ -576,7 +584,9 @@ static int cps_one(int b, int gamma, int64_t V, int dtype, const void* q, double
         int n = sdvo_cps_prune_row(row, dtype, V, T, tau, mmax, ci + j * mmax, cl + j * mmax, &mb, &ma);
         if (n < 0) return -1;
         nc[j] = n;
-        if (j < Lc && n < mmax && (fabs(ma - tau) <= 1e-5 || fabs(mb - tau) <= 1e-5))
+        /* band: the decision to stop (mass with the last kept token reaches
+         * tau) or to go on (mass before it was below tau) was within 1e-5 */
+        if (j < Lc && ((n < mmax && fabs(ma - tau) <= 1e-5) || (n > 1 && fabs(mb - tau) <= 1e-5)))
             band |= SDVO_CPS_BAND_MASS;
         if (j < Lc && eos_id >= 0 && ci[j * mmax] == eos_id) {
             Lc = j + 1;

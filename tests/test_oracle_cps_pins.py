@@ -96,3 +96,26 @@ def test_single_candidate_lattice_is_argmax(oracle_lib):
     out = oracle_lib.cps(q, 1.0, 0.0, 8, 4)
     assert (out["ncand"] == 1).all() and (out["npaths"] == 1).all()
     assert (out["paths"][:, 0] == q.argmax(-1)).all()
+
+
+def test_zero_probability_tokens_and_bad_rows(oracle_lib):
+    """A token of probability zero (logit -inf) adds no mass and is never a
+    candidate; a row with a NaN or +inf logit, or with no finite logit, has no
+    probability distribution and offers no candidates, so no path exists."""
+    row = np.full(20, -np.inf, np.float32)
+    row[[4, 9, 13]] = [1.0, 3.0, 2.0]
+    ids, lp, before, after = oracle_lib.cps_prune_row(row, 1.0, 1.0, 15)
+    assert list(ids) == [9, 13, 4]                     # all finite tokens, nothing else
+    assert after == pytest.approx(1.0, rel=1e-14)
+    np.testing.assert_allclose(np.exp(lp), _probs(row[[9, 13, 4]], 1.0), rtol=1e-12)
+    for bad in (np.nan, np.inf):
+        r2 = row.copy()
+        r2[0] = bad
+        assert len(oracle_lib.cps_prune_row(r2, 1.0, 0.8, 15)[0]) == 0
+    assert len(oracle_lib.cps_prune_row(np.full(8, -np.inf, np.float32), 1.0, 0.8, 15)[0]) == 0
+    q = np.random.default_rng(42).standard_normal((2, 3, 16)).astype(np.float32)
+    q[1, 1, 5] = np.nan
+    out = oracle_lib.cps(q, 1.0, 0.8, 6, 3)
+    assert out["ncand"][1, 1] == 0 and out["npaths"][1] == 0
+    assert (out["paths"][1] == -1).all() and np.isneginf(out["path_logp"][1]).all()
+    assert out["npaths"][0] >= 1
