@@ -76,6 +76,10 @@ def lib():
                                ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
                                vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
         L.sdvo_cps.restype = ctypes.c_int
+        L.sdvo_adl_state_words.argtypes = [ctypes.c_int]
+        L.sdvo_adl_state_words.restype = ctypes.c_int
+        L.sdvo_adl_step.argtypes = [ctypes.c_int] * 6 + [vp, vp, vp, vp]
+        L.sdvo_adl_step.restype = ctypes.c_int
         L.sdvo_max_threads.argtypes = []
         L.sdvo_max_threads.restype = ctypes.c_int
         _lib = L
@@ -248,7 +252,7 @@ def accept_ratio_greedy(lp):
     return lib().sdvo_accept_ratio_greedy(float(lp))
 
 
-CPS_BAND_MASS, CPS_BAND_BEAM = 1, 2
+CPS_BAND_MASS = 1
 
 
 def cps_prune_row(row, T, tau, mmax):
@@ -283,6 +287,25 @@ def cps(q, temps, tau, mmax, beam, eos_id=-1, nthreads=1):
     if st != 0:
         raise RuntimeError("oracle cps failed")
     return out
+
+
+def adl_state(B, W):
+    """Zeroed controller state for B sequences and window W."""
+    return np.zeros((B, lib().sdvo_adl_state_words(int(W))), np.int32)
+
+
+def adl_step(k, gen_len, acc_len, state, W=1, kmin=1, kmax=64, up=2, down=1):
+    """One adaptive-draft-length step: returns the next draft lengths [B] and
+    updates `state` (from adl_state) in place."""
+    k = np.ascontiguousarray(k, dtype=np.int32).copy()
+    g = np.ascontiguousarray(gen_len, dtype=np.int32)
+    a = np.ascontiguousarray(acc_len, dtype=np.int32)
+    assert state.dtype == np.int32 and state.flags.c_contiguous
+    st = lib().sdvo_adl_step(len(k), int(W), int(kmin), int(kmax), int(up), int(down), _ptr(g),
+                             _ptr(a), _ptr(k), _ptr(state))
+    if st != 0:
+        raise ValueError("oracle adl_step: invalid parameters")
+    return k
 
 
 def max_threads():

@@ -545,18 +545,21 @@ int sdvo_cps_prune_row(const void* row, int dtype, int64_t V, double T, double t
     return n;
 }
 
-/* One beam entry: score and the candidate rank chosen at every position. */
+/* One beam entry: the order key (sum of the chosen tokens' raw logits), the
+ * score (sum of their log-probabilities) and the candidate rank chosen at
+ * every position. */
 typedef struct {
+    double key;
     double score;
     int32_t* ranks;
 } cps_beam_t;
 
-/* order: score desc, then candidate ranks lexicographically asc */
-static int cps_beam_before(const double sa, const int32_t* ra, const double sb, const int32_t* rb,
+/* order: key desc, then candidate ranks lexicographically asc */
+static int cps_beam_before(const double ka, const int32_t* ra, const double kb, const int32_t* rb,
                            int len)
 {
-    if (sa > sb) return 1;
-    if (sa < sb) return 0;
+    if (ka > kb) return 1;
+    if (ka < kb) return 0;
     for (int i = 0; i < len; ++i) {
         if (ra[i] < rb[i]) return 1;
         if (ra[i] > rb[i]) return 0;
@@ -600,58 +603,57 @@ static int cps_one(int b, int gamma, int64_t V, int dtype, const void* q, double
     }
     lat_len[b] = Lc;
 
-    /* Beam search, left to right, keeping the `beam` best prefixes.  The
-     * candidates of a step are scored one by one and kept in a sorted list of
-     * at most `beam + 1` entries (one extra to see the first left out). */
+    /* Beam search, left to right, keeping the `beam` best prefixes.  A path's
+     * score is the sum of its log-probabilities, l_j(x_j) / T - lse_j; the
+     * temperature and every position's normaliser are shared by all paths of
+     * the sequence, so paths rank as the sums of their raw logits, taken
+     * left to right in fp64 (exact for bf16 logits).  The candidates of a
+     * step are taken one by one into a sorted list of at most `beam`. */
     const int W = beam;
     cps_beam_t* cur = (cps_beam_t*)calloc((size_t)W + 1, sizeof(cps_beam_t));
     cps_beam_t* nxt = (cps_beam_t*)calloc((size_t)W + 1, sizeof(cps_beam_t));
     int32_t* store = (int32_t*)calloc((size_t)(2 * (W + 1)) * (gamma > 0 ? gamma : 1), sizeof(int32_t));
     int32_t* tmp = (int32_t*)calloc((size_t)(gamma > 0 ? gamma : 1), sizeof(int32_t));
-    if (!cur || !nxt || !store || !tmp) { free(cur); free(nxt); free(store); free(tmp); return -1; }
+    double* rl = (double*)calloc((size_t)gamma * mmax, sizeof(double));
+    if (!cur || !nxt || !store || !tmp || !rl) {
+        free(cur); free(nxt); free(store); free(tmp); free(rl);
+        return -1;
+    }
+    for (int j = 0; j < Lc; ++j) {
+        const void* row = (const char*)q + (size_t)(((int64_t)b * gamma + j) * V) * elt;
+        for (int r = 0; r < nc[j]; ++r) rl[j * mmax + r] = sdvo_logit(row, dtype, ci[j * mmax + r]);
+    }
     for (int i = 0; i <= W; ++i) {
         cur[i].ranks = store + (size_t)i * gamma;
         nxt[i].ranks = store + (size_t)(W + 1 + i) * gamma;
     }
     int ncur = 1;
+    cur[0].key = 0.0;
     cur[0].score = 0.0;
-    double left_out = -INFINITY;           /* best score left out at the last step */
-    int have_left_out = 0;
     for (int j = 0; j < Lc; ++j) {
         int nn = 0;
         for (int w = 0; w < ncur; ++w) {
             for (int r = 0; r < nc[j]; ++r) {
-                double sc = cur[w].score + cl[j * mmax + r];
+                double key = cur[w].key + rl[j * mmax + r];
                 for (int i = 0; i < j; ++i) tmp[i] = cur[w].ranks[i];
                 tmp[j] = r;
-                /* insert into nxt (sorted, at most W + 1 entries) */
+                /* insert into nxt (sorted, at most W entries) */
                 int pos = nn;
-                while (pos > 0 && cps_beam_before(sc, tmp, nxt[pos - 1].score, nxt[pos - 1].ranks, j + 1))
+                while (pos > 0 && cps_beam_before(key, tmp, nxt[pos - 1].key, nxt[pos - 1].ranks, j + 1))
                     --pos;
-                if (pos > W) continue;
-                int last = nn < W + 1 ? nn : W;
+                if (pos >= W) continue;
+                int last = nn < W ? nn : W - 1;
                 int32_t* spare = nxt[last].ranks;
                 for (int i = last; i > pos; --i) nxt[i] = nxt[i - 1];
                 nxt[pos].ranks = spare;
-                nxt[pos].score = sc;
+                nxt[pos].key = key;
+                nxt[pos].score = cur[w].score + cl[j * mmax + r];
                 for (int i = 0; i <= j; ++i) nxt[pos].ranks[i] = tmp[i];
-                if (nn < W + 1) ++nn;
+                if (nn < W) ++nn;
             }
         }
-        have_left_out = nn > W;
-        left_out = have_left_out ? nxt[W].score : -INFINITY;
-        ncur = nn < W ? nn : W;
+        ncur = nn;
         cps_beam_t* t = cur; cur = nxt; nxt = t;
-    }
-    /* band: adjacent kept paths, or the last kept and the first left out,
-     * within 1e-5 but not equal */
-    for (int w = 0; w + 1 < ncur; ++w) {
-        double gap = cur[w].score - cur[w + 1].score;
-        if (gap > 0.0 && gap <= 1e-5 * (1.0 + fabs(cur[w].score))) band |= SDVO_CPS_BAND_BEAM;
-    }
-    if (have_left_out && ncur > 0) {
-        double gap = cur[ncur - 1].score - left_out;
-        if (gap > 0.0 && gap <= 1e-5 * (1.0 + fabs(left_out))) band |= SDVO_CPS_BAND_BEAM;
     }
     int32_t* pb = paths + (int64_t)b * W * gamma;
     double* sb = path_logp + (int64_t)b * W;
@@ -665,7 +667,70 @@ static int cps_one(int b, int gamma, int64_t V, int dtype, const void* q, double
     }
     npaths[b] = ncur;
     if (band_out) band_out[b] = band;
-    free(cur); free(nxt); free(store); free(tmp);
+    free(cur); free(nxt); free(store); free(tmp); free(rl);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Adaptive draft length.  Pinned by hand-worked traces of the rule (growth */
+/* to the cap, holding under EOS saturation, shrinking to the floor, the    */
+/* window's averaging) and by its invariants.                               */
+/* ------------------------------------------------------------------------ */
+
+/* state layout: [0] steps seen, then W entries of (k, g, a) in a ring */
+int sdvo_adl_state_words(int W)
+{
+    return 1 + 3 * W;
+}
+
+int sdvo_adl_step(int B, int W, int kmin, int kmax, int up, int down, const int32_t* gen_len,
+                  const int32_t* acc_len, int32_t* k, int32_t* state)
+{
+    if (B < 0 || W < 1 || kmin < 1 || kmax < kmin || up < 0 || down < 0) return -1;
+    for (int b = 0; b < B; ++b)
+        if (k[b] < kmin || k[b] > kmax) return -1;
+    const int words = sdvo_adl_state_words(W);
+    for (int b = 0; b < B; ++b) {
+        int32_t* st = state + (int64_t)b * words;
+        int64_t kb = k[b];
+        /* this step's lengths, clamped to what a step can produce */
+        int64_t g = gen_len[b];
+        if (g < 0) g = 0;
+        if (g > kb) g = kb;
+        int64_t a = acc_len[b];
+        if (a < 0) a = 0;
+        if (a > g) a = g;
+        /* record the step in the window */
+        int64_t seen = st[0];
+        int slot = (int)(seen % W);
+        st[1 + 3 * slot + 0] = (int32_t)kb;
+        st[1 + 3 * slot + 1] = (int32_t)g;
+        st[1 + 3 * slot + 2] = (int32_t)a;
+        seen += 1;
+        /* once the window is full the counter stays in [W, 2W): W + the ring
+         * position of the next slot, so it never overflows */
+        st[0] = (int32_t)(seen < W ? seen : W + (seen % W));
+        /* averages over the window, compared as sums */
+        int n = seen < W ? (int)seen : W;
+        int64_t sk = 0, sg = 0, sa = 0;
+        for (int i = 0; i < n; ++i) {
+            sk += st[1 + 3 * i + 0];
+            sg += st[1 + 3 * i + 1];
+            sa += st[1 + 3 * i + 2];
+        }
+        int keeps_pace = sa >= sg;
+        int fills = sg >= sk;
+        int64_t next;
+        if (keeps_pace && fills)
+            next = kb + up;           /* expand */
+        else if (keeps_pace)
+            next = kb;                /* generation saturated: hold */
+        else
+            next = kb - down;         /* acceptance falls behind: shrink */
+        if (next > kmax) next = kmax;
+        if (next < kmin) next = kmin;
+        k[b] = (int32_t)next;
+    }
     return 0;
 }
 

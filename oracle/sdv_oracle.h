@@ -161,13 +161,13 @@ int sdvo_verify_greedy(int B, int K, int gamma, int64_t V, int dtype,
 
 /* Band flags of a CPS result (one word per sequence). */
 #define SDVO_CPS_BAND_MASS 1   /* a cumulative mass within 1e-5 of tau at a cut  */
-#define SDVO_CPS_BAND_BEAM 2   /* two distinct paths within 1e-5 around the top W */
 
 /* Candidates of one drafter row: softmax(l / T), tokens in order of
  * (probability desc, id asc); keep the shortest prefix whose mass reaches tau,
- * at most mmax tokens.  Writes ids and natural-log probabilities, returns the
- * count (>= 1); *mass_before / *mass_after get the mass without / with the
- * last kept token (for the band check). */
+ * at most mmax tokens; a token of probability zero is never kept.  Writes ids
+ * and natural-log probabilities, returns the count (0 for a row with a NaN or
+ * +inf logit or none finite); *mass_before / *mass_after get the mass without
+ * / with the last kept token (for the band check). */
 int sdvo_cps_prune_row(const void* row, int dtype, int64_t V, double T, double tau, int mmax,
                        int32_t* ids, double* logp, double* mass_before, double* mass_after);
 
@@ -175,8 +175,11 @@ int sdvo_cps_prune_row(const void* row, int dtype, int64_t V, double T, double t
  * position whose most likely token is eos_id (kept as the last token; eos_id <
  * 0: no cut), and a left-to-right beam of width `beam` over the lattice,
  * scoring a path by the sum of its log-probabilities (drafter confidence).
- * Ties go to the path whose candidate ranks come first lexicographically.
- * With this separable score the beam returns the exact `beam` best paths.
+ * Paths rank as the sums of their raw logits (the temperature and the
+ * positions' normalisers are common to all paths), summed left to right in
+ * fp64; ties go to the path whose candidate ranks come first
+ * lexicographically.  With this separable score the beam returns the exact
+ * `beam` best paths.
  * Outputs: cand_ids / cand_logp [B][gamma][mmax] (-1 / -inf past the count),
  * ncand [B][gamma] (0 past the lattice), lat_len [B], paths [B][beam][gamma]
  * (-1 past the lattice), path_logp [B][beam] (-inf for missing paths),
@@ -185,6 +188,29 @@ int sdvo_cps(int B, int gamma, int64_t V, int dtype, const void* q, const double
              double tau, int mmax, int beam, int32_t eos_id,
              int32_t* cand_ids, double* cand_logp, int32_t* ncand, int32_t* lat_len,
              int32_t* paths, double* path_logp, int32_t* npaths, int32_t* band, int nthreads);
+
+/* ------------------------------------------------------------------------ */
+/* Adaptive draft length ("DiffuSpec", section 4.3; appendix C).  The page  */
+/* gives the controller's inputs and direction, not a formula.  Reading:    */
+/* over the last W steps of a sequence (k_i drafted, g_i generated up to    */
+/* and including the first EOS, a_i accepted), acceptance keeps pace when   */
+/* sum a >= sum g, and generation fills the drafts when sum g >= sum k.     */
+/* Then k grows by `up` (at most kmax); if acceptance keeps pace but        */
+/* generation saturates (EOS before the draft end), k holds; if acceptance  */
+/* falls behind, k shrinks by `down` (at least kmin).  Inputs are clamped   */
+/* to 0 <= g <= k and 0 <= a <= g before they enter the window.             */
+/* ------------------------------------------------------------------------ */
+
+/* Number of int32 words of one sequence's controller state for window W. */
+int sdvo_adl_state_words(int W);
+
+/* One step for B sequences: k [B] holds the draft length each sequence just
+ * used and receives the next one; gen_len / acc_len [B] are that step's
+ * generated and accepted lengths; state [B][sdvo_adl_state_words(W)] starts
+ * zeroed.  Returns 0, or -1 for invalid parameters (W < 1, kmin < 1,
+ * kmax < kmin, up < 0, down < 0, a k outside [kmin, kmax]). */
+int sdvo_adl_step(int B, int W, int kmin, int kmax, int up, int down, const int32_t* gen_len,
+                  const int32_t* acc_len, int32_t* k, int32_t* state);
 
 /* Number of threads the build can run (1 without OpenMP). */
 int sdvo_max_threads(void);

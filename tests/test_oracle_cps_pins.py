@@ -12,6 +12,7 @@ per-position log-probabilities, the beam must return the exact best paths of
 the whole lattice.
 """
 import itertools
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -46,32 +47,43 @@ def test_prune_invariants(oracle_lib, V, T, tau, mmax):
             assert p[a] > p[b] or (p[a] == p[b] and a < b)
 
 
-def _lattice_best(cand_logp, ncand, L, W):
-    """All paths of the lattice, best first: score desc, then ranks lexicographic."""
+def _lattice_best(q_b, cand_ids, ncand, L, W):
+    """All paths of the lattice, best first, in exact arithmetic: a path's
+    score is sum_j (l_j(x_j) / T - lse_j), so with T and the lse_j common to
+    every path the order is that of the exact sum of the raw logits
+    (fractions); equal sums go to the lexicographically first candidate
+    ranks."""
     paths = []
     for ranks in itertools.product(*[range(ncand[j]) for j in range(L)]):
-        score = sum(cand_logp[j, r] for j, r in enumerate(ranks))
-        paths.append((-score, ranks))
+        key = sum(Fraction(float(q_b[j, cand_ids[j, r]])) for j, r in enumerate(ranks))
+        paths.append((-key, ranks))
     paths.sort()
     return paths[:W]
 
 
 @pytest.mark.parametrize("W", [1, 3, 7])
-def test_beam_is_exact_top_paths(oracle_lib, W):
-    rng = np.random.default_rng(30 + W)
-    B, G, V = 6, 4, 10
+@pytest.mark.parametrize("grid", [False, True])
+def test_beam_is_exact_top_paths(oracle_lib, W, grid):
+    """With logits on a coarse grid (as bf16 logits are) many paths tie
+    exactly; the tie rule must then decide, not rounding."""
+    rng = np.random.default_rng(30 + W + 10 * grid)
+    B, G, V, T = 6, 4, 10, 0.7
     q = (rng.standard_normal((B, G, V)) * 1.5).astype(np.float32)
+    if grid:
+        q = np.round(q * 4) / 4
     q[0, 1, :3] = 2.0                                        # tied candidates
-    out = oracle_lib.cps(q, 1.0, 0.9, 4, W)
+    out = oracle_lib.cps(q, T, 0.9, 4, W)
     for b in range(B):
         L = out["lat_len"][b]
         assert L == G
-        best = _lattice_best(out["cand_logp"][b], out["ncand"][b], L, W)
+        best = _lattice_best(q[b], out["cand_ids"][b], out["ncand"][b], L, W)
         assert out["npaths"][b] == len(best)
-        for w, (negs, ranks) in enumerate(best):
+        for w, (negkey, ranks) in enumerate(best):
             ids = [out["cand_ids"][b, j, r] for j, r in enumerate(ranks)]
             assert list(out["paths"][b, w, :L]) == ids
-            assert out["path_logp"][b, w] == pytest.approx(-negs, rel=1e-12)
+            # the reported score is the path's log-probability
+            lp = sum(np.log(_probs(q[b, j], T)[i]) for j, i in enumerate(ids))
+            assert out["path_logp"][b, w] == pytest.approx(lp, rel=1e-12, abs=1e-12)
 
 
 def test_eos_cuts_the_lattice(oracle_lib):

@@ -51,9 +51,21 @@ MUTANTS = [
     ("cps_prune_ignores_temperature", "e[v].z = sdvo_logit(row, dtype, v) / T;",
      "e[v].z = sdvo_logit(row, dtype, v);", 1),
     ("cps_eos_dropped", "            Lc = j + 1;", "            Lc = j;", 1),
-    ("cps_score_not_accumulated", "double sc = cur[w].score + cl[j * mmax + r];",
-     "double sc = cl[j * mmax + r];", 1),
-    ("cps_beam_one_short", "ncur = nn < W ? nn : W;", "ncur = nn < W ? nn : (W > 1 ? W - 1 : 1);", 1),
+    ("cps_key_not_accumulated", "double key = cur[w].key + rl[j * mmax + r];",
+     "double key = rl[j * mmax + r];", 1),
+    ("cps_score_not_accumulated", "nxt[pos].score = cur[w].score + cl[j * mmax + r];",
+     "nxt[pos].score = cl[j * mmax + r];", 1),
+    ("cps_beam_one_short", "if (pos >= W) continue;", "if (pos >= (W > 1 ? W - 1 : 1)) continue;", 1),
+    ("cps_ties_lexicographic_last", "        if (ra[i] < rb[i]) return 1;\n        if (ra[i] > rb[i]) return 0;",
+     "        if (ra[i] > rb[i]) return 1;\n        if (ra[i] < rb[i]) return 0;", 1),
+    ("cps_keeps_zero_probability", "        if (e[n].z == -INFINITY) break;", "", 1),
+    ("adl_pace_strict", "int keeps_pace = sa >= sg;", "int keeps_pace = sa > sg;", 1),
+    ("adl_ignores_saturation", "int fills = sg >= sk;", "int fills = 1;", 1),
+    ("adl_no_clamp_of_generated", "        if (g > kb) g = kb;", "", 1),
+    ("adl_saturation_shrinks", "            next = kb;                /* generation saturated: hold */",
+     "            next = kb - down;", 1),
+    ("adl_window_one_short", "int n = seen < W ? (int)seen : W;", "int n = seen < W ? (int)seen : W - 1;", 1),
+    ("adl_no_clamp_of_accepted", "        if (a > g) a = g;", "", 1),
 ]
 
 
@@ -73,6 +85,7 @@ def test_pins_catch_mutant(name, old, new, count, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_greedy_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_cps_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_cps_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_adl_pins.py")],
                        env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-1500:])
