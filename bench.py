@@ -41,6 +41,8 @@ UNIT = "draft-tokens/s"
 DEFAULT_WORKLOAD = 5
 ROWPASS_SOURCES = ["k1_rowpass.cu", "sdv_device.cuh"]
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "rowpass_large-window.md")
+CPS_SOURCES = ["k4_cps.cu", "sdv_device.cuh"]
+CPS_TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "cps_prune_large-window.md")
 
 
 def parse_args():
@@ -50,6 +52,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["sdv", "reference"], default="sdv")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--cps", action="store_true",
+                    help="time the causal-consistency path search on the large-window marginals")
     ap.add_argument("--greedy", action="store_true",
                     help="greedy acceptance: verifier rows only, no drafter rows")
     ap.add_argument("--shared-q", action="store_true",
@@ -170,25 +174,28 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def rowpass_source_sha() -> str:
+def source_sha(sources) -> str:
     h = hashlib.sha256()
-    for f in ROWPASS_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "draft_verification_sdv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def traffic_per_row():
-    """DRAM bytes per logit row of the row-pass kernel from the committed ncu
-    summary, or None when that summary is absent or predates the kernel."""
+def traffic_per_row(profile: str = None, sources=None):
+    """DRAM bytes per logit row of a kernel (default: the row pass) from its
+    committed ncu summary, or None when that summary is absent or predates the
+    kernel's sources."""
+    profile = profile or TRAFFIC_PROFILE
+    sources = sources or ROWPASS_SOURCES
     try:
         kv = {}
-        with open(TRAFFIC_PROFILE) as f:
+        with open(profile) as f:
             for line in f:
                 if ":" in line and line.strip().startswith(("kernel_source_sha256", "dram_bytes_per_row")):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip().strip("`")
-        if kv.get("kernel_source_sha256") != rowpass_source_sha():
+        if kv.get("kernel_source_sha256") != source_sha(sources):
             return None
         return float(kv["dram_bytes_per_row"])
     except Exception:
@@ -355,6 +362,123 @@ def run_sdv(args, rank, world, local):
     return result
 
 
+def run_cps(args, rank, world):
+    """Path search over the drafter marginals of the large-window shape
+    (B 32, gamma 32, V 152064 bf16, per-sequence temperatures): beam 3, at most
+    15 candidates, mass 0.8.  One step = sdv_cps (pruning of every row, then
+    the beam).  The q rows (311 MB) exceed the L2, so no flush is needed."""
+    from draft_verification_sdv_gb300 import binding as bd
+    bd.load(build=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = synth.workload_shared(B=args.batch or 32, device=dev, seed=55 + 1000 * rank)
+    q, temps = w.q_logits, w.temps
+    del w
+    torch.cuda.empty_cache()
+    B, G, V = q.shape
+    tau, mmax, beam = 0.8, 15, 3
+    stream = torch.cuda.current_stream(dev)
+    out = bd.sdv_cps(q, tau, mmax, beam, temps=temps)
+
+    def step():
+        bd.sdv_cps(q, tau, mmax, beam, temps=temps, out=out)
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.25)
+    barrier(world)
+    t0 = time.time()
+    ms = timed(step, args.steps)
+    t1 = time.time()
+    ms = max_over_ranks(ms, world)
+    # the two kernels timed alone, same events on the launching stream
+    lat = {k: out[k] for k in ("cand_ids", "cand_logp", "cand_logit", "ncand")}
+    ms_prune = timed(lambda: bd.sdv_cps_prune(q, tau, mmax, temps=temps, out=lat), args.steps)
+    ms_beam = timed(lambda: bd.sdv_cps_beam(lat, V, beam), args.steps)
+    time.sleep(0.2)
+    clocks.stop()
+    row_bytes = q.numel() * q.element_size()
+    peak, kind = measured_peaks()
+    gbs = row_bytes / (ms_prune * 1e-3) / 1e9
+    tpr = traffic_per_row(CPS_TRAFFIC_PROFILE, CPS_SOURCES)
+    res = {"metric": "drafter rows pruned and beam-searched per second (causal-consistency path search)",
+           "value": world * B * G / (ms * 1e-3), "unit": "rows/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "input_dtype": "bf16", "data": "synthetic drafter marginals (seeded; no model weights)",
+           "config": {"workload": "large-window marginals B%d gamma%d V%d bf16" % (B, G, V),
+                      "beam": beam, "mmax": mmax, "tau": tau,
+                      "temperatures": "per-sequence {0.6, 1.0}",
+                      "l2": "inputs %.2f GB > L2 (126 MB): no flush" % (row_bytes / 1e9),
+                      "parallelism": "replicas (one batch per GPU)" if world > 1 else "1 GPU"},
+           "kernel_ms": {"prune": ms_prune, "beam": ms_beam,
+                         "how": "each half timed alone over the same number of steps"},
+           "roofline": {"bound": "hbm", "kernel": "cps_prune_kernel (one streaming pass per row)",
+                        "achieved": round(gbs, 1), "peak": peak, "peak_kind": kind,
+                        "unit": "GB/s", "frac": round(gbs / peak, 4),
+                        "traffic": round(tpr * B * G) if tpr else None,
+                        "algorithmic_bytes_per_launch": row_bytes,
+                        "ms_per_launch": round(ms_prune, 5)},
+           "gpu_launches": 2 * args.steps,
+           "clocks": clocks.summary(t0, t1)}
+    if not args.no_e2e:
+        # host marginals in pinned memory, copied in each step; paths read back
+        hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        hq.copy_(q)
+        ht = temps.cpu().pin_memory()
+        dq, dt_ = torch.empty_like(q), torch.empty_like(temps)
+        hp = torch.empty((B, beam, G), dtype=torch.int32, pin_memory=True)
+        hs = torch.empty((B, beam), dtype=torch.float32, pin_memory=True)
+        hn = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dt_.copy_(ht, non_blocking=True)
+            bd.sdv_cps(dq, tau, mmax, beam, temps=dt_, out=out)
+            hp.copy_(out["paths"], non_blocking=True)
+            hs.copy_(out["path_logp"], non_blocking=True)
+            hn.copy_(out["npaths"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        e2e_step()
+        barrier(world)
+        te0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        te = max_over_ranks(time.perf_counter() - te0, world)
+        res["e2e"] = {"value": world * B * G * args.e2e_steps / te, "unit": "rows/s",
+                      "h2d_bytes_per_step": row_bytes + ht.numel() * 4,
+                      "d2h_bytes_per_step": hp.numel() * 4 + hs.numel() * 4 + hn.numel() * 4,
+                      "steps": args.e2e_steps, "ms_per_step": te * 1e3 / args.e2e_steps}
+        del hq, dq
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        S = max(1, min(os.cpu_count() or 1, B, 8))
+        hq = q[:S].cpu()
+        hq = hq.view(torch.int16).numpy().view("uint16") if q.dtype == torch.bfloat16 else hq.numpy()
+        nt = min(S, oracle.max_threads()) if oracle.max_threads() > 1 else 1
+        c0 = time.perf_counter()
+        oracle.cps(hq, temps[:S].cpu().numpy(), tau, mmax, beam, nthreads=nt)
+        dtc = time.perf_counter() - c0
+        res["cpu_baseline"] = {"value": S * G / dtc, "unit": "rows/s", "cores": nt, "kind": "oracle",
+                               "sample": "first %d of %d sequences (%d rows), one thread per "
+                                         "sequence (%.1f s wall)" % (S, B, S * G, dtc)}
+    return res
+
+
 def cpu_baseline(w: synth.Workload):
     import oracle
     cores = os.cpu_count() or 1
@@ -435,7 +559,7 @@ def main():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
     rank, world, local = dist_setup()
-    res = run_sdv(args, rank, world, local)
+    res = run_cps(args, rank, world) if args.cps else run_sdv(args, rank, world, local)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

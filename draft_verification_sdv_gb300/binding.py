@@ -26,6 +26,7 @@ SDV_FLAG_GREEDY = 2
 STATUS_NAMES = {0: "SDV_OK", 1: "SDV_ERR_ARG", 2: "SDV_ERR_CUDA", 3: "SDV_ERR_OOM",
                 4: "SDV_ERR_DEVICE_DATA", 5: "SDV_ERR_SCRATCH"}
 STATIC_SCRATCH_BYTES = 8 << 20
+SDV_STATUS_BAD_LENGTH = 16
 
 # Every entry point of include/sdv.h, with its ctypes signature.
 _VP, _I, _I64, _U64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
@@ -44,6 +45,13 @@ SIGNATURES = {
     "sdv_profile_enable": (_I, [_VP, _I]),
     "sdv_profile_read": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_I)]),
     "sdv_verify_static": (_I, [_I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
+    "sdv_cps": (_I, [_I, _I, _I, _I, _VP, _VP, _F, _VP, _F, _I, _I, _I, _VP, _VP, _VP, _VP, _VP,
+                     _VP, _VP, _VP]),
+    "sdv_cps_prune": (_I, [_I, _I, _I, _I, _VP, _VP, _F, _VP, _F, _I, _VP, _VP, _VP, _VP]),
+    "sdv_cps_beam": (_I, [_I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "sdv_adl_state_words": (_I, [_I]),
+    "sdv_adl_step_host": (_I, [_I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP]),
+    "sdv_adl_step": (_I, [_I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]),
 }
 
 _lib = None
@@ -206,6 +214,117 @@ def sdv_verify_static(B, K, gamma, V, dtype, stream, p_logits, q_logits, drafts,
         int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
         _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
         _dev_ptr(out_next_token, torch.int32, "out_next_token"))
+
+
+def sdv_cps(q_marginals, tau: float = 0.8, mmax: int = 15, beam: int = 3, eos_id: int = -1,
+            temperature: float = 1.0, temps: Optional[torch.Tensor] = None, stream=None,
+            out: Optional[dict] = None) -> dict:
+    """Causal-consistency path search over drafter marginals q [B, gamma, V]
+    (candidate pruning by cumulative mass, EOS cut, beam by drafter
+    confidence).  Enqueues on `stream` (default: the current stream) and
+    returns the output tensors; `out` (a dict this returned for the same
+    shapes) reuses them."""
+    B, G, V = q_marginals.shape
+    dev = q_marginals.device
+    out = out if out is not None else {
+        "cand_ids": torch.empty((B, G, mmax), dtype=torch.int32, device=dev),
+        "cand_logp": torch.empty((B, G, mmax), dtype=torch.float32, device=dev),
+        "cand_logit": torch.empty((B, G, mmax), dtype=torch.float32, device=dev),
+        "ncand": torch.empty((B, G), dtype=torch.int32, device=dev),
+        "paths": torch.empty((B, beam, G), dtype=torch.int32, device=dev),
+        "path_logp": torch.empty((B, beam), dtype=torch.float32, device=dev),
+        "npaths": torch.empty((B,), dtype=torch.int32, device=dev),
+        "lat_len": torch.empty((B,), dtype=torch.int32, device=dev),
+    }
+    st = load().sdv_cps(B, G, V, _dtype_code(q_marginals.dtype), ctypes.c_void_p(_stream_handle(stream)),
+                        _dev_ptr(q_marginals, name="q_marginals"), float(temperature),
+                        _dev_ptr(temps, torch.float32, "temps"), float(tau), int(mmax), int(beam),
+                        int(eos_id), *[_dev_ptr(out[k]) for k in ("cand_ids", "cand_logp", "cand_logit",
+                                                                  "ncand", "paths", "path_logp",
+                                                                  "npaths", "lat_len")])
+    if st != SDV_OK:
+        raise SdvError(st, "sdv_cps")
+    return out
+
+
+def _cps_lattice(B, G, mmax, dev):
+    return {"cand_ids": torch.empty((B, G, mmax), dtype=torch.int32, device=dev),
+            "cand_logp": torch.empty((B, G, mmax), dtype=torch.float32, device=dev),
+            "cand_logit": torch.empty((B, G, mmax), dtype=torch.float32, device=dev),
+            "ncand": torch.empty((B, G), dtype=torch.int32, device=dev)}
+
+
+def sdv_cps_prune(q_marginals, tau: float = 0.8, mmax: int = 15, temperature: float = 1.0,
+                  temps: Optional[torch.Tensor] = None, stream=None, out: Optional[dict] = None) -> dict:
+    """The pruning half of sdv_cps: every row's candidate list (no EOS cut).
+    `out` (the dict this returns) may be passed back to reuse its tensors."""
+    B, G, V = q_marginals.shape
+    out = out if out is not None else _cps_lattice(B, G, mmax, q_marginals.device)
+    st = load().sdv_cps_prune(B, G, V, _dtype_code(q_marginals.dtype),
+                              ctypes.c_void_p(_stream_handle(stream)),
+                              _dev_ptr(q_marginals, name="q_marginals"), float(temperature),
+                              _dev_ptr(temps, torch.float32, "temps"), float(tau), int(mmax),
+                              *[_dev_ptr(out[k]) for k in ("cand_ids", "cand_logp", "cand_logit",
+                                                           "ncand")])
+    if st != SDV_OK:
+        raise SdvError(st, "sdv_cps_prune")
+    return out
+
+
+def sdv_cps_beam(lattice: dict, V: int, beam: int = 3, eos_id: int = -1, stream=None) -> dict:
+    """The beam half of sdv_cps over a lattice from sdv_cps_prune (trimmed in
+    place at an EOS end).  Returns the lattice dict with the path tensors."""
+    B, G, mmax = lattice["cand_ids"].shape
+    dev = lattice["cand_ids"].device
+    out = dict(lattice)
+    out.update({"paths": torch.empty((B, beam, G), dtype=torch.int32, device=dev),
+                "path_logp": torch.empty((B, beam), dtype=torch.float32, device=dev),
+                "npaths": torch.empty((B,), dtype=torch.int32, device=dev),
+                "lat_len": torch.empty((B,), dtype=torch.int32, device=dev)})
+    st = load().sdv_cps_beam(B, G, int(V), int(mmax), int(beam), int(eos_id),
+                             ctypes.c_void_p(_stream_handle(stream)),
+                             *[_dev_ptr(out[k]) for k in ("cand_ids", "cand_logp", "cand_logit",
+                                                          "ncand", "paths",
+                                                          "path_logp", "npaths", "lat_len")])
+    if st != SDV_OK:
+        raise SdvError(st, "sdv_cps_beam")
+    return out
+
+
+class DraftLengthController:
+    """Adaptive draft length for B sequences (the library's rule; see
+    sdv_adl_step in include/sdv.h).  On a CUDA device the state, the lengths
+    and the update stay on the device (`step` enqueues one kernel); on the
+    host the same rule runs in the library's C code."""
+
+    def __init__(self, B: int, k0, window: int = 1, kmin: int = 1, kmax: int = 64, up: int = 2,
+                 down: int = 1, device="cuda"):
+        words = load().sdv_adl_state_words(int(window))
+        if words < 0:
+            raise SdvError(SDV_ERR_ARG, "window")
+        self.B, self.window, self.kmin, self.kmax, self.up, self.down = B, window, kmin, kmax, up, down
+        self.device = torch.device(device)
+        self.state = torch.zeros((B, words), dtype=torch.int32, device=self.device)
+        self.k = torch.as_tensor(k0, dtype=torch.int32).expand(B).clone().to(self.device)
+        self.status = (torch.zeros(1, dtype=torch.int32, device=self.device)
+                       if self.device.type == "cuda" else None)
+
+    def step(self, gen_len: torch.Tensor, acc_len: torch.Tensor, stream=None) -> torch.Tensor:
+        """Record one step's generated and accepted lengths [B] (int32, on the
+        controller's device) and return the next draft lengths (self.k)."""
+        g = gen_len.to(torch.int32).contiguous()
+        a = acc_len.to(torch.int32).contiguous()
+        if self.device.type == "cuda":
+            st = load().sdv_adl_step(self.B, self.window, self.kmin, self.kmax, self.up, self.down,
+                                     ctypes.c_void_p(_stream_handle(stream)), _dev_ptr(g), _dev_ptr(a),
+                                     _dev_ptr(self.k), _dev_ptr(self.state), _dev_ptr(self.status))
+        else:
+            st = load().sdv_adl_step_host(self.B, self.window, self.kmin, self.kmax, self.up,
+                                          self.down, _host_ptr(g), _host_ptr(a), _host_ptr(self.k),
+                                          _host_ptr(self.state))
+        if st != SDV_OK:
+            raise SdvError(st, "sdv_adl_step")
+        return self.k
 
 
 def sdv_set_stream(ctx, stream) -> int:

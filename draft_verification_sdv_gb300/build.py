@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdv.so")
-SOURCES = ["k1_rowpass.cu", "k2_select.cu", "k3_sample.cu", "sdv_api.cu", "sdv_static.cu"]
+SOURCES = ["k1_rowpass.cu", "k2_select.cu", "k3_sample.cu", "k4_cps.cu", "k5_adl.cu", "sdv_api.cu", "sdv_static.cu"]
 HEADERS = ["sdv_device.cuh", "sdv_plan.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

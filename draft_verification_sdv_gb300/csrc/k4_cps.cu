@@ -1,0 +1,392 @@
+// k4_cps.cu -- causal-consistency path search over drafter marginals
+// ("DiffuSpec: Unlocking Diffusion Language Models for Speculative Decoding",
+// section 4.2; settings of section 5.3: beam 3, at most 15 candidates, mass
+// 0.8).  The causal fluency proxy the page mentions is not specified there, so
+// a path is scored by drafter confidence alone: the sum of its per-position
+// log-probabilities.
+//
+// cps_prune_kernel, one CTA per drafter row q[b, j, :]: each warp streams a
+// contiguous share of the row (eight 16-byte loads in flight per lane),
+// keeping the online softmax statistics (max, sum 2^{(l - max) c}) and the
+// warp's 16 largest logits (ties to the lower id) as one key per lane.  Only
+// a vector holding a value at or above the list's last entry enters the
+// (rare, warp-uniform) insertion path, so the pass costs about what the
+// statistics cost.  Warp 0 then merges the warps' lists and statistics.  The
+// kept candidates are the shortest prefix of the row's list, in order of
+// probability, whose mass reaches tau, capped at mmax; tokens of probability
+// zero are never candidates, and a row with a NaN or +inf logit, or none
+// finite, keeps none.
+//
+// cps_beam_kernel, one warp per sequence: the lattice ends at the first
+// position whose most likely candidate is eos_id (kept alone as the last
+// token); a left-to-right beam of width W keeps, at every step, the W best
+// prefixes.  A path's score is the sum of its log-probabilities; the
+// temperature and the positions' normalisers are common to all paths, so
+// prefixes rank by the sum of their raw logits, taken left to right in fp64
+// (exact for bf16 logits), with equal sums in lexicographic order of their
+// candidate ranks (tracked as each beam's place among the beams).  With a
+// separable score this gives the W best paths of the whole lattice.
+#include "sdv_device.cuh"
+#include "sdv_plan.h"
+
+namespace sdv {
+namespace {
+
+constexpr int kTopK = 16;                  // list length (mmax <= 16)
+constexpr int kBeamMaxExp = kCpsMaxBeam * kCpsMaxCand;   // expansions per step
+
+// Order-preserving 32-bit key of a logit (larger value -> larger key).
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint64_t key) {
+    const uint32_t k = static_cast<uint32_t>(key >> 32);
+    const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+
+// Key of (logit, id): value first, then the lower id.  0 = empty slot.
+__device__ __forceinline__ uint64_t cand_key(float f, uint32_t id) {
+    return (static_cast<uint64_t>(order_key(f)) << 32) | static_cast<uint64_t>(0xffffffffu - id);
+}
+
+__device__ __forceinline__ uint32_t key_id(uint64_t key) {
+    return 0xffffffffu - static_cast<uint32_t>(key & 0xffffffffu);
+}
+
+// The warp's best kTopK keys, one per lane: lane i < kTopK holds the i-th
+// largest (0 = empty slot), lanes >= kTopK hold 0.  Inserting a warp-uniform
+// key shifts the smaller ones down one lane.
+__device__ __forceinline__ uint64_t wlist_insert(uint64_t mine, uint64_t k, int lane) {
+    const uint64_t prev = __shfl_up_sync(0xffffffffu, mine, 1);
+    if (lane < kTopK && !(mine > k)) mine = (lane == 0 || prev > k) ? k : prev;
+    return mine;
+}
+
+__device__ __forceinline__ float wlist_threshold(uint64_t mine) {
+    const uint64_t last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
+    return last ? key_value(last) : -INFINITY;
+}
+
+// Offer one 16-byte vector per lane (ids id0 .. id0 + EPV - 1) to the warp's
+// list; called by the whole warp when some lane holds a value at or above the
+// list's threshold (rare once the list is full).
+template <bool BF16>
+__device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, uint64_t mine, int lane) {
+    constexpr int EPV = BF16 ? 8 : 4;
+    uint64_t last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+        const uint32_t wd = BF16 ? (i < 4 ? (i < 2 ? v.x : v.y) : (i < 6 ? v.z : v.w))
+                                 : (i < 2 ? (i == 0 ? v.x : v.y) : (i == 2 ? v.z : v.w));
+        const float f = BF16 ? ((i & 1) ? bf16_hi(wd) : bf16_lo(wd)) : __uint_as_float(wd);
+        const uint64_t key = cand_key(f, id0 + i);
+        // a -inf logit has probability zero and is never a candidate
+        unsigned pending = __ballot_sync(0xffffffffu, f != -INFINITY && f == f && key > last);
+        while (pending) {
+            const int src = __ffs(pending) - 1;
+            pending &= pending - 1;
+            const uint64_t k = __shfl_sync(0xffffffffu, key, src);
+            if (k > last) {
+                mine = wlist_insert(mine, k, lane);
+                last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
+            }
+        }
+    }
+    return mine;
+}
+
+constexpr int kPruneUnroll = 8;            // 16-byte vectors in flight per lane
+
+// One CTA of NW warps per row; each warp streams a contiguous 1/NW of it.
+template <bool BF16, int NW>
+__global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(const CpsArgs a) {
+    __shared__ uint64_t s_best[NW][kTopK];
+    __shared__ float s_m[NW], s_s[NW];
+    const int64_t row = blockIdx.x;
+    const int b = static_cast<int>(row / a.G);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float T = a.temps ? a.temps[b] : a.temperature;
+    const float c = kLog2e / T;
+    const uint4* rowv = static_cast<const uint4*>(a.q) + row * a.nvec;
+    constexpr int EPV = BF16 ? 8 : 4;
+    const int64_t per_warp = (a.nvec + NW - 1) / NW;
+    const int64_t v0 = warp * per_warp;
+    const int64_t v1 = v0 + per_warp < a.nvec ? v0 + per_warp : a.nvec;
+
+    uint64_t mine = 0;                // this lane's slot of the warp's list
+    float thr = -INFINITY;            // value of the list's last key once full
+    float m = -INFINITY, s = 0.0f;
+    for (int64_t base = v0 + lane; base - lane < v1; base += 32 * kPruneUnroll) {
+        uint4 w[kPruneUnroll];
+#pragma unroll
+        for (int u = 0; u < kPruneUnroll; ++u) {
+            const int64_t idx = base + 32 * u;
+            const uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
+            w[u] = idx < v1 ? ld_stream(rowv + idx) : make_uint4(ninf, ninf, ninf, ninf);
+        }
+#pragma unroll
+        for (int u = 0; u < kPruneUnroll; ++u) {
+            float e[EPV];
+            if constexpr (BF16) {
+                e[0] = bf16_lo(w[u].x); e[1] = bf16_hi(w[u].x); e[2] = bf16_lo(w[u].y);
+                e[3] = bf16_hi(w[u].y); e[4] = bf16_lo(w[u].z); e[5] = bf16_hi(w[u].z);
+                e[6] = bf16_lo(w[u].w); e[7] = bf16_hi(w[u].w);
+            } else {
+                e[0] = __uint_as_float(w[u].x); e[1] = __uint_as_float(w[u].y);
+                e[2] = __uint_as_float(w[u].z); e[3] = __uint_as_float(w[u].w);
+            }
+            float vm = e[0];
+#pragma unroll
+            for (int i = 1; i < EPV; ++i) asm("max.NaN.f32 %0, %0, %1;" : "+f"(vm) : "f"(e[i]));
+            if (!(vm <= m)) {
+                s *= ex2((m - vm) * c);
+                m = vm;
+            }
+            if (m != -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < EPV; ++i) s += ex2((e[i] - m) * c);
+            }
+            // warp-uniform: does any lane hold a value that may enter the list?
+            if (__any_sync(0xffffffffu, vm >= thr && vm != -INFINITY)) {
+                const int64_t vec = base + 32 * u;
+                mine = wlist_absorb<BF16>(w[u], static_cast<uint32_t>(vec * EPV), mine, lane);
+                thr = wlist_threshold(mine);
+            }
+        }
+    }
+    // row statistics: warp, then CTA
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+        merge_stat(m, s, m2, s2, c);
+    }
+    if (lane < kTopK) s_best[warp][lane] = mine;
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_s[warp] = s;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    // warp 0 merges the other warps' lists into its own, best keys first
+    uint64_t last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
+    for (int w2 = 1; w2 < NW; ++w2) {
+        for (int i = 0; i < kTopK; ++i) {
+            const uint64_t k = s_best[w2][i];          // same address in every lane
+            if (k <= last) break;                      // that list is descending
+            mine = wlist_insert(mine, k, lane);
+            last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
+        }
+    }
+    float M = s_m[0], S = s_s[0];
+    for (int w2 = 1; w2 < NW; ++w2) merge_stat(M, S, s_m[w2], s_s[w2], c);
+    // lane r holds the rank-r candidate; the cut is a running sum of masses
+    const int mmax = a.mmax;
+    const bool ok = isfinite(M) && isfinite(S) && S > 0.0f;
+    float pm = 0.0f, lp = -INFINITY;
+    if (ok && mine != 0) {
+        const float val = key_value(mine);
+        lp = ((val - M) * c - log2f(S)) * kLn2;
+        pm = ex2((val - M) * c) * (1.0f / S);
+    }
+    // inclusive running mass in rank order, added one by one in that order
+    float run = 0.0f, mine_after = 0.0f;
+    for (int r = 0; r < kTopK; ++r) {
+        run += __shfl_sync(0xffffffffu, pm, r);
+        if (lane == r) mine_after = run;
+    }
+    // n = first rank whose running mass reaches tau (+1), at most mmax, and
+    // only over existing candidates
+    const bool stop_here = lane < mmax && mine != 0 && mine_after >= a.tau;
+    const unsigned stop_mask = __ballot_sync(0xffffffffu, stop_here);
+    const unsigned have_mask = __ballot_sync(0xffffffffu, lane < mmax && mine != 0);
+    int n = stop_mask ? __ffs(stop_mask) : __popc(have_mask);
+    if (!ok) n = 0;
+    int32_t* ids = a.cand_ids + row * mmax;
+    float* lpo = a.cand_logp + row * mmax;
+    float* lgo = a.cand_logit + row * mmax;
+    if (lane < mmax) {
+        ids[lane] = lane < n ? static_cast<int32_t>(key_id(mine)) : -1;
+        lpo[lane] = lane < n ? lp : -INFINITY;
+        lgo[lane] = lane < n ? key_value(mine) : -INFINITY;
+    }
+    if (lane == 0) a.ncand[row] = n;      // 0 for a row with NaN / +inf / only -inf
+}
+
+__global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
+    // dynamic shared memory: the lattice's log-probabilities [G][M] and raw
+    // logits [G][M] (float), counts [G], then the back-pointers [G][W] parent
+    // and [G][W] rank
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    __shared__ double x_key[kBeamMaxExp];      // this step's expansions
+    __shared__ float x_score[kBeamMaxExp];
+    __shared__ int x_lx[kBeamMaxExp];
+    __shared__ double b_key[kCpsMaxBeam];      // the beams
+    __shared__ float b_score[kCpsMaxBeam];
+    __shared__ int b_lex[kCpsMaxBeam];
+    __shared__ double n_key[kCpsMaxBeam];      // the beams being chosen
+    __shared__ float n_score[kCpsMaxBeam];
+    __shared__ int n_lx[kCpsMaxBeam];
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x;
+    const int G = a.G, W = a.beam, M = a.mmax;
+    float* clp_s = reinterpret_cast<float*>(s_raw);
+    float* rl_s = clp_s + G * M;
+    int* nc_s = reinterpret_cast<int*>(rl_s + G * M);
+    unsigned char* bp_parent = reinterpret_cast<unsigned char*>(nc_s + G);
+    unsigned char* bp_rank = bp_parent + G * W;
+    int32_t* cids = a.cand_ids + static_cast<int64_t>(b) * G * M;
+    float* clp = a.cand_logp + static_cast<int64_t>(b) * G * M;
+    float* crl = a.cand_logit + static_cast<int64_t>(b) * G * M;
+    int32_t* nc = a.ncand + static_cast<int64_t>(b) * G;
+    for (int i = lane; i < G * M; i += 32) {
+        clp_s[i] = clp[i];
+        rl_s[i] = crl[i];
+    }
+    for (int i = lane; i < G; i += 32) nc_s[i] = nc[i];
+    __syncwarp();
+
+    // the lattice: cut at the first position whose best candidate is EOS
+    int Lc = G;
+    bool eos_cut = false;
+    if (a.eos_id >= 0) {
+        for (int j0 = 0; j0 < G; j0 += 32) {        // lanes test 32 positions at a time
+            const int j = j0 + lane;
+            const bool hit = j < G && nc_s[j] > 0 && cids[j * M] == a.eos_id;
+            const unsigned mask = __ballot_sync(0xffffffffu, hit);
+            if (mask) {
+                Lc = j0 + __ffs(mask);
+                eos_cut = true;
+                break;
+            }
+        }
+    }
+    bool empty = false;
+    for (int j = lane; j < Lc; j += 32) empty |= nc_s[j] == 0;
+    empty = __any_sync(0xffffffffu, empty);
+
+    // Beams: order key (sum of raw logits, fp64: exact for bf16 logits, and
+    // the same operations as any left-to-right fp64 sum), score (sum of
+    // log-probabilities) and place among the beams in lexicographic order of
+    // their candidate ranks (the tie rule).
+    if (lane == 0) {
+        b_key[0] = 0.0;
+        b_score[0] = 0.0f;
+        b_lex[0] = 0;
+    }
+    __syncwarp();
+    int ncur = 1;
+    for (int j = 0; j < Lc && !empty; ++j) {
+        const int n = eos_cut && j == Lc - 1 ? 1 : nc_s[j];   // EOS is kept alone
+        const int E = ncur * n;
+        // expansion e = (parent e / n, candidate e % n)
+        for (int e = lane; e < E; e += 32) {
+            const int par = e / n, r = e - par * n;
+            x_key[e] = b_key[par] + static_cast<double>(rl_s[j * M + r]);
+            x_score[e] = b_score[par] + clp_s[j * M + r];
+            x_lx[e] = b_lex[par] * n + r;
+        }
+        __syncwarp();
+        // each expansion's rank: how many expansions come before it (key
+        // desc, then lexicographic place asc); the first W are kept
+        const int keep = E < W ? E : W;
+        for (int e = lane; e < E; e += 32) {
+            const double k = x_key[e];
+            const int l = x_lx[e];
+            int rank = 0;
+            for (int e2 = 0; e2 < E; ++e2) {
+                const double k2 = x_key[e2];
+                rank += (k2 > k) || (k2 == k && x_lx[e2] < l);
+            }
+            if (rank < keep) {
+                const int par = e / n;
+                n_key[rank] = k;
+                n_score[rank] = x_score[e];
+                n_lx[rank] = l;
+                bp_parent[j * W + rank] = static_cast<unsigned char>(par);
+                bp_rank[j * W + rank] = static_cast<unsigned char>(e - par * n);
+            }
+        }
+        __syncwarp();
+        if (lane < keep) {
+            const int l = n_lx[lane];
+            int pos = 0;
+            for (int t = 0; t < keep; ++t) pos += n_lx[t] < l;
+            b_key[lane] = n_key[lane];
+            b_score[lane] = n_score[lane];
+            b_lex[lane] = pos;
+        }
+        __syncwarp();
+        ncur = keep;
+    }
+    const int np = empty ? 0 : ncur;
+    // back-track the paths of the final beams
+    if (lane < W) {
+        int32_t* path = a.paths + (static_cast<int64_t>(b) * W + lane) * G;
+        if (lane < np) {
+            int cur = lane;
+            for (int j = Lc - 1; j >= 0; --j) {
+                const int r = bp_rank[j * W + cur];
+                path[j] = cids[j * M + r];
+                cur = bp_parent[j * W + cur];
+            }
+            for (int j = Lc; j < G; ++j) path[j] = -1;
+            a.path_logp[static_cast<int64_t>(b) * W + lane] = b_score[lane];
+        } else {
+            for (int j = 0; j < G; ++j) path[j] = -1;
+            a.path_logp[static_cast<int64_t>(b) * W + lane] = -INFINITY;
+        }
+    }
+    if (lane == 0) {
+        a.npaths[b] = np;
+        if (a.lat_len) a.lat_len[b] = Lc;
+    }
+    // the lattice as used: one candidate at an EOS end, none past it
+    __syncwarp();
+    if (eos_cut) {
+        for (int i = lane; i < (G - (Lc - 1)) * M; i += 32) {
+            const int j = Lc - 1 + i / M, r = i % M;
+            if (j >= Lc || r >= 1) {
+                cids[j * M + r] = -1;
+                clp[j * M + r] = -INFINITY;
+                crl[j * M + r] = -INFINITY;
+            }
+        }
+        for (int j = Lc - 1 + lane; j < G; j += 32) nc[j] = j >= Lc ? 0 : 1;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_cps_prune(const CpsArgs& a, bool bf16, cudaStream_t s) {
+    // one CTA per row: 4 warps when the rows alone fill the GPU (8 CTAs per
+    // SM), 16 when they are few
+    const int64_t rows = static_cast<int64_t>(a.B) * a.G;
+    const unsigned grid = static_cast<unsigned>(rows);
+    const bool wide = rows < 600;
+    if (bf16) {
+        if (wide) cps_prune_kernel<true, 16><<<grid, 512, 0, s>>>(a);
+        else cps_prune_kernel<true, 4><<<grid, 128, 0, s>>>(a);
+    } else {
+        if (wide) cps_prune_kernel<false, 16><<<grid, 512, 0, s>>>(a);
+        else cps_prune_kernel<false, 4><<<grid, 128, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(a.G) * a.mmax * 8 + static_cast<size_t>(a.G) * 4 +
+                        static_cast<size_t>(2) * a.G * a.beam;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            cps_beam_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    cps_beam_kernel<<<a.B, 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace sdv

@@ -418,6 +418,155 @@ sdv_status sdv_profile_read(sdv_ctx* ctx, float* ms_avg, int* steps) {
     return SDV_OK;
 }
 
+namespace {
+
+// Checks shared by the CPS entry points; q / temps are checked only when
+// `with_q`, the beam outputs only when `with_beam`.
+sdv_status cps_check(int B, int gamma, int mmax, int beam, bool with_beam, const void* const* ptrs,
+                     int nptrs) {
+    if (B < 1 || gamma < 1 || gamma > kCpsMaxGamma) return SDV_ERR_ARG;
+    if (mmax < 1 || mmax > kCpsMaxCand) return SDV_ERR_ARG;
+    if (with_beam && (beam < 1 || beam > kCpsMaxBeam)) return SDV_ERR_ARG;
+    for (int i = 0; i < nptrs; ++i)
+        if (ptrs[i] && !is_device_ptr(ptrs[i])) return SDV_ERR_ARG;
+    return SDV_OK;
+}
+
+sdv_status cps_prune_args(int B, int gamma, int V, sdv_dtype dtype, const void* q,
+                          float temperature, const float* temps, float tau, int mmax,
+                          CpsArgs& a) {
+    if (V < 1 || (dtype != SDV_BF16 && dtype != SDV_F32)) return SDV_ERR_ARG;
+    const int64_t elt = dtype == SDV_BF16 ? 2 : 4;
+    if ((static_cast<int64_t>(V) * elt) % 16 != 0) return SDV_ERR_ARG;
+    if (!(tau >= 0.0f && tau <= 1.0f)) return SDV_ERR_ARG;
+    if (!temps && !(std::isfinite(temperature) && temperature > 0.0f)) return SDV_ERR_ARG;
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15u)) return SDV_ERR_ARG;
+    a.q = q;
+    a.temps = temps;
+    a.temperature = temperature;
+    a.tau = tau;
+    a.B = B;
+    a.G = gamma;
+    a.mmax = mmax;
+    a.nvec = static_cast<int64_t>(V) * elt / 16;
+    return SDV_OK;
+}
+
+}  // namespace
+
+sdv_status sdv_cps_prune(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                         const void* q_marginals, float temperature,
+                         const float* temperature_per_seq, float tau, int mmax,
+                         int32_t* out_cand_ids, float* out_cand_logp, float* out_cand_logit,
+                         int32_t* out_ncand) {
+    if (!out_cand_ids || !out_cand_logp || !out_cand_logit || !out_ncand) return SDV_ERR_ARG;
+    const void* ptrs[6] = {q_marginals,   temperature_per_seq, out_cand_ids,
+                           out_cand_logp, out_cand_logit,      out_ncand};
+    sdv_status st = cps_check(B, gamma, mmax, 1, false, ptrs, 6);
+    if (st != SDV_OK) return st;
+    CpsArgs a{};
+    st = cps_prune_args(B, gamma, V, dtype, q_marginals, temperature, temperature_per_seq, tau,
+                        mmax, a);
+    if (st != SDV_OK) return st;
+    a.cand_ids = out_cand_ids;
+    a.cand_logp = out_cand_logp;
+    a.cand_logit = out_cand_logit;
+    a.ncand = out_ncand;
+    return launch_cps_prune(a, dtype == SDV_BF16, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SDV_OK : SDV_ERR_CUDA;
+}
+
+sdv_status sdv_cps_beam(int B, int gamma, int V, int mmax, int beam, int eos_id, void* stream,
+                        int32_t* cand_ids, float* cand_logp, float* cand_logit, int32_t* ncand,
+                        int32_t* out_paths, float* out_path_logp, int32_t* out_npaths,
+                        int32_t* out_lat_len) {
+    if (V < 1 || eos_id >= V) return SDV_ERR_ARG;
+    if (!cand_ids || !cand_logp || !cand_logit || !ncand || !out_paths || !out_path_logp ||
+        !out_npaths)
+        return SDV_ERR_ARG;
+    const void* ptrs[8] = {cand_ids,  cand_logp,     cand_logit, ncand,
+                           out_paths, out_path_logp, out_npaths, out_lat_len};
+    const sdv_status st = cps_check(B, gamma, mmax, beam, true, ptrs, 8);
+    if (st != SDV_OK) return st;
+    CpsArgs a{};
+    a.B = B;
+    a.G = gamma;
+    a.mmax = mmax;
+    a.beam = beam;
+    a.eos_id = eos_id;
+    a.cand_ids = cand_ids;
+    a.cand_logp = cand_logp;
+    a.cand_logit = cand_logit;
+    a.ncand = ncand;
+    a.paths = out_paths;
+    a.path_logp = out_path_logp;
+    a.npaths = out_npaths;
+    a.lat_len = out_lat_len;
+    return launch_cps_beam(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SDV_OK
+                                                                                : SDV_ERR_CUDA;
+}
+
+sdv_status sdv_cps(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                   const void* q_marginals, float temperature, const float* temperature_per_seq,
+                   float tau, int mmax, int beam, int eos_id, int32_t* out_cand_ids,
+                   float* out_cand_logp, float* out_cand_logit, int32_t* out_ncand,
+                   int32_t* out_paths,
+                   float* out_path_logp, int32_t* out_npaths, int32_t* out_lat_len) {
+    // both halves' argument checks run before either launches
+    if (V < 1 || eos_id >= V || beam < 1 || beam > kCpsMaxBeam) return SDV_ERR_ARG;
+    if (!out_paths || !out_path_logp || !out_npaths) return SDV_ERR_ARG;
+    const void* ptrs[4] = {out_paths, out_path_logp, out_npaths, out_lat_len};
+    sdv_status st = cps_check(B, gamma, mmax, beam, true, ptrs, 4);
+    if (st != SDV_OK) return st;
+    st = sdv_cps_prune(B, gamma, V, dtype, stream, q_marginals, temperature, temperature_per_seq,
+                       tau, mmax, out_cand_ids, out_cand_logp, out_cand_logit, out_ncand);
+    if (st != SDV_OK) return st;
+    return sdv_cps_beam(B, gamma, V, mmax, beam, eos_id, stream, out_cand_ids, out_cand_logp,
+                        out_cand_logit, out_ncand, out_paths, out_path_logp, out_npaths,
+                        out_lat_len);
+}
+
+namespace {
+
+bool adl_params_ok(int B, int W, int kmin, int kmax, int up, int down) {
+    return B >= 0 && W >= 1 && W <= kAdlMaxWindow && kmin >= 1 && kmax >= kmin &&
+           kmax <= kAdlMaxLength && up >= 0 && up <= kAdlMaxLength && down >= 0 &&
+           down <= kAdlMaxLength;
+}
+
+}  // namespace
+
+int sdv_adl_state_words(int window) {
+    return window >= 1 && window <= kAdlMaxWindow ? adl_state_words(window) : -1;
+}
+
+sdv_status sdv_adl_step_host(int B, int window, int kmin, int kmax, int up, int down,
+                             const int32_t* gen_len, const int32_t* acc_len, int32_t* k,
+                             int32_t* state) {
+    if (!adl_params_ok(B, window, kmin, kmax, up, down)) return SDV_ERR_ARG;
+    if (B > 0 && (!gen_len || !acc_len || !k || !state)) return SDV_ERR_ARG;
+    for (int b = 0; b < B; ++b)
+        if (k[b] < kmin || k[b] > kmax) return SDV_ERR_ARG;     // nothing updated
+    const int words = adl_state_words(window);
+    for (int b = 0; b < B; ++b)
+        k[b] = adl_update(state + static_cast<int64_t>(b) * words, window, kmin, kmax, up, down,
+                          k[b], gen_len[b], acc_len[b]);
+    return SDV_OK;
+}
+
+sdv_status sdv_adl_step(int B, int window, int kmin, int kmax, int up, int down, void* stream,
+                        const int32_t* gen_len, const int32_t* acc_len, int32_t* k,
+                        int32_t* state, int32_t* status) {
+    if (!adl_params_ok(B, window, kmin, kmax, up, down)) return SDV_ERR_ARG;
+    if (B == 0) return SDV_OK;
+    if (!gen_len || !acc_len || !k || !state) return SDV_ERR_ARG;
+    const void* ptrs[5] = {gen_len, acc_len, k, state, status};
+    for (const void* p : ptrs)
+        if (p && !is_device_ptr(p)) return SDV_ERR_ARG;
+    AdlArgs a{B, window, kmin, kmax, up, down, gen_len, acc_len, k, state, status};
+    return launch_adl(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
+}
+
 sdv_status sdv_set_stream(sdv_ctx* ctx, void* stream) {
     if (!ctx) return SDV_ERR_ARG;
     ctx->stream = static_cast<cudaStream_t>(stream);

@@ -26,7 +26,56 @@ enum : unsigned {
     kStatusBadRow = 2u,      // a row with NaN / +inf, or only -inf
     kStatusBadTemp = 4u,     // per-sequence temperature not finite and positive
     kStatusTimeout = 8u,     // a bounded device wait gave up
+    kStatusBadLength = 16u,  // a draft length outside [kmin, kmax] given to the controller
 };
+
+// Adaptive draft length ("DiffuSpec", section 4.3).  A sequence's state is
+// [entries in the window (at most W), next ring slot, sum k, sum g, sum a,
+// then the W ring entries of k, of g and of a].  One step records (k, g, a)
+// -- g clamped to [0, k], a to [0, g] -- evicting the oldest entry of a full
+// window, and returns the next draft length: grow by `up` when the window's
+// accepted lengths sum to its generated ones and those to its drafted ones,
+// hold when only the first holds (generation saturated by EOS), shrink by
+// `down` otherwise; clamped to [kmin, kmax].  Shared by the host entry point
+// and the device kernel.
+constexpr int kAdlMaxWindow = 64;
+constexpr int kAdlMaxLength = 1 << 20;
+__host__ __device__ inline int adl_state_words(int W) { return 5 + 3 * W; }
+
+__host__ __device__ inline int32_t adl_update(int32_t* st, int W, int kmin, int kmax, int up,
+                                              int down, int32_t k, int32_t g, int32_t a) {
+    g = g < 0 ? 0 : (g > k ? k : g);
+    a = a < 0 ? 0 : (a > g ? g : a);
+    int32_t* rk = st + 5;
+    int32_t* rg = rk + W;
+    int32_t* ra = rg + W;
+    int32_t n = st[0], pos = st[1], sk = st[2], sg = st[3], sa = st[4];
+    if (n == W) {
+        sk -= rk[pos];
+        sg -= rg[pos];
+        sa -= ra[pos];
+    } else {
+        ++n;
+    }
+    rk[pos] = k;
+    rg[pos] = g;
+    ra[pos] = a;
+    sk += k;
+    sg += g;
+    sa += a;
+    st[0] = n;
+    st[1] = pos + 1 == W ? 0 : pos + 1;
+    st[2] = sk;
+    st[3] = sg;
+    st[4] = sa;
+    int32_t next = k;
+    if (sa >= sg && sg >= sk)
+        next = k + up;
+    else if (sa < sg)
+        next = k - down;
+    return next < kmin ? kmin : (next > kmax ? kmax : next);
+}
+
 
 // The draw to make for one sequence, decided by the selection and scan.
 // mode 0: nothing to draw (data error); 1: residual max(0, p - q) of rows
@@ -95,6 +144,42 @@ struct SampleArgs {
     int64_t slice_vec;
     int cluster;
 };
+
+// Causal-consistency path search (k4_cps.cu): prune kernel over the B*G
+// drafter rows, then one warp per sequence for the beam.
+constexpr int kCpsMaxBeam = 16;
+constexpr int kCpsMaxCand = 16;
+constexpr int kCpsMaxGamma = 1024;
+struct CpsArgs {
+    const void* q;          // [B][G][V]
+    const float* temps;     // [B] or nullptr
+    float temperature;
+    float tau;
+    int B, G, mmax, beam, eos_id;
+    int64_t nvec;
+    int32_t* cand_ids;      // [B][G][mmax]
+    float* cand_logp;       // [B][G][mmax]
+    float* cand_logit;      // [B][G][mmax] raw logits of the candidates
+    int32_t* ncand;         // [B][G]
+    int32_t* paths;         // [B][beam][G]
+    float* path_logp;       // [B][beam]
+    int32_t* npaths;        // [B]
+    int32_t* lat_len;       // [B] or nullptr
+};
+// Pruning (reads q, temps; writes cand_ids, cand_logp, ncand) and the beam
+// (reads and trims the lattice; writes paths, path_logp, npaths, lat_len).
+cudaError_t launch_cps_prune(const CpsArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s);
+
+struct AdlArgs {
+    int B, W, kmin, kmax, up, down;
+    const int32_t* gen_len;   // [B]
+    const int32_t* acc_len;   // [B]
+    int32_t* k;               // [B] in/out
+    int32_t* state;           // [B][adl_state_words(W)]
+    int32_t* status;          // or nullptr
+};
+cudaError_t launch_adl(const AdlArgs& a, cudaStream_t s);
 
 // Launchers (defined next to their kernels).  `bf16` selects the element type
 // (bf16 when true, fp32 otherwise).  Each returns the launch's error code.

@@ -195,6 +195,102 @@ sdv_status sdv_profile_enable(sdv_ctx* ctx, int enable);
 sdv_status sdv_profile_read(sdv_ctx* ctx, float* ms_avg, int* steps);
 
 /*
+ * Causal-consistency path search over drafter marginals ("DiffuSpec:
+ * Unlocking Diffusion Language Models for Speculative Decoding", section 4.2;
+ * the page's settings, section 5.3: beam 3, mmax 15, tau 0.8).  Produces
+ * left-to-right drafts from one denoising pass's position-wise marginals:
+ *   1. each row q[b][j] is pruned to the shortest list of its most likely
+ *      tokens (probability of softmax(q / T) descending, ties to the lower id)
+ *      whose mass reaches tau, at most mmax tokens; a token of probability
+ *      zero (logit -inf) is never a candidate;
+ *   2. the lattice ends at the first position whose most likely token is
+ *      eos_id, which is kept alone as the last token (eos_id < 0: no cut);
+ *   3. a beam of width `beam` runs left to right over the lattice, scoring a
+ *      path by the sum of its log-probabilities (drafter confidence; the
+ *      page's causal fluency proxy is not specified there and is not used).
+ *      The temperature and each position's normaliser are common to all of a
+ *      sequence's paths, so paths rank by the sum of their raw logits, taken
+ *      left to right in fp64 (exact for bf16 logits); equal sums go to the
+ *      path whose candidate ranks come first lexicographically.  The result
+ *      is the `beam` best paths of the lattice, best first.
+ * The paths serve as the K = beam drafts of a verification step
+ * (SDV_FLAG_SHARED_Q, with the same q).
+ * Arguments: q_marginals device [B][gamma][V] bf16 or fp32 (16-byte aligned,
+ * V * elt % 16 == 0); temperature, or device temperature_per_seq [B];
+ * 0 <= tau <= 1; 1 <= mmax <= 16; 1 <= beam <= 16; gamma <= 1024;
+ * eos_id < V.  Outputs (device, caller-owned): out_cand_ids / out_cand_logp /
+ * out_cand_logit [B][gamma][mmax] (candidate ids, natural-log probabilities
+ * and raw logits; -1 / -inf / -inf past the count), out_ncand [B][gamma] (0
+ * past the lattice), out_paths [B][beam][gamma] (-1 past the lattice or past
+ * npaths), out_path_logp [B][beam] (-inf past npaths), out_npaths [B],
+ * out_lat_len [B] or NULL.  A row holding NaN, +inf or only -inf gets no
+ * candidates and its sequence no path.  Stateless: allocates nothing, only
+ * enqueues on `stream`.
+ */
+sdv_status sdv_cps(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                   const void* q_marginals, float temperature,
+                   const float* temperature_per_seq, float tau, int mmax, int beam,
+                   int eos_id, int32_t* out_cand_ids, float* out_cand_logp,
+                   float* out_cand_logit, int32_t* out_ncand, int32_t* out_paths,
+                   float* out_path_logp, int32_t* out_npaths, int32_t* out_lat_len);
+
+/*
+ * The two halves of sdv_cps, for callers that inspect or reuse the pruned
+ * lattice.  sdv_cps_prune is step 1 for every row (no EOS cut): it reads
+ * q_marginals / temperature(_per_seq) and writes out_cand_ids, out_cand_logp,
+ * out_cand_logit and out_ncand exactly as sdv_cps documents them, before the
+ * cut.  sdv_cps_beam is steps 2-3: it reads the lattice (as sdv_cps_prune
+ * wrote it), trims it in place at an EOS end (one candidate at the EOS
+ * position, none past it) and writes the paths.  V is only used to check
+ * eos_id.  Argument rules, ownership and errors as for sdv_cps; sdv_cps is
+ * sdv_cps_prune followed by sdv_cps_beam on `stream`.
+ */
+sdv_status sdv_cps_prune(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                         const void* q_marginals, float temperature,
+                         const float* temperature_per_seq, float tau, int mmax,
+                         int32_t* out_cand_ids, float* out_cand_logp, float* out_cand_logit,
+                         int32_t* out_ncand);
+sdv_status sdv_cps_beam(int B, int gamma, int V, int mmax, int beam, int eos_id, void* stream,
+                        int32_t* cand_ids, float* cand_logp, float* cand_logit, int32_t* ncand,
+                        int32_t* out_paths, float* out_path_logp, int32_t* out_npaths,
+                        int32_t* out_lat_len);
+
+/*
+ * Adaptive draft length ("DiffuSpec: Unlocking Diffusion Language Models for
+ * Speculative Decoding", section 4.3 and appendix C).  The page states the
+ * controller's inputs and direction only; this is the plainest rule that
+ * fits it.  Per sequence, a window of the last `window` steps records the
+ * draft length k used, the EOS-aware generated length g (tokens up to and
+ * including the first EOS of the chosen draft, e.g. sdv_cps's lattice length)
+ * and the accepted length a (e.g. sdv_verify's out_len); g is clamped to
+ * [0, k] and a to [0, g].  Acceptance keeps pace when the window's a sum to
+ * its g; generation fills the drafts when its g sum to its k.  The next
+ * length is k + up if both hold, k if only the first holds (generation
+ * saturated: EOS before the end of the draft), k - down otherwise, clamped to
+ * [kmin, kmax].
+ * Limits: 1 <= window <= 64; 1 <= kmin <= kmax <= 2^20; 0 <= up, down <= 2^20.
+ * sdv_adl_state_words(window): int32 words of one sequence's state (-1 for a
+ * bad window).  The state [B][words] is caller-owned and starts zeroed; its
+ * layout is private to the library.
+ * sdv_adl_step_host: host pointers; k [B] holds the lengths just used and
+ * receives the next ones.  SDV_ERR_ARG for bad limits or any k outside
+ * [kmin, kmax] (then nothing is updated).
+ * sdv_adl_step: the same on device pointers, enqueued on `stream` (one thread
+ * per sequence); a sequence whose k lies outside [kmin, kmax] is left as it
+ * is and sets bit 16 in *status (device int32, may be NULL), which the caller
+ * clears.  Host-checked argument errors return SDV_ERR_ARG.
+ */
+#define SDV_ADL_MAX_WINDOW 64
+#define SDV_STATUS_BAD_LENGTH 16
+int sdv_adl_state_words(int window);
+sdv_status sdv_adl_step_host(int B, int window, int kmin, int kmax, int up, int down,
+                             const int32_t* gen_len, const int32_t* acc_len, int32_t* k,
+                             int32_t* state);
+sdv_status sdv_adl_step(int B, int window, int kmin, int kmax, int up, int down, void* stream,
+                        const int32_t* gen_len, const int32_t* acc_len, int32_t* k,
+                        int32_t* state, int32_t* status);
+
+/*
  * sdv_verify_static -- the step of sdv_verify_ex for callers that cannot
  * allocate device memory.  The pages have no counterpart to this entry point:
  * it exists for deployment, not for the method.
