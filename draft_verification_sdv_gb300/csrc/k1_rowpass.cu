@@ -32,55 +32,6 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
     return make_uint4(w, w, w, w);
 }
 
-// Max over kUnroll vectors; NaN propagates so that a NaN row is caught.
-template <bool BF16>
-__device__ __forceinline__ float vec_max(const uint4 (&v)[kUnroll]) {
-    if constexpr (BF16) {
-        uint32_t m[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
-#pragma unroll
-        for (int u = 1; u < kUnroll; ++u) {
-            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(v[u].x));
-            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[1]) : "r"(v[u].y));
-            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[2]) : "r"(v[u].z));
-            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[3]) : "r"(v[u].w));
-        }
-        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(m[1]));
-        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[2]) : "r"(m[3]));
-        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(m[2]));
-        float r;
-        asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(bf16_lo(m[0])), "f"(bf16_hi(m[0])));
-        return r;
-    } else {
-        float r = __uint_as_float(v[0].x);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const float e[4] = {__uint_as_float(v[u].x), __uint_as_float(v[u].y),
-                                __uint_as_float(v[u].z), __uint_as_float(v[u].w)};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) asm("max.NaN.f32 %0, %0, %1;" : "+f"(r) : "f"(e[i]));
-        }
-        return r;
-    }
-}
-
-// Sum of 2^{(l - m) c} over one vector (pairwise tree).
-template <bool BF16>
-__device__ __forceinline__ float vec_sum(const uint4& v, float m, float c) {
-    if constexpr (BF16) {
-        const float e0 = ex2((bf16_lo(v.x) - m) * c), e1 = ex2((bf16_hi(v.x) - m) * c);
-        const float e2 = ex2((bf16_lo(v.y) - m) * c), e3 = ex2((bf16_hi(v.y) - m) * c);
-        const float e4 = ex2((bf16_lo(v.z) - m) * c), e5 = ex2((bf16_hi(v.z) - m) * c);
-        const float e6 = ex2((bf16_lo(v.w) - m) * c), e7 = ex2((bf16_hi(v.w) - m) * c);
-        return ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
-    } else {
-        const float e0 = ex2((__uint_as_float(v.x) - m) * c);
-        const float e1 = ex2((__uint_as_float(v.y) - m) * c);
-        const float e2 = ex2((__uint_as_float(v.z) - m) * c);
-        const float e3 = ex2((__uint_as_float(v.w) - m) * c);
-        return (e0 + e1) + (e2 + e3);
-    }
-}
-
 template <bool BF16>
 __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassArgs a) {
     // Let the select kernel launch now: it waits for this grid before it
@@ -116,7 +67,7 @@ __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassA
                 const int64_t idx = base + 32 * u;
                 v[u] = idx < v1 ? ld_stream(rowv + idx) : neg_inf_vec<BF16>();
             }
-            const float vm = vec_max<BF16>(v);
+            const float vm = vec_max_n<BF16, kUnroll>(v);
             if (!(vm <= m)) {                 // new maximum (or NaN: poisons s)
                 s *= ex2((m - vm) * c);
                 m = vm;
@@ -124,7 +75,7 @@ __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassA
             if (m != -INFINITY) {             // all -inf so far: nothing to add
                 float t[kUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) t[u] = vec_sum<BF16>(v[u], m, c);
+                for (int u = 0; u < kUnroll; ++u) t[u] = vec_exp_sum<BF16>(v[u], m, c);
 #pragma unroll
                 for (int w = kUnroll / 2; w > 0; w >>= 1)
 #pragma unroll

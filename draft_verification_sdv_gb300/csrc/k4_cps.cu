@@ -70,25 +70,43 @@ __device__ __forceinline__ float wlist_threshold(uint64_t mine) {
     return last ? key_value(last) : -INFINITY;
 }
 
-// Offer one 16-byte vector per lane (ids id0 .. id0 + EPV - 1) to the warp's
-// list; called by the whole warp when some lane holds a value at or above the
-// list's threshold (rare once the list is full).
+// Offer the lanes' 16-byte vectors (lane's ids id0 .. id0 + EPV - 1, its
+// vector max vmax) to the warp's list.  Only lanes whose vector reaches
+// `floor` (a value the warp's 16th best is known to reach) take part: each in
+// turn broadcasts its vector, lanes 0 .. EPV-1 take one logit each, and the
+// logits that beat the list's last key are inserted.
 template <bool BF16>
-__device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, uint64_t mine, int lane) {
+__device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, float vmax, uint64_t mine,
+                                              float floor, int lane) {
     constexpr int EPV = BF16 ? 8 : 4;
     uint64_t last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
-#pragma unroll
-    for (int i = 0; i < EPV; ++i) {
-        const uint32_t wd = BF16 ? (i < 4 ? (i < 2 ? v.x : v.y) : (i < 6 ? v.z : v.w))
-                                 : (i < 2 ? (i == 0 ? v.x : v.y) : (i == 2 ? v.z : v.w));
-        const float f = BF16 ? ((i & 1) ? bf16_hi(wd) : bf16_lo(wd)) : __uint_as_float(wd);
-        const uint64_t key = cand_key(f, id0 + i);
+    unsigned hot = __ballot_sync(0xffffffffu, vmax >= floor && vmax != -INFINITY);
+    while (hot) {
+        const int src = __ffs(hot) - 1;
+        hot &= hot - 1;
+        const uint32_t x = __shfl_sync(0xffffffffu, v.x, src);
+        const uint32_t y = __shfl_sync(0xffffffffu, v.y, src);
+        const uint32_t z = __shfl_sync(0xffffffffu, v.z, src);
+        const uint32_t w = __shfl_sync(0xffffffffu, v.w, src);
+        const uint32_t base = __shfl_sync(0xffffffffu, id0, src);
+        const int i = lane & (EPV - 1);
+        uint32_t wd;
+        float f;
+        if constexpr (BF16) {
+            wd = i < 4 ? (i < 2 ? x : y) : (i < 6 ? z : w);
+            f = (i & 1) ? bf16_hi(wd) : bf16_lo(wd);
+        } else {
+            wd = i < 2 ? (i == 0 ? x : y) : (i == 2 ? z : w);
+            f = __uint_as_float(wd);
+        }
+        const uint64_t key = cand_key(f, base + i);
         // a -inf logit has probability zero and is never a candidate
-        unsigned pending = __ballot_sync(0xffffffffu, f != -INFINITY && f == f && key > last);
+        unsigned pending = __ballot_sync(
+            0xffffffffu, lane < EPV && f != -INFINITY && f >= floor && key > last);
         while (pending) {
-            const int src = __ffs(pending) - 1;
+            const int l = __ffs(pending) - 1;
             pending &= pending - 1;
-            const uint64_t k = __shfl_sync(0xffffffffu, key, src);
+            const uint64_t k = __shfl_sync(0xffffffffu, key, l);
             if (k > last) {
                 mine = wlist_insert(mine, k, lane);
                 last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
@@ -99,6 +117,40 @@ __device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, uint64_t mi
 }
 
 constexpr int kPruneUnroll = 8;            // 16-byte vectors in flight per lane
+
+// NaN-propagating max of one 16-byte vector.
+template <bool BF16>
+__device__ __forceinline__ float vec1_max(const uint4& v) {
+    if constexpr (BF16) {
+        uint32_t a = v.x, b = v.z;
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(a) : "r"(v.y));
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(b) : "r"(v.w));
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(a) : "r"(b));
+        float r;
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(bf16_lo(a)), "f"(bf16_hi(a)));
+        return r;
+    } else {
+        float r = __uint_as_float(v.x), t = __uint_as_float(v.z);
+        asm("max.NaN.f32 %0, %0, %1;" : "+f"(r) : "f"(__uint_as_float(v.y)));
+        asm("max.NaN.f32 %0, %0, %1;" : "+f"(t) : "f"(__uint_as_float(v.w)));
+        asm("max.NaN.f32 %0, %0, %1;" : "+f"(r) : "f"(t));
+        return r;
+    }
+}
+
+// The 16th largest of the lanes' values (-inf when fewer than 16 are finite):
+// at least 16 logits of the batch reach it, so the warp's 16th best does too.
+__device__ __forceinline__ float warp_16th(float x, int lane) {
+    int rank = 0;
+#pragma unroll
+    for (int l2 = 0; l2 < 32; ++l2) {
+        const float y = __shfl_sync(0xffffffffu, x, l2);
+        rank += (y > x) || (y == x && l2 < lane);
+    }
+    const unsigned at = __ballot_sync(0xffffffffu, rank == kTopK - 1);
+    const float t = __shfl_sync(0xffffffffu, x, at ? __ffs(at) - 1 : 0);
+    return at && t == t ? t : -INFINITY;
+}
 
 // One CTA of NW warps per row; each warp streams a contiguous 1/NW of it.
 template <bool BF16, int NW>
@@ -119,6 +171,7 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(con
     uint64_t mine = 0;                // this lane's slot of the warp's list
     float thr = -INFINITY;            // value of the list's last key once full
     float m = -INFINITY, s = 0.0f;
+    // every lane runs the same number of iterations (warp-wide votes inside)
     for (int64_t base = v0 + lane; base - lane < v1; base += 32 * kPruneUnroll) {
         uint4 w[kPruneUnroll];
 #pragma unroll
@@ -127,34 +180,39 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(con
             const uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
             w[u] = idx < v1 ? ld_stream(rowv + idx) : make_uint4(ninf, ninf, ninf, ninf);
         }
+        const float vm = vec_max_n<BF16, kPruneUnroll>(w);
+        if (!(vm <= m)) {                 // new maximum (or NaN: poisons s)
+            s *= ex2((m - vm) * c);
+            m = vm;
+        }
+        if (m != -INFINITY) {
+            float t[kPruneUnroll];
 #pragma unroll
-        for (int u = 0; u < kPruneUnroll; ++u) {
-            float e[EPV];
-            if constexpr (BF16) {
-                e[0] = bf16_lo(w[u].x); e[1] = bf16_hi(w[u].x); e[2] = bf16_lo(w[u].y);
-                e[3] = bf16_hi(w[u].y); e[4] = bf16_lo(w[u].z); e[5] = bf16_hi(w[u].z);
-                e[6] = bf16_lo(w[u].w); e[7] = bf16_hi(w[u].w);
-            } else {
-                e[0] = __uint_as_float(w[u].x); e[1] = __uint_as_float(w[u].y);
-                e[2] = __uint_as_float(w[u].z); e[3] = __uint_as_float(w[u].w);
-            }
-            float vm = e[0];
+            for (int u = 0; u < kPruneUnroll; ++u) t[u] = vec_exp_sum<BF16>(w[u], m, c);
 #pragma unroll
-            for (int i = 1; i < EPV; ++i) asm("max.NaN.f32 %0, %0, %1;" : "+f"(vm) : "f"(e[i]));
-            if (!(vm <= m)) {
-                s *= ex2((m - vm) * c);
-                m = vm;
-            }
-            if (m != -INFINITY) {
+            for (int h = kPruneUnroll / 2; h > 0; h >>= 1)
 #pragma unroll
-                for (int i = 0; i < EPV; ++i) s += ex2((e[i] - m) * c);
+                for (int u = 0; u < h; ++u) t[u] += t[u + h];
+            s += t[0];
+        }
+        // candidates: only when some lane holds a value that may enter the list
+        if (__any_sync(0xffffffffu, vm >= thr && vm != -INFINITY)) {
+            // while the list is not full, the 16th largest lane maximum of
+            // this batch bounds the warp's 16th best from below
+            float floor = thr;
+            if (thr == -INFINITY) floor = warp_16th(vm, lane);
+#pragma unroll
+            for (int u = 0; u < kPruneUnroll; ++u) {
+                const float vmu = vec1_max<BF16>(w[u]);
+                if (__any_sync(0xffffffffu, vmu >= floor && vmu != -INFINITY)) {
+                    const int64_t vec = base + 32 * u;
+                    mine = wlist_absorb<BF16>(w[u], static_cast<uint32_t>(vec * EPV), vmu, mine,
+                                              floor, lane);
+                    const float t2 = wlist_threshold(mine);
+                    floor = t2 > floor ? t2 : floor;
+                }
             }
-            // warp-uniform: does any lane hold a value that may enter the list?
-            if (__any_sync(0xffffffffu, vm >= thr && vm != -INFINITY)) {
-                const int64_t vec = base + 32 * u;
-                mine = wlist_absorb<BF16>(w[u], static_cast<uint32_t>(vec * EPV), mine, lane);
-                thr = wlist_threshold(mine);
-            }
+            thr = wlist_threshold(mine);
         }
     }
     // row statistics: warp, then CTA
@@ -216,12 +274,21 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(con
     if (lane == 0) a.ncand[row] = n;      // 0 for a row with NaN / +inf / only -inf
 }
 
+// An integer with the order of a double (keys here are never NaN and never
+// -0: a sum that cancels to zero rounds to +0).  Integer compares keep the
+// ranking off the (slow) fp64 pipe.
+__device__ __forceinline__ long long ordered_i64(double d) {
+    const long long bits = __double_as_longlong(d);
+    return bits ^ ((bits >> 63) & 0x7fffffffffffffffLL);
+}
+
 __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     // dynamic shared memory: the lattice's log-probabilities [G][M] and raw
     // logits [G][M] (float), counts [G], then the back-pointers [G][W] parent
-    // and [G][W] rank
+    // and [G][W] rank, and the final paths' ranks [W][G]
     extern __shared__ __align__(16) unsigned char s_raw[];
     __shared__ double x_key[kBeamMaxExp];      // this step's expansions
+    __shared__ long long x_ord[kBeamMaxExp];   // x_key as an order-preserving integer
     __shared__ float x_score[kBeamMaxExp];
     __shared__ int x_lx[kBeamMaxExp];
     __shared__ double b_key[kCpsMaxBeam];      // the beams
@@ -238,10 +305,12 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     int* nc_s = reinterpret_cast<int*>(rl_s + G * M);
     unsigned char* bp_parent = reinterpret_cast<unsigned char*>(nc_s + G);
     unsigned char* bp_rank = bp_parent + G * W;
+    unsigned char* path_rank = bp_rank + G * W;
     int32_t* cids = a.cand_ids + static_cast<int64_t>(b) * G * M;
     float* clp = a.cand_logp + static_cast<int64_t>(b) * G * M;
     float* crl = a.cand_logit + static_cast<int64_t>(b) * G * M;
     int32_t* nc = a.ncand + static_cast<int64_t>(b) * G;
+#pragma unroll 4
     for (int i = lane; i < G * M; i += 32) {
         clp_s[i] = clp[i];
         rl_s[i] = crl[i];
@@ -281,11 +350,16 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     int ncur = 1;
     for (int j = 0; j < Lc && !empty; ++j) {
         const int n = eos_cut && j == Lc - 1 ? 1 : nc_s[j];   // EOS is kept alone
-        const int E = ncur * n;
-        // expansion e = (parent e / n, candidate e % n)
+        // A parent's expansions come in candidate order (raw logits sorted,
+        // ties by id), so only its first W can be among the W best.
+        const int nw = n < W ? n : W;
+        const int E = ncur * nw;
+        // expansion e = (parent e / nw, candidate e % nw)
         for (int e = lane; e < E; e += 32) {
-            const int par = e / n, r = e - par * n;
-            x_key[e] = b_key[par] + static_cast<double>(rl_s[j * M + r]);
+            const int par = e / nw, r = e - par * nw;
+            const double key = b_key[par] + static_cast<double>(rl_s[j * M + r]);
+            x_key[e] = key;
+            x_ord[e] = ordered_i64(key);
             x_score[e] = b_score[par] + clp_s[j * M + r];
             x_lx[e] = b_lex[par] * n + r;
         }
@@ -294,20 +368,20 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
         // desc, then lexicographic place asc); the first W are kept
         const int keep = E < W ? E : W;
         for (int e = lane; e < E; e += 32) {
-            const double k = x_key[e];
+            const long long k = x_ord[e];
             const int l = x_lx[e];
             int rank = 0;
             for (int e2 = 0; e2 < E; ++e2) {
-                const double k2 = x_key[e2];
+                const long long k2 = x_ord[e2];
                 rank += (k2 > k) || (k2 == k && x_lx[e2] < l);
             }
             if (rank < keep) {
-                const int par = e / n;
-                n_key[rank] = k;
+                const int par = e / nw;
+                n_key[rank] = x_key[e];
                 n_score[rank] = x_score[e];
                 n_lx[rank] = l;
                 bp_parent[j * W + rank] = static_cast<unsigned char>(par);
-                bp_rank[j * W + rank] = static_cast<unsigned char>(e - par * n);
+                bp_rank[j * W + rank] = static_cast<unsigned char>(e - par * nw);
             }
         }
         __syncwarp();
@@ -323,22 +397,23 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
         ncur = keep;
     }
     const int np = empty ? 0 : ncur;
-    // back-track the paths of the final beams
-    if (lane < W) {
-        int32_t* path = a.paths + (static_cast<int64_t>(b) * W + lane) * G;
-        if (lane < np) {
-            int cur = lane;
-            for (int j = Lc - 1; j >= 0; --j) {
-                const int r = bp_rank[j * W + cur];
-                path[j] = cids[j * M + r];
-                cur = bp_parent[j * W + cur];
-            }
-            for (int j = Lc; j < G; ++j) path[j] = -1;
-            a.path_logp[static_cast<int64_t>(b) * W + lane] = b_score[lane];
-        } else {
-            for (int j = 0; j < G; ++j) path[j] = -1;
-            a.path_logp[static_cast<int64_t>(b) * W + lane] = -INFINITY;
+    // back-track the final beams' candidate ranks in shared memory, then
+    // gather their ids with independent loads
+    if (lane < np) {
+        int cur = lane;
+        for (int j = Lc - 1; j >= 0; --j) {
+            path_rank[lane * G + j] = bp_rank[j * W + cur];
+            cur = bp_parent[j * W + cur];
         }
+    }
+    if (lane < W)
+        a.path_logp[static_cast<int64_t>(b) * W + lane] = lane < np ? b_score[lane] : -INFINITY;
+    __syncwarp();
+    int32_t* paths = a.paths + static_cast<int64_t>(b) * W * G;
+#pragma unroll 4
+    for (int i = lane; i < W * G; i += 32) {
+        const int w = i / G, j = i - w * G;
+        paths[i] = w < np && j < Lc ? cids[j * M + path_rank[i]] : -1;
     }
     if (lane == 0) {
         a.npaths[b] = np;
@@ -379,7 +454,7 @@ cudaError_t launch_cps_prune(const CpsArgs& a, bool bf16, cudaStream_t s) {
 
 cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(a.G) * a.mmax * 8 + static_cast<size_t>(a.G) * 4 +
-                        static_cast<size_t>(2) * a.G * a.beam;
+                        static_cast<size_t>(3) * a.G * a.beam;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(
             cps_beam_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -57,6 +57,56 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Max of the logits of N 16-byte vectors (packed pairs for bf16); NaN
+// propagates so that a NaN row is caught.
+template <bool BF16, int N>
+__device__ __forceinline__ float vec_max_n(const uint4 (&v)[N]) {
+    if constexpr (BF16) {
+        uint32_t m[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+#pragma unroll
+        for (int u = 1; u < N; ++u) {
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(v[u].x));
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[1]) : "r"(v[u].y));
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[2]) : "r"(v[u].z));
+            asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[3]) : "r"(v[u].w));
+        }
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(m[1]));
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[2]) : "r"(m[3]));
+        asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(m[0]) : "r"(m[2]));
+        float r;
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(bf16_lo(m[0])), "f"(bf16_hi(m[0])));
+        return r;
+    } else {
+        float r = __uint_as_float(v[0].x);
+#pragma unroll
+        for (int u = 0; u < N; ++u) {
+            const float e[4] = {__uint_as_float(v[u].x), __uint_as_float(v[u].y),
+                                __uint_as_float(v[u].z), __uint_as_float(v[u].w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) asm("max.NaN.f32 %0, %0, %1;" : "+f"(r) : "f"(e[i]));
+        }
+        return r;
+    }
+}
+
+// Sum of 2^{(l - m) c} over the logits of one 16-byte vector (pairwise tree).
+template <bool BF16>
+__device__ __forceinline__ float vec_exp_sum(const uint4& v, float m, float c) {
+    if constexpr (BF16) {
+        const float e0 = ex2((bf16_lo(v.x) - m) * c), e1 = ex2((bf16_hi(v.x) - m) * c);
+        const float e2 = ex2((bf16_lo(v.y) - m) * c), e3 = ex2((bf16_hi(v.y) - m) * c);
+        const float e4 = ex2((bf16_lo(v.z) - m) * c), e5 = ex2((bf16_hi(v.z) - m) * c);
+        const float e6 = ex2((bf16_lo(v.w) - m) * c), e7 = ex2((bf16_hi(v.w) - m) * c);
+        return ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
+    } else {
+        const float e0 = ex2((__uint_as_float(v.x) - m) * c);
+        const float e1 = ex2((__uint_as_float(v.y) - m) * c);
+        const float e2 = ex2((__uint_as_float(v.z) - m) * c);
+        const float e3 = ex2((__uint_as_float(v.w) - m) * c);
+        return (e0 + e1) + (e2 + e3);
+    }
+}
+
 // Merge two partial softmax statistics (max m, sum s of 2^{(l - m) c}).
 // NaN sums propagate; an empty partial (s == 0) contributes nothing.
 __device__ __forceinline__ void merge_stat(float& m, float& s, float m2, float s2, float c) {
