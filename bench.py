@@ -202,13 +202,16 @@ def traffic_per_row(profile: str = None, sources=None):
         return None
 
 
-def step_bytes(w: synth.Workload, accept_len, greedy: bool = False) -> dict:
-    """Algorithmic bytes of one step: every logit row once, the re-read rows
-    of the draw (two for a residual, one for a bonus or a greedy replacement),
-    drafts, outputs."""
+def step_bytes(w: synth.Workload, accept_len, greedy: bool = False,
+               shared_prefix_row: bool = False) -> dict:
+    """Algorithmic bytes of one step: every logit row read once (one prefix
+    row per sequence when the drafts share it), the re-read rows of the draw
+    (two for a residual, one for a bonus or a greedy replacement), drafts,
+    outputs."""
     elt = 2 if w.dtype == torch.bfloat16 else 4
     q_rows = 0 if greedy else (w.B if w.shared_q else w.B * w.K) * w.gamma
-    rows = w.B * w.K * (w.gamma + 1) + q_rows
+    p_rows = w.B * (w.K * w.gamma + 1) if shared_prefix_row else w.B * w.K * (w.gamma + 1)
+    rows = p_rows + q_rows
     reread = sum(2 if int(L) < w.gamma and not greedy else 1 for L in accept_len)
     k1 = elt * w.V * rows
     total = k1 + elt * w.V * reread + w.B * w.K * w.gamma * 4 + w.B * 12
@@ -228,8 +231,10 @@ def run_sdv(args, rank, world, local):
     else:
         w = synth.workload(args.workload, device=dev, seed=args.workload + 1000 * rank, B=args.batch)
     stream = torch.cuda.Stream(device=dev)
+    # drafts from one pass's marginals also share the prefix row (j = 0)
+    prefix_row = bool(w.shared_q)
     v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q,
-                    greedy=args.greedy)
+                    greedy=args.greedy, shared_prefix_row=prefix_row)
     if args.greedy:
         w.q_logits = None
         torch.cuda.empty_cache()
@@ -280,7 +285,7 @@ def run_sdv(args, rank, world, local):
     tokens_per_step = w.B * w.K * w.gamma
     value = world * tokens_per_step * args.steps / (ms_max / 1e3)
     ms_step = ms_max / args.steps
-    sb = step_bytes(w, accept_len, greedy=args.greedy)
+    sb = step_bytes(w, accept_len, greedy=args.greedy, shared_prefix_row=prefix_row)
     peak, peak_kind = measured_peaks()
     k1_gbs = sb["k1"] / (ms_kernels[0] * 1e-3) / 1e9 if ms_kernels[0] > 0 else None
     step_gbs = sb["total"] / (ms_step * 1e-3) / 1e9
@@ -314,9 +319,11 @@ def run_sdv(args, rank, world, local):
         "config": {"workload": w.name, "B": w.B, "K": w.K, "gamma": w.gamma, "V": w.V,
                    "q_layout": ("none (greedy acceptance)" if args.greedy else
                                 "[B,gamma,V] shared by the K drafts" if w.shared_q else "[B,K,gamma,V]"),
+                   "prefix_row": "one per sequence" if prefix_row else "one per draft",
                    "temperatures": "per-sequence {0.6, 1.0}" if w.temps is not None else w.temperature,
                    "l2": "inputs %.2f GB > L2 (126 MB): no flush" % (sb["k1"] / 1e9),
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "1 GPU"},
+        "committed_tokens_per_s": world * sum(int(L) + 1 for L in accept_len) * args.steps / (ms_max / 1e3),
         "hbm": {"step_gbs": round(step_gbs, 1), "frac": round(step_gbs / peak, 4),
                 "bytes_per_step": sb["total"], "reread_rows": sb["reread_rows"]},
         "kernel_ms": {"rowpass": ms_kernels[0], "select": ms_kernels[1], "sample": ms_kernels[2],
@@ -479,6 +486,18 @@ def run_cps(args, rank, world):
     return res
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w: synth.Workload):
     import oracle
     cores = os.cpu_count() or 1
@@ -488,9 +507,15 @@ def cpu_baseline(w: synth.Workload):
     t0 = time.perf_counter()
     oracle.verify(p, q, d, t, w.seed, nthreads=nt)
     dt = time.perf_counter() - t0
+    # the same oracle on one thread, first sequence only
+    t1 = time.perf_counter()
+    oracle.verify(p[:1], q[:1], d[:1], t[:1], w.seed, nthreads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": S * w.K * w.gamma / dt, "unit": UNIT, "cores": nt, "kind": "oracle",
+            "single_thread": w.K * w.gamma / dt1, "cpu": "%s, %d cores" % (cpu_model(), cores),
             "sample": "first %d of %d sequences of the same workload, one thread per sequence "
-                      "(%.1f s wall)" % (S, w.B, dt)}
+                      "(%.1f s wall); single_thread: the first sequence on one thread "
+                      "(%.1f s)" % (S, w.B, dt, dt1)}
 
 
 # ---------------------------------------------------------------------------

@@ -23,6 +23,7 @@ SDV_OK, SDV_ERR_ARG, SDV_ERR_CUDA, SDV_ERR_OOM, SDV_ERR_DEVICE_DATA, SDV_ERR_SCR
 SDV_BF16, SDV_F32 = 0, 1
 SDV_FLAG_SHARED_Q = 1
 SDV_FLAG_GREEDY = 2
+SDV_FLAG_SHARED_PREFIX_ROW = 4
 STATUS_NAMES = {0: "SDV_OK", 1: "SDV_ERR_ARG", 2: "SDV_ERR_CUDA", 3: "SDV_ERR_OOM",
                 4: "SDV_ERR_DEVICE_DATA", 5: "SDV_ERR_SCRATCH"}
 STATIC_SCRATCH_BYTES = 8 << 20
@@ -339,7 +340,8 @@ class Verifier:
     """
 
     def __init__(self, B: int, K: int, gamma: int, V: int, dtype=torch.bfloat16,
-                 device=None, stream=None, shared_q: bool = False, greedy: bool = False):
+                 device=None, stream=None, shared_q: bool = False, greedy: bool = False,
+                 shared_prefix_row: bool = False):
         self.B, self.K, self.gamma, self.V, self.dtype = B, K, gamma, V, dtype
         self.shared_q = shared_q
         self.greedy = greedy
@@ -349,7 +351,8 @@ class Verifier:
             self.stream = stream
             self.ctx = sdv_create(B, K, gamma, V, dtype, stream,
                                   (SDV_FLAG_SHARED_Q if shared_q else 0) |
-                                  (SDV_FLAG_GREEDY if greedy else 0))
+                                  (SDV_FLAG_GREEDY if greedy else 0) |
+                                  (SDV_FLAG_SHARED_PREFIX_ROW if shared_prefix_row else 0))
 
     def __call__(self, p_logits, q_logits, drafts, temperature: float = 1.0, seed: int = 0,
                  temps: Optional[torch.Tensor] = None, scores: bool = False, lse: bool = False,

@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassA
         if (row < a.rows_p) {
             rowv = static_cast<const uint4*>(a.p) + row * a.nvec;
             b = row / rows_per_seq_p;
+            // a prefix row (j = 0) of draft k > 0 that the shared one replaces
+            const int64_t r = row - b * rows_per_seq_p;
+            if ((a.flags & kFlagSharedPrefixRow) && r > a.G && r % (a.G + 1) == 0) return;
         } else {
             rowv = static_cast<const uint4*>(a.q) + (row - a.rows_p) * a.nvec;
             b = (row - a.rows_p) / rows_per_seq_q;

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const int k = tid / G, j = tid - (tid / G) * G;
         x0 = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
         if (x0 >= 0 && x0 < a.V) {
-            lp0 = load_logit(a.p, (seq_p + static_cast<int64_t>(k) * (G + 1) + j) * a.V + x0, BF16);
+            lp0 = load_logit(a.p, p_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
             if (!greedy) lq0 = load_logit(a.q, q_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
         }
     }
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     // Acceptance ratio at every drafted token of every draft.
     for (int idx = tid; idx < KG; idx += kSelectThreads) {
         const int k = idx / G, j = idx - (idx / G) * G;
-        const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + j;
+        const int64_t rp = p_row_index(a.flags, b, k, j, K, G);
         const int64_t rq = greedy ? 0 : q_row_index(a.flags, b, k, j, K, G);
         int32_t x = x0;
         float lp = lp0, lq = lq0;
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         SeqTask t = {};
         t.w = uniform24(r.y);
         t.c = c;
-        t.row_p = seq_p + static_cast<int64_t>(sel) * (G + 1) + L;
+        t.row_p = p_row_index(a.flags, b, sel, L, K, G);
         const float2 ps = pstat[sel * (G + 1) + L];
         t.mp = ps.x;
         t.inv_sp = 1.0f / ps.y;

@@ -41,10 +41,13 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ float key_value(uint64_t key) {
-    const uint32_t k = static_cast<uint32_t>(key >> 32);
+__device__ __forceinline__ float key32_value(uint32_t k) {
     const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
     return __uint_as_float(u);
+}
+
+__device__ __forceinline__ float key_value(uint64_t key) {
+    return key32_value(static_cast<uint32_t>(key >> 32));
 }
 
 // Key of (logit, id): value first, then the lower id.  0 = empty slot.
@@ -154,9 +157,12 @@ __device__ __forceinline__ float warp_16th(float x, int lane) {
 
 // One CTA of NW warps per row; each warp streams a contiguous 1/NW of it.
 template <bool BF16, int NW>
-__global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(const CpsArgs a) {
+__global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : 2) cps_prune_kernel(const CpsArgs a) {
     __shared__ uint64_t s_best[NW][kTopK];
     __shared__ float s_m[NW], s_s[NW];
+    // the highest list threshold any warp of the row has reached (order key):
+    // the row's 16th best is at least that, so every warp may skip below it
+    __shared__ unsigned s_floor;
     const int64_t row = blockIdx.x;
     const int b = static_cast<int>(row / a.G);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -167,6 +173,9 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(con
     const int64_t per_warp = (a.nvec + NW - 1) / NW;
     const int64_t v0 = warp * per_warp;
     const int64_t v1 = v0 + per_warp < a.nvec ? v0 + per_warp : a.nvec;
+
+    if (tid == 0) s_floor = order_key(-INFINITY);
+    __syncthreads();
 
     uint64_t mine = 0;                // this lane's slot of the warp's list
     float thr = -INFINITY;            // value of the list's last key once full
@@ -196,11 +205,16 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(con
             s += t[0];
         }
         // candidates: only when some lane holds a value that may enter the list
-        if (__any_sync(0xffffffffu, vm >= thr && vm != -INFINITY)) {
+        const float row_floor = key32_value(*reinterpret_cast<volatile unsigned*>(&s_floor));
+        const float gate = thr > row_floor ? thr : row_floor;
+        if (__any_sync(0xffffffffu, vm >= gate && vm != -INFINITY)) {
             // while the list is not full, the 16th largest lane maximum of
             // this batch bounds the warp's 16th best from below
-            float floor = thr;
-            if (thr == -INFINITY) floor = warp_16th(vm, lane);
+            float floor = gate;
+            if (thr == -INFINITY) {
+                const float t0 = warp_16th(vm, lane);
+                floor = t0 > floor ? t0 : floor;
+            }
 #pragma unroll
             for (int u = 0; u < kPruneUnroll; ++u) {
                 const float vmu = vec1_max<BF16>(w[u]);
@@ -213,6 +227,7 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 8 : 2) cps_prune_kernel(con
                 }
             }
             thr = wlist_threshold(mine);
+            if (lane == 0 && thr > row_floor) atomicMax(&s_floor, order_key(thr));
         }
     }
     // row statistics: warp, then CTA
@@ -437,8 +452,8 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
 }  // namespace
 
 cudaError_t launch_cps_prune(const CpsArgs& a, bool bf16, cudaStream_t s) {
-    // one CTA per row: 4 warps when the rows alone fill the GPU (8 CTAs per
-    // SM), 16 when they are few
+    // one CTA per row: 4 warps when the rows fill the GPU (7 CTAs per SM,
+    // 1064 on 152 SMs: one wave up to that many rows), 16 when they are few
     const int64_t rows = static_cast<int64_t>(a.B) * a.G;
     const unsigned grid = static_cast<unsigned>(rows);
     const bool wide = rows < 600;

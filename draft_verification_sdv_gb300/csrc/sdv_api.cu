@@ -47,6 +47,10 @@ struct sdv_ctx {
     char err[512];
 };
 
+static_assert(SDV_FLAG_SHARED_Q == sdv::kFlagSharedQ && SDV_FLAG_GREEDY == sdv::kFlagGreedy &&
+                  SDV_FLAG_SHARED_PREFIX_ROW == sdv::kFlagSharedPrefixRow,
+              "public layout flags and kernel flags must agree");
+
 namespace {
 
 sdv_status fail(sdv_ctx* ctx, sdv_status st, const char* fmt, ...) {
@@ -91,7 +95,9 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
                          void* stream, unsigned flags) {
     if (!out) return SDV_ERR_ARG;
     *out = nullptr;
-    if (flags & ~static_cast<unsigned>(SDV_FLAG_SHARED_Q | SDV_FLAG_GREEDY)) return SDV_ERR_ARG;
+    if (flags & ~static_cast<unsigned>(SDV_FLAG_SHARED_Q | SDV_FLAG_GREEDY |
+                                       SDV_FLAG_SHARED_PREFIX_ROW))
+        return SDV_ERR_ARG;
     if ((flags & SDV_FLAG_SHARED_Q) && (flags & SDV_FLAG_GREEDY)) return SDV_ERR_ARG;
     if (B < 1 || K < 1 || gamma < 1 || V < 1) return SDV_ERR_ARG;
     if (dtype != SDV_BF16 && dtype != SDV_F32) return SDV_ERR_ARG;

@@ -11,7 +11,17 @@ namespace sdv {
 enum : unsigned {
     kFlagSharedQ = 1u,       // q is [B][G][V]: one marginal row per (b, j), shared by all k
     kFlagGreedy = 2u,        // greedy acceptance: no drafter rows at all
+    kFlagSharedPrefixRow = 4u,   // the verifier row at j = 0 is (b, 0, 0) for every k
 };
+
+// Row index of the verifier row of (b, k, j) within the p buffer.  The row at
+// j = 0 sees only the prefix s, so with kFlagSharedPrefixRow the row of draft
+// 0 serves every draft (the others are not read).
+__host__ __device__ __forceinline__ int64_t p_row_index(unsigned flags, int b, int k, int j, int K,
+                                                        int G) {
+    const int kk = (flags & kFlagSharedPrefixRow) && j == 0 ? 0 : k;
+    return (static_cast<int64_t>(b) * K + kk) * (G + 1) + j;
+}
 
 // Row index of the drafter row of (b, k, j) within the q buffer.
 __host__ __device__ __forceinline__ int64_t q_row_index(unsigned flags, int b, int k, int j, int K,

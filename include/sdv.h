@@ -115,6 +115,17 @@ sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V,
  */
 #define SDV_FLAG_GREEDY 2u
 
+/*
+ * SDV_FLAG_SHARED_PREFIX_ROW: the verifier row at position 0 of every draft
+ * conditions only on the shared prefix s (same page, section 5.2: the K
+ * drafts extend one prefix), so it is one row per sequence: row (b, 0, 0) of
+ * p_logits serves every draft k and rows (b, k > 0, 0) are not read (their
+ * contents do not matter).  p_logits keeps its [B][K][gamma+1][V] shape.
+ * Results equal those of the full layout with row (b, 0, 0) copied to every
+ * k.  Combines with either flag above.
+ */
+#define SDV_FLAG_SHARED_PREFIX_ROW 4u
+
 /* sdv_create with layout flags (0 = the full [B][K][gamma][V] q layout). */
 sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V,
                          sdv_dtype dtype, void* stream, unsigned flags);

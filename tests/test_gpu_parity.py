@@ -28,9 +28,10 @@ def _lib():
     bd.load(build=True)
 
 
-def run_gpu(w: synth.Workload, seed=None, stream=None, greedy=False):
-    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q,
-                    greedy=greedy)
+def run_gpu(w: synth.Workload, seed=None, stream=None, greedy=False, shared_prefix_row=False):
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream,
+                    shared_q=w.shared_q and not greedy, greedy=greedy,
+                    shared_prefix_row=shared_prefix_row)
     out = v(w.p_logits, None if greedy else w.q_logits, w.drafts, temperature=w.temperature,
             seed=w.seed if seed is None else seed, temps=w.temps, scores=True, lse=True)
     status = bd.sdv_sync(v.ctx)
@@ -421,6 +422,45 @@ def test_greedy_large_window_sampled():
     assert compare(gpu, orc, seqs, tag="greedy large-window") <= 1
     del w
     torch.cuda.empty_cache()
+
+
+def _poison_prefix_rows(w):
+    """A copy of w whose prefix rows (b, k > 0, 0) hold NaN: with the shared
+    prefix-row layout they must not be read."""
+    p = w.p_logits.clone()
+    p[:, 1:, 0, :] = float("nan")
+    return synth.Workload(name=w.name + " poisoned", B=w.B, K=w.K, gamma=w.gamma, V=w.V,
+                          dtype=w.dtype, p_logits=p, q_logits=w.q_logits, drafts=w.drafts,
+                          temperature=w.temperature, temps=w.temps, seed=w.seed,
+                          shared_q=w.shared_q)
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_shared_prefix_row_reads_one_prefix_row(greedy):
+    """With SDV_FLAG_SHARED_PREFIX_ROW the other drafts' prefix rows are never
+    read (NaN there changes nothing) and the outputs equal, bit for bit, the
+    full layout's on inputs whose prefix rows are identical."""
+    w = synth.generate_shared(5, 4, 6, 12000, temps=torch.tensor([0.6, 1.0, 1.3, 0.8, 1.0]),
+                              seed=113, device="cuda")
+    assert torch.equal(w.p_logits[:, 1:, 0], w.p_logits[:, :1, 0].expand(-1, w.K - 1, -1))
+    ref = run_gpu(w, seed=7, greedy=greedy)
+    got = run_gpu(_poison_prefix_rows(w), seed=7, greedy=greedy, shared_prefix_row=True)
+    assert got["status"] == bd.SDV_OK
+    for k in ("sel", "accept_len", "next_token", "scores", "lse"):
+        assert np.array_equal(got[k], ref[k]), k
+    orc = run_oracle(w, seed=7, greedy=greedy)
+    assert compare(got, orc, tag="prefix row") <= 1
+
+
+def test_shared_prefix_row_with_full_q_layout():
+    w = synth.workload(3, device="cuda", seed=3)
+    p = w.p_logits.clone()
+    p[:, 1:, 0] = p[:, :1, 0]
+    w.p_logits = p
+    ref = run_gpu(w)
+    got = run_gpu(_poison_prefix_rows(w), shared_prefix_row=True)
+    for k in ("sel", "accept_len", "next_token", "scores", "lse"):
+        assert np.array_equal(got[k], ref[k]), k
 
 
 def test_greedy_rejects_shared_q_combination():
