@@ -26,6 +26,8 @@
 // (exact for bf16 logits), with equal sums in lexicographic order of their
 // candidate ranks (tracked as each beam's place among the beams).  With a
 // separable score this gives the W best paths of the whole lattice.
+#include <climits>
+
 #include "sdv_device.cuh"
 #include "sdv_plan.h"
 
@@ -174,6 +176,8 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : 2) cps_prune_kernel(con
     const int64_t v0 = warp * per_warp;
     const int64_t v1 = v0 + per_warp < a.nvec ? v0 + per_warp : a.nvec;
 
+    // let the beam launch now: it waits for this grid before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) s_floor = order_key(-INFINITY);
     __syncthreads();
 
@@ -325,10 +329,26 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     float* clp = a.cand_logp + static_cast<int64_t>(b) * G * M;
     float* crl = a.cand_logit + static_cast<int64_t>(b) * G * M;
     int32_t* nc = a.ncand + static_cast<int64_t>(b) * G;
+    // launched as a programmatic dependent of the pruning pass: wait for it
+    // before reading the lattice
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if ((G * M) % 4 == 0 &&
+        ((reinterpret_cast<uintptr_t>(clp) | reinterpret_cast<uintptr_t>(crl)) & 15u) == 0) {
+        const float4* c4 = reinterpret_cast<const float4*>(clp);
+        const float4* r4 = reinterpret_cast<const float4*>(crl);
+        float4* cs4 = reinterpret_cast<float4*>(clp_s);
+        float4* rs4 = reinterpret_cast<float4*>(rl_s);
 #pragma unroll 4
-    for (int i = lane; i < G * M; i += 32) {
-        clp_s[i] = clp[i];
-        rl_s[i] = crl[i];
+        for (int i = lane; i < G * M / 4; i += 32) {
+            cs4[i] = c4[i];
+            rs4[i] = r4[i];
+        }
+    } else {
+#pragma unroll 4
+        for (int i = lane; i < G * M; i += 32) {
+            clp_s[i] = clp[i];
+            rl_s[i] = crl[i];
+        }
     }
     for (int i = lane; i < G; i += 32) nc_s[i] = nc[i];
     __syncwarp();
@@ -352,16 +372,13 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     for (int j = lane; j < Lc; j += 32) empty |= nc_s[j] == 0;
     empty = __any_sync(0xffffffffu, empty);
 
-    // Beams: order key (sum of raw logits, fp64: exact for bf16 logits, and
-    // the same operations as any left-to-right fp64 sum), score (sum of
-    // log-probabilities) and place among the beams in lexicographic order of
-    // their candidate ranks (the tie rule).
-    if (lane == 0) {
-        b_key[0] = 0.0;
-        b_score[0] = 0.0f;
-        b_lex[0] = 0;
-    }
-    __syncwarp();
+    // Beams, lane w holding beam w: order key (sum of raw logits, fp64:
+    // exact for bf16 logits, and the same operations as any left-to-right
+    // fp64 sum), score (sum of log-probabilities) and place among the beams
+    // in lexicographic order of their candidate ranks (the tie rule).
+    double bkey = 0.0;
+    float bscore = 0.0f;
+    int blex = 0;
     int ncur = 1;
     for (int j = 0; j < Lc && !empty; ++j) {
         const int n = eos_cut && j == Lc - 1 ? 1 : nc_s[j];   // EOS is kept alone
@@ -369,48 +386,103 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
         // ties by id), so only its first W can be among the W best.
         const int nw = n < W ? n : W;
         const int E = ncur * nw;
-        // expansion e = (parent e / nw, candidate e % nw)
-        for (int e = lane; e < E; e += 32) {
-            const int par = e / nw, r = e - par * nw;
-            const double key = b_key[par] + static_cast<double>(rl_s[j * M + r]);
-            x_key[e] = key;
-            x_ord[e] = ordered_i64(key);
-            x_score[e] = b_score[par] + clp_s[j * M + r];
-            x_lx[e] = b_lex[par] * n + r;
-        }
-        __syncwarp();
-        // each expansion's rank: how many expansions come before it (key
-        // desc, then lexicographic place asc); the first W are kept
         const int keep = E < W ? E : W;
-        for (int e = lane; e < E; e += 32) {
-            const long long k = x_ord[e];
-            const int l = x_lx[e];
+        // e / nw as a multiply and shift: exact for e < 256 and nw <= 16
+        const unsigned magic = (65536u + nw - 1) / nw;
+        if (E <= 32) {
+            // one expansion per lane, ranked with shuffles
+            const int e = lane;
+            const int par = static_cast<int>((e * magic) >> 16), r = e - par * nw;
+            const bool valid = e < E;
+            const float rl = rl_s[j * M + r], lp = clp_s[j * M + r];   // r < nw <= M
+            const double key = __shfl_sync(0xffffffffu, bkey, par) + static_cast<double>(rl);
+            const float sc = __shfl_sync(0xffffffffu, bscore, par) + lp;
+            const int lx = __shfl_sync(0xffffffffu, blex, par) * n + r;
+            const long long ord = valid ? ordered_i64(key) : LLONG_MIN;
             int rank = 0;
-            for (int e2 = 0; e2 < E; ++e2) {
-                const long long k2 = x_ord[e2];
-                rank += (k2 > k) || (k2 == k && x_lx[e2] < l);
+            for (int src = 0; src < E; ++src) {
+                const long long o2 = __shfl_sync(0xffffffffu, ord, src);
+                const int l2 = __shfl_sync(0xffffffffu, lx, src);
+                rank += (o2 > ord) || (o2 == ord && l2 < lx);
             }
-            if (rank < keep) {
-                const int par = e / nw;
-                n_key[rank] = x_key[e];
-                n_score[rank] = x_score[e];
-                n_lx[rank] = l;
+            if (valid && rank < keep) {
                 bp_parent[j * W + rank] = static_cast<unsigned char>(par);
-                bp_rank[j * W + rank] = static_cast<unsigned char>(e - par * nw);
+                bp_rank[j * W + rank] = static_cast<unsigned char>(r);
             }
-        }
-        __syncwarp();
-        if (lane < keep) {
-            const int l = n_lx[lane];
+            // beam t becomes the expansion ranked t
+            int new_lx = 0x7fffffff;
+            for (int t = 0; t < keep; ++t) {
+                const unsigned m = __ballot_sync(0xffffffffu, valid && rank == t);
+                const int src = __ffs(m) - 1;
+                const double k2 = __shfl_sync(0xffffffffu, key, src);
+                const float s2 = __shfl_sync(0xffffffffu, sc, src);
+                const int l2 = __shfl_sync(0xffffffffu, lx, src);
+                if (lane == t) {
+                    bkey = k2;
+                    bscore = s2;
+                    new_lx = l2;
+                }
+            }
             int pos = 0;
-            for (int t = 0; t < keep; ++t) pos += n_lx[t] < l;
-            b_key[lane] = n_key[lane];
-            b_score[lane] = n_score[lane];
-            b_lex[lane] = pos;
+            for (int t = 0; t < keep; ++t) pos += __shfl_sync(0xffffffffu, new_lx, t) < new_lx;
+            blex = pos;
+        } else {
+            // more expansions than lanes: through shared memory
+            if (lane < ncur) {
+                b_key[lane] = bkey;
+                b_score[lane] = bscore;
+                b_lex[lane] = blex;
+            }
+            __syncwarp();
+            for (int e = lane; e < E; e += 32) {
+                const int par = static_cast<int>((e * magic) >> 16), r = e - par * nw;
+                const double key = b_key[par] + static_cast<double>(rl_s[j * M + r]);
+                x_key[e] = key;
+                x_ord[e] = ordered_i64(key);
+                x_score[e] = b_score[par] + clp_s[j * M + r];
+                x_lx[e] = b_lex[par] * n + r;
+            }
+            __syncwarp();
+            // each expansion's rank: how many expansions come before it (key
+            // desc, then lexicographic place asc); the first W are kept
+            for (int e = lane; e < E; e += 32) {
+                const long long k = x_ord[e];
+                const int l = x_lx[e];
+                int rank = 0, e2 = 0;
+                for (; e2 + 4 <= E; e2 += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const long long k2 = x_ord[e2 + u];
+                        rank += (k2 > k) || (k2 == k && x_lx[e2 + u] < l);
+                    }
+                }
+                for (; e2 < E; ++e2) {
+                    const long long k2 = x_ord[e2];
+                    rank += (k2 > k) || (k2 == k && x_lx[e2] < l);
+                }
+                if (rank < keep) {
+                    const int par = static_cast<int>((e * magic) >> 16);
+                    n_key[rank] = x_key[e];
+                    n_score[rank] = x_score[e];
+                    n_lx[rank] = l;
+                    bp_parent[j * W + rank] = static_cast<unsigned char>(par);
+                    bp_rank[j * W + rank] = static_cast<unsigned char>(e - par * nw);
+                }
+            }
+            __syncwarp();
+            if (lane < keep) {
+                const int l = n_lx[lane];
+                int pos = 0;
+                for (int t = 0; t < keep; ++t) pos += n_lx[t] < l;
+                bkey = n_key[lane];
+                bscore = n_score[lane];
+                blex = pos;
+            }
+            __syncwarp();
         }
-        __syncwarp();
         ncur = keep;
     }
+    __syncwarp();
     const int np = empty ? 0 : ncur;
     // back-track the final beams' candidate ranks in shared memory, then
     // gather their ids with independent loads
@@ -422,7 +494,7 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
         }
     }
     if (lane < W)
-        a.path_logp[static_cast<int64_t>(b) * W + lane] = lane < np ? b_score[lane] : -INFINITY;
+        a.path_logp[static_cast<int64_t>(b) * W + lane] = lane < np ? bscore : -INFINITY;
     __syncwarp();
     int32_t* paths = a.paths + static_cast<int64_t>(b) * W * G;
 #pragma unroll 4
@@ -475,8 +547,20 @@ cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s) {
             cps_beam_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    cps_beam_kernel<<<a.B, 32, smem, s>>>(a);
-    return cudaGetLastError();
+    // a programmatic dependent of the kernel before it on the stream (the
+    // pruning pass triggers at its start): the launch overlaps that kernel's
+    // tail and the kernel waits for it before reading
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B));
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, cps_beam_kernel, a);
 }
 
 }  // namespace sdv
