@@ -48,3 +48,39 @@ def test_device_controller_reports_bad_length():
                         host.data_ptr(), None)
     assert st == bd.SDV_ERR_ARG
     assert L.sdv_adl_step(0, 2, 2, 8, 2, 1, None, None, None, None, None, None) == bd.SDV_OK
+
+
+def test_decode_step_chain_search_verify_control():
+    """One DiffuSpec-style step per iteration, all enqueued on the stream with
+    no host synchronisation in between: path search over the marginals ->
+    verification of the paths (shared marginals, shared prefix row) ->
+    draft-length update from the lattice length and the accepted length.
+    Each iteration's lengths are checked against the oracle's controller."""
+    import oracle
+    from draft_verification_sdv_gb300 import synth
+    B, K, G, V = 6, 3, 8, 4000
+    ctl = bd.DraftLengthController(B, 6, window=2, kmin=2, kmax=G, up=2, down=1)
+    st = oracle.adl_state(B, 2)
+    k_ref = np.full(B, 6, np.int32)
+    v = bd.Verifier(B, K, G, V, shared_q=True, shared_prefix_row=True)
+    gens, accs, ks = [], [], []
+    for it in range(3):
+        w = synth.generate_shared(B, K, G, V, q_sigma=torch.full((B, G), 0.6), temperature=1.0,
+                                  seed=80 + it, device="cuda")
+        w.q_logits[:, :, 17] = -30.0
+        w.q_logits[1, 5, 17] = 30.0                  # sequence 1 ends at position 5
+        cps = bd.sdv_cps(w.q_logits, tau=0.8, mmax=15, beam=K, eos_id=17)
+        # the caller pads the drafts past EOS with EOS itself
+        drafts = torch.where(cps["paths"] < 0, torch.full_like(cps["paths"], 17), cps["paths"])
+        out = v(w.p_logits, w.q_logits, drafts, temperature=1.0, seed=it)
+        ks.append(ctl.step(cps["lat_len"], out["accept_len"]).clone())
+        gens.append(cps["lat_len"].clone())
+        accs.append(out["accept_len"].clone())
+    torch.cuda.synchronize()
+    v.sync()
+    assert all(int(g[1]) == 6 for g in gens) and all((g[[0, 2, 3, 4, 5]] == G).all() for g in gens)
+    for g, a, k in zip(gens, accs, ks):
+        k_ref = oracle.adl_step(k_ref, g.cpu().numpy(), a.cpu().numpy(), st, W=2, kmin=2, kmax=G,
+                                up=2, down=1)
+        assert np.array_equal(k.cpu().numpy(), k_ref)
+    v.close()
