@@ -75,14 +75,42 @@ __device__ __forceinline__ float wlist_threshold(uint64_t mine) {
     return last ? key_value(last) : -INFINITY;
 }
 
+// Logit i of a 16-byte vector (selects, no local memory).
+template <bool BF16>
+__device__ __forceinline__ float vec_elem(uint32_t x, uint32_t y, uint32_t z, uint32_t w, int i) {
+    if constexpr (BF16) {
+        const uint32_t wd = i < 4 ? (i < 2 ? x : y) : (i < 6 ? z : w);
+        return (i & 1) ? bf16_hi(wd) : bf16_lo(wd);
+    } else {
+        return __uint_as_float(i < 2 ? (i == 0 ? x : y) : (i == 2 ? z : w));
+    }
+}
+
+// The list seeded with the 16 largest of the lanes' keys (0 = none): a
+// bitonic sort of the 32 keys, descending, of which lanes 0..15 keep theirs.
+__device__ __forceinline__ uint64_t wlist_seed(uint64_t key, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t other = __shfl_xor_sync(0xffffffffu, key, j);
+            const bool take_max = ((lane & j) == 0) == ((lane & k) == 0);
+            const uint64_t hi = key > other ? key : other, lo = key > other ? other : key;
+            key = take_max ? hi : lo;
+        }
+    }
+    return lane < kTopK ? key : 0;
+}
+
 // Offer the lanes' 16-byte vectors (lane's ids id0 .. id0 + EPV - 1, its
 // vector max vmax) to the warp's list.  Only lanes whose vector reaches
 // `floor` (a value the warp's 16th best is known to reach) take part: each in
 // turn broadcasts its vector, lanes 0 .. EPV-1 take one logit each, and the
 // logits that beat the list's last key are inserted.
+// With `dedup`, a key already in the list (a seeded one) is not inserted again.
 template <bool BF16>
 __device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, float vmax, uint64_t mine,
-                                              float floor, int lane) {
+                                              float floor, bool dedup, int lane) {
     constexpr int EPV = BF16 ? 8 : 4;
     uint64_t last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
     unsigned hot = __ballot_sync(0xffffffffu, vmax >= floor && vmax != -INFINITY);
@@ -95,15 +123,7 @@ __device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, float vmax,
         const uint32_t w = __shfl_sync(0xffffffffu, v.w, src);
         const uint32_t base = __shfl_sync(0xffffffffu, id0, src);
         const int i = lane & (EPV - 1);
-        uint32_t wd;
-        float f;
-        if constexpr (BF16) {
-            wd = i < 4 ? (i < 2 ? x : y) : (i < 6 ? z : w);
-            f = (i & 1) ? bf16_hi(wd) : bf16_lo(wd);
-        } else {
-            wd = i < 2 ? (i == 0 ? x : y) : (i == 2 ? z : w);
-            f = __uint_as_float(wd);
-        }
+        const float f = vec_elem<BF16>(x, y, z, w, i);
         const uint64_t key = cand_key(f, base + i);
         // a -inf logit has probability zero and is never a candidate
         unsigned pending = __ballot_sync(
@@ -112,7 +132,7 @@ __device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, float vmax,
             const int l = __ffs(pending) - 1;
             pending &= pending - 1;
             const uint64_t k = __shfl_sync(0xffffffffu, key, l);
-            if (k > last) {
+            if (k > last && !(dedup && __any_sync(0xffffffffu, mine == k))) {
                 mine = wlist_insert(mine, k, lane);
                 last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
             }
@@ -121,7 +141,7 @@ __device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, float vmax,
     return mine;
 }
 
-constexpr int kPruneUnroll = 8;            // 16-byte vectors in flight per lane
+constexpr int kHalf = 4;                   // 16-byte vectors per lane in each half-batch
 
 // NaN-propagating max of one 16-byte vector.
 template <bool BF16>
@@ -184,55 +204,106 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : 2) cps_prune_kernel(con
     uint64_t mine = 0;                // this lane's slot of the warp's list
     float thr = -INFINITY;            // value of the list's last key once full
     float m = -INFINITY, s = 0.0f;
-    // every lane runs the same number of iterations (warp-wide votes inside)
-    for (int64_t base = v0 + lane; base - lane < v1; base += 32 * kPruneUnroll) {
-        uint4 w[kPruneUnroll];
-#pragma unroll
-        for (int u = 0; u < kPruneUnroll; ++u) {
-            const int64_t idx = base + 32 * u;
-            const uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
-            w[u] = idx < v1 ? ld_stream(rowv + idx) : make_uint4(ninf, ninf, ninf, ninf);
-        }
-        const float vm = vec_max_n<BF16, kPruneUnroll>(w);
+    // One half-batch of kHalf vectors per lane: the softmax statistics, then
+    // the candidates when some lane holds a value that may enter the list.
+    auto process = [&](const uint4 (&w)[kHalf], int64_t base) {
+        const float vm = vec_max_n<BF16, kHalf>(w);
         if (!(vm <= m)) {                 // new maximum (or NaN: poisons s)
             s *= ex2((m - vm) * c);
             m = vm;
         }
         if (m != -INFINITY) {
-            float t[kPruneUnroll];
+            float t[kHalf];
 #pragma unroll
-            for (int u = 0; u < kPruneUnroll; ++u) t[u] = vec_exp_sum<BF16>(w[u], m, c);
+            for (int u = 0; u < kHalf; ++u) t[u] = vec_exp_sum<BF16>(w[u], m, c);
 #pragma unroll
-            for (int h = kPruneUnroll / 2; h > 0; h >>= 1)
+            for (int h = kHalf / 2; h > 0; h >>= 1)
 #pragma unroll
                 for (int u = 0; u < h; ++u) t[u] += t[u + h];
             s += t[0];
         }
-        // candidates: only when some lane holds a value that may enter the list
         const float row_floor = key32_value(*reinterpret_cast<volatile unsigned*>(&s_floor));
         const float gate = thr > row_floor ? thr : row_floor;
-        if (__any_sync(0xffffffffu, vm >= gate && vm != -INFINITY)) {
-            // while the list is not full, the 16th largest lane maximum of
-            // this batch bounds the warp's 16th best from below
-            float floor = gate;
-            if (thr == -INFINITY) {
+        if (!__any_sync(0xffffffffu, vm >= gate && vm != -INFINITY)) return;
+        float floor = gate;
+        float vmu[kHalf];
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) vmu[u] = vec1_max<BF16>(w[u]);
+        bool seeded = false;
+        if (thr == -INFINITY) {
+            if (!__any_sync(0xffffffffu, mine != 0)) {
+                // empty list: seed it with the 16 largest lane maxima (each
+                // lane's first maximum, the lowest id); the 16th bounds the
+                // warp's 16th best from below
+                int uu = 0;
+#pragma unroll
+                for (int u = kHalf - 1; u >= 0; --u) uu = vmu[u] == vm ? u : uu;
+                uint4 v = w[0];
+#pragma unroll
+                for (int u = 1; u < kHalf; ++u) v = u == uu ? w[u] : v;
+                int ii = 0;
+#pragma unroll
+                for (int i = EPV - 1; i >= 0; --i)
+                    ii = vec_elem<BF16>(v.x, v.y, v.z, v.w, i) == vm ? i : ii;
+                const uint32_t id = static_cast<uint32_t>((base + 32 * uu) * EPV + ii);
+                const bool real = vm != -INFINITY && vm == vm;
+                const uint64_t key0 = real ? cand_key(vm, id) : 0;
+                mine = wlist_seed(key0, lane);
+                seeded = true;
+                const float t0 = wlist_threshold(mine);
+                floor = t0 > floor ? t0 : floor;
+                // a lane whose seeded maximum is its only logit at or above
+                // the floor has nothing more to offer from that vector
+                float m2 = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < EPV; ++i) {
+                    const float e = vec_elem<BF16>(v.x, v.y, v.z, v.w, i);
+                    m2 = i != ii && e > m2 ? e : m2;
+                }
+                const uint64_t last = __shfl_sync(0xffffffffu, mine, kTopK - 1);
+                if (real && key0 >= last && !(m2 >= floor)) {
+#pragma unroll
+                    for (int u = 0; u < kHalf; ++u) vmu[u] = u == uu ? -INFINITY : vmu[u];
+                }
+            } else {
+                // a partly filled list: the 16th largest lane maximum of
+                // this batch bounds the warp's 16th best from below
                 const float t0 = warp_16th(vm, lane);
                 floor = t0 > floor ? t0 : floor;
             }
-#pragma unroll
-            for (int u = 0; u < kPruneUnroll; ++u) {
-                const float vmu = vec1_max<BF16>(w[u]);
-                if (__any_sync(0xffffffffu, vmu >= floor && vmu != -INFINITY)) {
-                    const int64_t vec = base + 32 * u;
-                    mine = wlist_absorb<BF16>(w[u], static_cast<uint32_t>(vec * EPV), vmu, mine,
-                                              floor, lane);
-                    const float t2 = wlist_threshold(mine);
-                    floor = t2 > floor ? t2 : floor;
-                }
-            }
-            thr = wlist_threshold(mine);
-            if (lane == 0 && thr > row_floor) atomicMax(&s_floor, order_key(thr));
         }
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) {
+            if (__any_sync(0xffffffffu, vmu[u] >= floor && vmu[u] != -INFINITY)) {
+                const int64_t vec = base + 32 * u;
+                mine = wlist_absorb<BF16>(w[u], static_cast<uint32_t>(vec * EPV), vmu[u], mine,
+                                          floor, seeded, lane);
+                const float t2 = wlist_threshold(mine);
+                floor = t2 > floor ? t2 : floor;
+            }
+        }
+        thr = wlist_threshold(mine);
+        if (lane == 0 && thr > row_floor) atomicMax(&s_floor, order_key(thr));
+    };
+    auto load = [&](uint4 (&w)[kHalf], int64_t base) {
+#pragma unroll
+        for (int u = 0; u < kHalf; ++u) {
+            const int64_t idx = base + 32 * u;
+            const uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
+            w[u] = idx < v1 ? ld_stream(rowv + idx) : make_uint4(ninf, ninf, ninf, ninf);
+        }
+    };
+    // Two half-batches in turn: one is in flight while the other is
+    // processed, so the loads continue through the candidate work.  Every
+    // lane runs the same number of iterations (warp-wide votes inside).
+    uint4 wa[kHalf], wb[kHalf];
+    int64_t base = v0 + lane;
+    load(wa, base);
+    for (; base - lane < v1; base += 64 * kHalf) {
+        load(wb, base + 32 * kHalf);
+        process(wa, base);
+        load(wa, base + 64 * kHalf);
+        process(wb, base + 32 * kHalf);
     }
     // row statistics: warp, then CTA
 #pragma unroll
