@@ -142,6 +142,7 @@ __device__ __noinline__ uint64_t wlist_absorb(uint4 v, uint32_t id0, float vmax,
 }
 
 constexpr int kHalf = 4;                   // 16-byte vectors per lane in each half-batch
+static_assert((kHalf & (kHalf - 1)) == 0, "the pairwise sum tree needs a power of two");
 
 // NaN-propagating max of one 16-byte vector.
 template <bool BF16>
