@@ -158,8 +158,9 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         }
         ratio[idx] = r;
     }
-    // The bonus rows (j = G): validity and LSE.
-    for (int k = tid; k < K; k += kSelectThreads) {
+    // The bonus rows (j = G): validity and LSE, on the last threads (idle
+    // above when K * G leaves them free).
+    for (int k = kSelectThreads - 1 - tid; k < K; k += kSelectThreads) {
         const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + G;
         float mp, sp;
         merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);

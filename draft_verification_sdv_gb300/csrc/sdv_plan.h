@@ -214,16 +214,20 @@ constexpr int kRowPassThreads = 256;
 // waves (that balances SMs whose bandwidth differs; a persistent grid with a
 // static item order does not).  Chunks target kChunkTargetVec vectors
 // (76 KB of bf16), are split further until there are at least
-// kMinItemWaves waves of resident warps, stay >= 64 vectors, and are rounded
-// to 8 vectors (128 bytes).  Chunks are fixed per row, so rows with the same
-// bytes give bit-identical partials wherever they sit.
+// kMinItemWaves waves of resident warps, but to at most kMaxChunks per row
+// (the select kernel merges a row's partials on one thread), stay >= 64
+// vectors, and are rounded to 8 vectors (128 bytes).  Chunks are fixed per
+// row, so rows with the same bytes give bit-identical partials wherever they
+// sit.
 constexpr int64_t kChunkTargetVec = 4752;
 constexpr int64_t kMinItemWaves = 4;
+constexpr int64_t kMaxChunks = 64;
 
 inline void plan_rowpass_chunks(int64_t rows, int64_t nvec, int64_t resident_warps,
                                 int64_t max_items, int* chunks, int64_t* chunk_vec) {
     int64_t c = (nvec + kChunkTargetVec - 1) / kChunkTargetVec;
-    const int64_t want = (kMinItemWaves * resident_warps + rows - 1) / rows;
+    int64_t want = (kMinItemWaves * resident_warps + rows - 1) / rows;
+    if (want > kMaxChunks) want = kMaxChunks;
     if (want > c) c = want;
     const int64_t cmax = nvec >= 64 ? nvec / 64 : 1;
     if (c > cmax) c = cmax;
