@@ -186,3 +186,41 @@ def test_cps_exact_ties_on_a_coarse_grid(dt):
     q = (torch.round(torch.randn((B, G, V), generator=gen, device="cuda") * 4) / 4 * 1.5).to(dt)
     gpu, orc = run_both(q, torch.tensor([0.6, 1.0, 1.0, 0.8, 1.3, 0.7], device="cuda"), 0.9, 12, 7)
     assert compare_cps(gpu, orc, "grid", _qf(q)) <= 1
+
+
+def test_cps_four_warp_rows_full_size_sampled():
+    """The bench's shape (1024 rows: one CTA of 4 warps per row) against the
+    oracle on sampled sequences, and a smaller many-row case in full."""
+    w = synth.workload_shared(B=32, device="cuda", seed=57)
+    g = bd.sdv_cps(w.q_logits, tau=0.8, mmax=15, beam=3, temps=w.temps)
+    torch.cuda.synchronize()
+    gpu = {k: v.cpu().numpy() for k, v in g.items()}
+    import oracle
+    seqs = [0, 13, 31]
+    qh = _host(w.q_logits[seqs])
+    orc = oracle.cps(qh, w.temps[seqs].cpu().numpy(), 0.8, 15, 3, nthreads=oracle.max_threads())
+    sub = {k: v[seqs] for k, v in gpu.items()}
+    assert compare_cps(sub, orc, "full-size", _qf(w.q_logits[seqs])) <= 1
+    del w, g
+    torch.cuda.empty_cache()
+    # 20 x 32 = 640 rows, all compared
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(58)
+    q = (torch.randn((20, 32, 2000), generator=gen, device="cuda") * 2.0).to(torch.bfloat16)
+    gpu, orc = run_both(q, 0.8, 0.8, 15, 3)
+    assert compare_cps(gpu, orc, "640 rows", _qf(q)) <= 1
+
+
+def test_cps_deterministic_and_argmax_path():
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(59)
+    q = torch.randn((7, 9, 3000), generator=gen, device="cuda")
+    a = bd.sdv_cps(q, tau=0.9, mmax=12, beam=5, temperature=0.7)
+    b = bd.sdv_cps(q, tau=0.9, mmax=12, beam=5, temperature=0.7)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    # beam 1 keeps the most likely candidate at every position
+    one = bd.sdv_cps(q, tau=0.9, mmax=12, beam=1, temperature=0.7)
+    torch.cuda.synchronize()
+    assert torch.equal(one["paths"][:, 0].long(), q.argmax(-1))
