@@ -365,6 +365,10 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : 2) cps_prune_kernel(con
     if (lane == 0) a.ncand[row] = n;      // 0 for a row with NaN / +inf / only -inf
 }
 
+// ceil(65536 / n) for n = 1..16: (e * kDivMagic[n]) >> 16 == e / n for e < 256.
+__constant__ unsigned kDivMagic[17] = {0,    65536, 32768, 21846, 16384, 13108, 10923, 9363, 8192,
+                                       7282, 6554,  5958,  5462,  5042,  4682,  4370,  4096};
+
 // An integer with the order of a double (keys here are never NaN and never
 // -0: a sum that cancels to zero rounds to +0).  Integer compares keep the
 // ranking off the (slow) fp64 pipe.
@@ -452,15 +456,17 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     float bscore = 0.0f;
     int blex = 0;
     int ncur = 1;
+    int n_next = nc_s[0];                      // the next position's count, read a step ahead
     for (int j = 0; j < Lc && !empty; ++j) {
-        const int n = eos_cut && j == Lc - 1 ? 1 : nc_s[j];   // EOS is kept alone
+        const int n = eos_cut && j == Lc - 1 ? 1 : n_next;    // EOS is kept alone
+        n_next = j + 1 < G ? nc_s[j + 1] : 0;
         // A parent's expansions come in candidate order (raw logits sorted,
         // ties by id), so only its first W can be among the W best.
         const int nw = n < W ? n : W;
         const int E = ncur * nw;
         const int keep = E < W ? E : W;
         // e / nw as a multiply and shift: exact for e < 256 and nw <= 16
-        const unsigned magic = (65536u + nw - 1) / nw;
+        const unsigned magic = kDivMagic[nw];
         if (E <= 32) {
             // one expansion per lane, ranked with shuffles
             const int e = lane;
@@ -472,32 +478,34 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
             const int lx = __shfl_sync(0xffffffffu, blex, par) * n + r;
             const long long ord = valid ? ordered_i64(key) : LLONG_MIN;
             int rank = 0;
-            for (int src = 0; src < E; ++src) {
-                const long long o2 = __shfl_sync(0xffffffffu, ord, src);
-                const int l2 = __shfl_sync(0xffffffffu, lx, src);
-                rank += (o2 > ord) || (o2 == ord && l2 < lx);
+            // four sources per round: their shuffles go out together
+            for (int s0 = 0; s0 < E; s0 += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int src = s0 + u < E ? s0 + u : lane;     // lane itself adds 0
+                    const long long o2 = __shfl_sync(0xffffffffu, ord, src);
+                    const int l2 = __shfl_sync(0xffffffffu, lx, src);
+                    rank += (o2 > ord) || (o2 == ord && l2 < lx);
+                }
             }
+            // the kept expansions hand their state to beam slot `rank`
             if (valid && rank < keep) {
                 bp_parent[j * W + rank] = static_cast<unsigned char>(par);
                 bp_rank[j * W + rank] = static_cast<unsigned char>(r);
+                n_key[rank] = key;
+                n_score[rank] = sc;
+                n_lx[rank] = lx;
             }
-            // beam t becomes the expansion ranked t
-            int new_lx = 0x7fffffff;
-            for (int t = 0; t < keep; ++t) {
-                const unsigned m = __ballot_sync(0xffffffffu, valid && rank == t);
-                const int src = __ffs(m) - 1;
-                const double k2 = __shfl_sync(0xffffffffu, key, src);
-                const float s2 = __shfl_sync(0xffffffffu, sc, src);
-                const int l2 = __shfl_sync(0xffffffffu, lx, src);
-                if (lane == t) {
-                    bkey = k2;
-                    bscore = s2;
-                    new_lx = l2;
-                }
+            __syncwarp();
+            if (lane < keep) {
+                const int l = n_lx[lane];
+                int pos = 0;
+                for (int t = 0; t < keep; ++t) pos += n_lx[t] < l;
+                bkey = n_key[lane];
+                bscore = n_score[lane];
+                blex = pos;
             }
-            int pos = 0;
-            for (int t = 0; t < keep; ++t) pos += __shfl_sync(0xffffffffu, new_lx, t) < new_lx;
-            blex = pos;
+            __syncwarp();
         } else {
             // more expansions than lanes: through shared memory
             if (lane < ncur) {
