@@ -478,14 +478,25 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
             const int lx = __shfl_sync(0xffffffffu, blex, par) * n + r;
             const long long ord = valid ? ordered_i64(key) : LLONG_MIN;
             int rank = 0;
-            // four sources per round: their shuffles go out together
-            for (int s0 = 0; s0 < E; s0 += 4) {
+            if (E <= 16) {
+                // all sources at once: independent shuffles, no loop-carried wait
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int src = s0 + u < E ? s0 + u : lane;     // lane itself adds 0
+                for (int src0 = 0; src0 < 16; ++src0) {
+                    const int src = src0 < E ? src0 : lane;        // lane itself adds 0
                     const long long o2 = __shfl_sync(0xffffffffu, ord, src);
                     const int l2 = __shfl_sync(0xffffffffu, lx, src);
                     rank += (o2 > ord) || (o2 == ord && l2 < lx);
+                }
+            } else {
+                // four sources per round: their shuffles go out together
+                for (int s0 = 0; s0 < E; s0 += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int src = s0 + u < E ? s0 + u : lane;
+                        const long long o2 = __shfl_sync(0xffffffffu, ord, src);
+                        const int l2 = __shfl_sync(0xffffffffu, lx, src);
+                        rank += (o2 > ord) || (o2 == ord && l2 < lx);
+                    }
                 }
             }
             // the kept expansions hand their state to beam slot `rank`
@@ -500,7 +511,8 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
             if (lane < keep) {
                 const int l = n_lx[lane];
                 int pos = 0;
-                for (int t = 0; t < keep; ++t) pos += n_lx[t] < l;
+#pragma unroll
+                for (int t = 0; t < kCpsMaxBeam; ++t) pos += t < keep && n_lx[t] < l;
                 bkey = n_key[lane];
                 bscore = n_score[lane];
                 blex = pos;
