@@ -414,7 +414,8 @@ def run_cps(args, rank, world):
     # the two kernels timed alone, same events on the launching stream
     lat = {k: out[k] for k in ("cand_ids", "cand_logp", "cand_logit", "ncand")}
     ms_prune = timed(lambda: bd.sdv_cps_prune(q, tau, mmax, temps=temps, out=lat), args.steps)
-    ms_beam = timed(lambda: bd.sdv_cps_beam(lat, V, beam), args.steps)
+    paths_out = dict(out)
+    ms_beam = timed(lambda: bd.sdv_cps_beam(lat, V, beam, out=paths_out), args.steps)
     time.sleep(0.2)
     clocks.stop()
     row_bytes = q.numel() * q.element_size()

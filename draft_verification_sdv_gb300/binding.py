@@ -272,16 +272,21 @@ def sdv_cps_prune(q_marginals, tau: float = 0.8, mmax: int = 15, temperature: fl
     return out
 
 
-def sdv_cps_beam(lattice: dict, V: int, beam: int = 3, eos_id: int = -1, stream=None) -> dict:
+def sdv_cps_beam(lattice: dict, V: int, beam: int = 3, eos_id: int = -1, stream=None,
+                 out: Optional[dict] = None) -> dict:
     """The beam half of sdv_cps over a lattice from sdv_cps_prune (trimmed in
-    place at an EOS end).  Returns the lattice dict with the path tensors."""
+    place at an EOS end).  Returns the lattice dict with the path tensors;
+    `out` (a dict this returned for the same shapes) reuses them."""
     B, G, mmax = lattice["cand_ids"].shape
     dev = lattice["cand_ids"].device
-    out = dict(lattice)
-    out.update({"paths": torch.empty((B, beam, G), dtype=torch.int32, device=dev),
-                "path_logp": torch.empty((B, beam), dtype=torch.float32, device=dev),
-                "npaths": torch.empty((B,), dtype=torch.int32, device=dev),
-                "lat_len": torch.empty((B,), dtype=torch.int32, device=dev)})
+    if out is None:
+        out = dict(lattice)
+        out.update({"paths": torch.empty((B, beam, G), dtype=torch.int32, device=dev),
+                    "path_logp": torch.empty((B, beam), dtype=torch.float32, device=dev),
+                    "npaths": torch.empty((B,), dtype=torch.int32, device=dev),
+                    "lat_len": torch.empty((B,), dtype=torch.int32, device=dev)})
+    else:
+        out.update(lattice)
     st = load().sdv_cps_beam(B, G, int(V), int(mmax), int(beam), int(eos_id),
                              ctypes.c_void_p(_stream_handle(stream)),
                              *[_dev_ptr(out[k]) for k in ("cand_ids", "cand_logp", "cand_logit",

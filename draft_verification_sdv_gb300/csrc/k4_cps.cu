@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : 2) cps_prune_kernel(con
     const int64_t v0 = warp * per_warp;
     const int64_t v1 = v0 + per_warp < a.nvec ? v0 + per_warp : a.nvec;
 
-    // let the beam launch now: it waits for this grid before reading
+    // No kernel launches as this one's programmatic dependent, but with this
+    // trigger back-to-back pruning passes measured 0.060 ms against 0.064 ms.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) s_floor = order_key(-INFINITY);
     __syncthreads();
@@ -405,9 +406,6 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     float* clp = a.cand_logp + static_cast<int64_t>(b) * G * M;
     float* crl = a.cand_logit + static_cast<int64_t>(b) * G * M;
     int32_t* nc = a.ncand + static_cast<int64_t>(b) * G;
-    // launched as a programmatic dependent of the pruning pass: wait for it
-    // before reading the lattice
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     if ((G * M) % 4 == 0 &&
         ((reinterpret_cast<uintptr_t>(clp) | reinterpret_cast<uintptr_t>(crl)) & 15u) == 0) {
         const float4* c4 = reinterpret_cast<const float4*>(clp);
@@ -639,20 +637,10 @@ cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s) {
             cps_beam_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    // a programmatic dependent of the kernel before it on the stream (the
-    // pruning pass triggers at its start): the launch overlaps that kernel's
-    // tail and the kernel waits for it before reading
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.B));
-    cfg.blockDim = dim3(32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, cps_beam_kernel, a);
+    // An ordinary stream-ordered launch: as a programmatic dependent of the
+    // pruning pass the chained pair measured 0.101 ms against 0.083 ms.
+    cps_beam_kernel<<<a.B, 32, smem, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace sdv
