@@ -203,12 +203,13 @@ def test_cps_four_warp_rows_full_size_sampled():
     assert compare_cps(sub, orc, "full-size", _qf(w.q_logits[seqs])) <= 1
     del w, g
     torch.cuda.empty_cache()
-    # 20 x 32 = 640 rows, all compared
+    # 20 x 32 = 640 rows, all compared, bf16 and fp32
     gen = torch.Generator(device="cuda")
     gen.manual_seed(58)
-    q = (torch.randn((20, 32, 2000), generator=gen, device="cuda") * 2.0).to(torch.bfloat16)
-    gpu, orc = run_both(q, 0.8, 0.8, 15, 3)
-    assert compare_cps(gpu, orc, "640 rows", _qf(q)) <= 1
+    q32 = torch.randn((20, 32, 2000), generator=gen, device="cuda") * 2.0
+    for q in (q32.to(torch.bfloat16), q32):
+        gpu, orc = run_both(q, 0.8, 0.8, 15, 3)
+        assert compare_cps(gpu, orc, "640 rows %s" % q.dtype, _qf(q)) <= 1
 
 
 def test_cps_deterministic_and_argmax_path():
