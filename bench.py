@@ -487,12 +487,20 @@ def run_cps(args, rank, world):
     return res
 
 
+ARM_PARTS = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1",
+             "0xd49": "Arm Neoverse-N2"}
+
+
 def cpu_model() -> str:
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu part")):
+                low = line.lower()
+                if low.startswith("model name"):
                     return line.split(":", 1)[1].strip()
+                if low.startswith("cpu part"):
+                    part = line.split(":", 1)[1].strip()
+                    return ARM_PARTS.get(part, "Arm CPU part " + part)
     except OSError:
         pass
     import platform
