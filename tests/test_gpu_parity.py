@@ -377,6 +377,9 @@ def test_shared_marginals_equal_full_layout_bitwise():
 
 
 def test_shared_marginals_large_window_sampled():
+    """The shared-marginal bench configuration at full size: sampled
+    sequences against the oracle, and the shared prefix-row layout (what the
+    bench line uses) bit-identical to reading every prefix row."""
     w = synth.workload_shared(device="cuda")
     gpu = run_gpu(w)
     assert gpu["status"] == bd.SDV_OK
@@ -384,6 +387,9 @@ def test_shared_marginals_large_window_sampled():
     seqs = [3, 30]
     orc = run_oracle(w, seqs)
     assert compare(gpu, orc, seqs, tag="shared large-window") <= 1
+    pre = run_gpu(w, shared_prefix_row=True)
+    for k in ("sel", "accept_len", "next_token", "scores", "lse"):
+        assert np.array_equal(pre[k], gpu[k]), k
     del w
     torch.cuda.empty_cache()
 
