@@ -180,7 +180,7 @@ __device__ __forceinline__ float warp_16th(float x, int lane) {
 
 // One CTA of NW warps per row; each warp streams a contiguous 1/NW of it.
 template <bool BF16, int NW>
-__global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : 2) cps_prune_kernel(const CpsArgs a) {
+__global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_prune_kernel(const CpsArgs a) {
     __shared__ uint64_t s_best[NW][kTopK];
     __shared__ float s_m[NW], s_s[NW];
     // the highest list threshold any warp of the row has reached (order key):
@@ -613,20 +613,24 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
 
 }  // namespace
 
-cudaError_t launch_cps_prune(const CpsArgs& a, bool bf16, cudaStream_t s) {
-    // one CTA per row: 4 warps when the rows fill the GPU (7 CTAs per SM,
-    // 1064 on 152 SMs: one wave up to that many rows), 16 when they are few
+template <bool BF16>
+cudaError_t launch_prune_typed(const CpsArgs& a, cudaStream_t s) {
+    // One CTA per row, with more warps per row the fewer the rows (measured
+    // on 152064-logit rows: 4 warps from 512 rows up, 8 at 256, 16 at 128
+    // and below).  At 4 warps, 7 CTAs fit an SM: 1064 rows in one wave.
     const int64_t rows = static_cast<int64_t>(a.B) * a.G;
     const unsigned grid = static_cast<unsigned>(rows);
-    const bool wide = rows < 600;
-    if (bf16) {
-        if (wide) cps_prune_kernel<true, 16><<<grid, 512, 0, s>>>(a);
-        else cps_prune_kernel<true, 4><<<grid, 128, 0, s>>>(a);
-    } else {
-        if (wide) cps_prune_kernel<false, 16><<<grid, 512, 0, s>>>(a);
-        else cps_prune_kernel<false, 4><<<grid, 128, 0, s>>>(a);
-    }
+    if (rows >= 384)
+        cps_prune_kernel<BF16, 4><<<grid, 128, 0, s>>>(a);
+    else if (rows >= 128)
+        cps_prune_kernel<BF16, 8><<<grid, 256, 0, s>>>(a);
+    else
+        cps_prune_kernel<BF16, 16><<<grid, 512, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_cps_prune(const CpsArgs& a, bool bf16, cudaStream_t s) {
+    return bf16 ? launch_prune_typed<true>(a, s) : launch_prune_typed<false>(a, s);
 }
 
 cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s) {
