@@ -67,6 +67,10 @@ def lib():
                                          ctypes.c_int, vp, vp, vp, ctypes.c_uint64,
                                          ctypes.c_int32] + outs
         L.sdvo_verify_greedy.restype = ctypes.c_int
+        L.sdvo_verify_lens.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                       ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp,
+                                       ctypes.c_uint64, ctypes.c_int32] + outs
+        L.sdvo_verify_lens.restype = ctypes.c_int
         L.sdvo_accept_ratio_greedy.argtypes = [ctypes.c_double]
         L.sdvo_accept_ratio_greedy.restype = ctypes.c_double
         L.sdvo_cps_prune_row.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
@@ -185,17 +189,28 @@ def _outs(out, nthreads):
     return [_ptr(out[k]) for k in _OUT_ORDER] + [int(nthreads)]
 
 
-def verify(p_logits, q_logits, drafts, temps, seed, b0=0, nthreads=1):
+def _lens(lens, B):
+    return None if lens is None else np.ascontiguousarray(
+        np.broadcast_to(np.asarray(lens, dtype=np.int32), (B,)))
+
+
+def verify(p_logits, q_logits, drafts, temps, seed, b0=0, nthreads=1, lens=None):
     """Full step with Philox uniforms keyed by (seed, b0 + b, j).
 
     p_logits [B,K,gamma+1,V] and q_logits [B,K,gamma,V] as uint16 (bf16 words)
-    or float32; drafts [B,K,gamma] int; temps scalar or [B].  Returns a dict
-    of numpy arrays: sel, accept_len, next_token, lse, scores, ratio, band,
-    err, resid_mass.
+    or float32; drafts [B,K,gamma] int; temps scalar or [B]; lens None or the
+    draft length of each sequence [B] (0..gamma; positions past it are not
+    read).  Returns a dict of numpy arrays: sel, accept_len, next_token, lse,
+    scores, ratio, band, err, resid_mass.
     """
     p, q, d, t, dt, (B, K, G, V), out = _verify_common(p_logits, q_logits, drafts, temps)
-    lib().sdvo_verify(B, K, G, V, dt, _ptr(p), _ptr(q), _ptr(d), _ptr(t), int(seed), int(b0),
-                      *_outs(out, nthreads))
+    if lens is None:
+        lib().sdvo_verify(B, K, G, V, dt, _ptr(p), _ptr(q), _ptr(d), _ptr(t), int(seed),
+                          int(b0), *_outs(out, nthreads))
+    else:
+        ln = _lens(lens, B)
+        lib().sdvo_verify_lens(B, K, G, V, dt, 0, _ptr(p), _ptr(q), _ptr(d), _ptr(t), _ptr(ln),
+                               int(seed), int(b0), *_outs(out, nthreads))
     if G == 0:
         out["ratio"] = out["ratio"][..., :0]
     return out
@@ -230,11 +245,16 @@ def _greedy_common(p_logits, drafts, temps):
     return p_logits, drafts, temps, dt, (B, K, G, V), out
 
 
-def verify_greedy(p_logits, drafts, temps, seed, b0=0, nthreads=1):
-    """Greedy acceptance (no drafter rows), Philox uniforms as verify()."""
+def verify_greedy(p_logits, drafts, temps, seed, b0=0, nthreads=1, lens=None):
+    """Greedy acceptance (no drafter rows), Philox uniforms and lens as verify()."""
     p, d, t, dt, (B, K, G, V), out = _greedy_common(p_logits, drafts, temps)
-    lib().sdvo_verify_greedy(B, K, G, V, dt, _ptr(p), _ptr(d), _ptr(t), int(seed), int(b0),
-                             *_outs(out, nthreads))
+    if lens is None:
+        lib().sdvo_verify_greedy(B, K, G, V, dt, _ptr(p), _ptr(d), _ptr(t), int(seed), int(b0),
+                                 *_outs(out, nthreads))
+    else:
+        ln = _lens(lens, B)
+        lib().sdvo_verify_lens(B, K, G, V, dt, 1, _ptr(p), None, _ptr(d), _ptr(t), _ptr(ln),
+                               int(seed), int(b0), *_outs(out, nthreads))
     return out
 
 

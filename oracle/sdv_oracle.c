@@ -214,8 +214,12 @@ static const void* q_row(const void* base, const shape_t* sh, int b, int k, int 
     return (const char*)base + (size_t)idx * elt;
 }
 
+/* One sequence.  Its drafts are Lb tokens long (0 <= Lb <= gamma; the
+ * arrays keep their gamma stride and positions >= Lb are not read): the
+ * scores, the scan and the draw use positions j < Lb, and with every token
+ * accepted the bonus token comes from the verifier row at position Lb. */
 static int verify_one(const shape_t* sh, int b, const void* p_logits,
-                      const void* q_logits, const int32_t* drafts, double T,
+                      const void* q_logits, const int32_t* drafts, double T, int Lb,
                       const double* u, const double* w, int32_t* sel_out,
                       int32_t* len_out, int32_t* tok_out, double* lse_out,
                       double* scores_out, double* ratio_out, int32_t* band_out,
@@ -230,8 +234,9 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
     if (resid_out) *resid_out = NAN;
 
     if (!(T > 0.0) || isinf(T)) err |= SDVO_BAD_TEMP;
+    if (Lb < 0 || Lb > G) err |= SDVO_BAD_DRAFT;
     for (int k = 0; k < K && !err; ++k)
-        for (int j = 0; j < G; ++j) {
+        for (int j = 0; j < Lb; ++j) {
             int32_t x = drafts[((int64_t)b * K + k) * G + j];
             if (x < 0 || (int64_t)x >= V) err |= SDVO_BAD_DRAFT;
         }
@@ -255,16 +260,19 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
 #endif
     for (int i = 0; i < K * nrow; ++i) {
         const int k = i / nrow, r = i % nrow;
-        if (r <= G)
+        if (r <= Lb)
             lse[i] = sdvo_row_lse(p_row(p_logits, sh, b, k, r), dtype, V, T);
-        else if (!greedy)
+        else if (r > G && r - G - 1 < Lb && !greedy)
             lse[i] = sdvo_row_lse(q_row(q_logits, sh, b, k, r - G - 1), dtype, V, T);
         else
-            lse[i] = NAN;                 /* greedy acceptance reads no q row */
+            lse[i] = NAN;     /* a row past the drafts, or a q row under greedy acceptance */
     }
     (void)row_threads;
-    for (int i = 0; i < K * nrow; ++i)
-        if (!isfinite(lse[i]) && !(greedy && i % nrow > G)) err |= SDVO_BAD_ROW;
+    for (int i = 0; i < K * nrow; ++i) {
+        const int r = i % nrow;
+        const int used = r <= Lb || (r > G && r - G - 1 < Lb && !greedy);
+        if (used && !isfinite(lse[i])) err |= SDVO_BAD_ROW;
+    }
     if (lse_out) memcpy(lse_out, lse, sizeof(double) * (size_t)K * nrow);
     if (err) goto done;
 
@@ -272,8 +280,9 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
      * accepted streak of every draft.  lo/hi: the same ratios with p/q moved
      * by a relative 1e-5 (exact cases -- q(x) = 0, p(x) = 0, equal
      * log-probabilities -- stay put); they only feed the boundary band. */
+    for (size_t i = 0; i < nkg * 3; ++i) a[i] = NAN;
     for (int k = 0; k < K; ++k) {
-        for (int j = 0; j < G; ++j) {
+        for (int j = 0; j < Lb; ++j) {
             int32_t x = drafts[((int64_t)b * K + k) * G + j];
             double lp = sdvo_logprob(p_row(p_logits, sh, b, k, j), dtype, x, T, lse[k * nrow + j]);
             if (greedy) {
@@ -298,9 +307,9 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
                 a_hi[k * G + j] = fmin(1.0, r * (1.0 + 1e-5));
             }
         }
-        S[k] = sdvo_streak_score(a + (size_t)k * G, G);
-        S_lo[k] = sdvo_streak_score(a_lo + (size_t)k * G, G);
-        S_hi[k] = sdvo_streak_score(a_hi + (size_t)k * G, G);
+        S[k] = sdvo_streak_score(a + (size_t)k * G, Lb);
+        S_lo[k] = sdvo_streak_score(a_lo + (size_t)k * G, Lb);
+        S_hi[k] = sdvo_streak_score(a_hi + (size_t)k * G, Lb);
     }
     if (scores_out) memcpy(scores_out, S, sizeof(double) * (size_t)K);
     if (ratio_out && G > 0) memcpy(ratio_out, a, sizeof(double) * (size_t)K * G);
@@ -317,17 +326,17 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
 
     /* Left-to-right acceptance of the selected draft. */
     const double* as = a + (size_t)sel * G;
-    int L = sdvo_accept_length(as, u, G);
-    for (int j = 0; j < G && j <= L; ++j)
+    int L = sdvo_accept_length(as, u, Lb);
+    for (int j = 0; j < Lb && j <= L; ++j)
         if (fabs(u[j] - as[j]) <= 1e-5 * as[j]) band |= SDVO_BAND_ACCEPT;
 
     /* Replacement at the first rejection (residual max(0, p - q)), or the
-     * bonus token from p at position G when every draft token was accepted. */
+     * bonus token from p at position Lb when every draft token was accepted. */
     int64_t tok;
     double R = 0.0, t = 0.0, c_prev = 0.0, c_v = 0.0;
     const void* prow = p_row(p_logits, sh, b, sel, L);
     double lse_p = lse[sel * nrow + L];
-    if (L < G && greedy) {
+    if (L < Lb && greedy) {
         /* greedy: draw from p with the rejected token zeroed out */
         const int32_t xr = drafts[((int64_t)b * K + sel) * G + L];
         for (int64_t v = 0; v < V; ++v)
@@ -340,7 +349,7 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
                 r[v] = exp(sdvo_logit(prow, dtype, v) / T - lse_p);
             tok = sdvo_inverse_cdf(r, V, w[L], &R, &t, &c_prev, &c_v);
         }
-    } else if (L < G) {
+    } else if (L < Lb) {
         const void* qrow = q_row(q_logits, sh, b, sel, L);
         double lse_q = lse[sel * nrow + G + 1 + L];
         for (int64_t v = 0; v < V; ++v) {
@@ -362,7 +371,7 @@ static int verify_one(const shape_t* sh, int b, const void* p_logits,
     } else {
         for (int64_t v = 0; v < V; ++v)
             r[v] = exp(sdvo_logit(prow, dtype, v) / T - lse_p);
-        tok = sdvo_inverse_cdf(r, V, w[G], &R, &t, &c_prev, &c_v);
+        tok = sdvo_inverse_cdf(r, V, w[Lb], &R, &t, &c_prev, &c_v);
     }
     if (fabs(t - c_v) <= 1e-5 * R || fabs(t - c_prev) <= 1e-5 * R) band |= SDVO_BAND_CDF;
 
@@ -378,7 +387,7 @@ done:
 
 static int run_batch(int B, int K, int gamma, int64_t V, int dtype, int greedy,
                      const void* p_logits, const void* q_logits,
-                     const int32_t* drafts, const double* temps,
+                     const int32_t* drafts, const double* temps, const int32_t* lens,
                      const double* u_in, const double* w_in, int use_philox,
                      uint64_t seed, int32_t b0,
                      int32_t* sel, int32_t* accept_len, int32_t* next_token,
@@ -410,7 +419,8 @@ static int run_batch(int B, int K, int gamma, int64_t V, int dtype, int greedy,
                 w[j] = w_in[(int64_t)b * (gamma + 1) + j];
             }
         }
-        int e = verify_one(&sh, b, p_logits, q_logits, drafts, temps[b], u, w,
+        int e = verify_one(&sh, b, p_logits, q_logits, drafts, temps[b],
+                           lens ? lens[b] : gamma, u, w,
                            &sel[b], &accept_len[b], &next_token[b],
                            lse ? lse + (int64_t)b * K * nrow : NULL,
                            scores ? scores + (int64_t)b * K : NULL,
@@ -434,7 +444,7 @@ int sdvo_verify_uniforms(int B, int K, int gamma, int64_t V, int dtype,
                          int32_t* band, int32_t* err, double* resid_mass,
                          int nthreads)
 {
-    return run_batch(B, K, gamma, V, dtype, 0, p_logits, q_logits, drafts, temps, u, w, 0, 0, 0,
+    return run_batch(B, K, gamma, V, dtype, 0, p_logits, q_logits, drafts, temps, NULL, u, w, 0, 0, 0,
                      sel, accept_len, next_token, lse, scores, ratio, band, err, resid_mass,
                      nthreads);
 }
@@ -447,7 +457,7 @@ int sdvo_verify_greedy_uniforms(int B, int K, int gamma, int64_t V, int dtype,
                                 int32_t* band, int32_t* err, double* resid_mass,
                                 int nthreads)
 {
-    return run_batch(B, K, gamma, V, dtype, 1, p_logits, NULL, drafts, temps, u, w, 0, 0, 0,
+    return run_batch(B, K, gamma, V, dtype, 1, p_logits, NULL, drafts, temps, NULL, u, w, 0, 0, 0,
                      sel, accept_len, next_token, lse, scores, ratio, band, err, resid_mass,
                      nthreads);
 }
@@ -461,7 +471,7 @@ int sdvo_verify(int B, int K, int gamma, int64_t V, int dtype,
                 int32_t* band, int32_t* err, double* resid_mass,
                 int nthreads)
 {
-    return run_batch(B, K, gamma, V, dtype, 0, p_logits, q_logits, drafts, temps, NULL, NULL, 1,
+    return run_batch(B, K, gamma, V, dtype, 0, p_logits, q_logits, drafts, temps, NULL, NULL, NULL, 1,
                      seed, b0, sel, accept_len, next_token, lse, scores, ratio, band, err,
                      resid_mass, nthreads);
 }
@@ -474,9 +484,23 @@ int sdvo_verify_greedy(int B, int K, int gamma, int64_t V, int dtype,
                        int32_t* band, int32_t* err, double* resid_mass,
                        int nthreads)
 {
-    return run_batch(B, K, gamma, V, dtype, 1, p_logits, NULL, drafts, temps, NULL, NULL, 1,
+    return run_batch(B, K, gamma, V, dtype, 1, p_logits, NULL, drafts, temps, NULL, NULL, NULL, 1,
                      seed, b0, sel, accept_len, next_token, lse, scores, ratio, band, err,
                      resid_mass, nthreads);
+}
+
+int sdvo_verify_lens(int B, int K, int gamma, int64_t V, int dtype, int greedy,
+                     const void* p_logits, const void* q_logits,
+                     const int32_t* drafts, const double* temps, const int32_t* lens,
+                     uint64_t seed, int32_t b0,
+                     int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                     double* lse, double* scores, double* ratio,
+                     int32_t* band, int32_t* err, double* resid_mass,
+                     int nthreads)
+{
+    return run_batch(B, K, gamma, V, dtype, greedy ? 1 : 0, p_logits, greedy ? NULL : q_logits,
+                     drafts, temps, lens, NULL, NULL, 1, seed, b0, sel, accept_len, next_token,
+                     lse, scores, ratio, band, err, resid_mass, nthreads);
 }
 
 int sdvo_max_threads(void)

@@ -154,6 +154,22 @@ int sdvo_verify_greedy(int B, int K, int gamma, int64_t V, int dtype,
                        int32_t* band, int32_t* err, double* resid_mass,
                        int nthreads);
 
+/* Either rule (greedy = 0: the standard rule, 1: greedy acceptance, q_logits
+ * unused) with a draft length per sequence: lens[b] in [0, gamma] (the arrays
+ * keep their gamma stride; positions at or past lens[b] are not read).  The
+ * scores and the scan run over j < lens[b]; with every token accepted the
+ * bonus token comes from p at position lens[b], drawn with the uniform
+ * w_{lens[b]}.  lse[] entries of rows not read are NaN; a length outside
+ * [0, gamma] is a draft error. */
+int sdvo_verify_lens(int B, int K, int gamma, int64_t V, int dtype, int greedy,
+                     const void* p_logits, const void* q_logits,
+                     const int32_t* drafts, const double* temps, const int32_t* lens,
+                     uint64_t seed, int32_t b0,
+                     int32_t* sel, int32_t* accept_len, int32_t* next_token,
+                     double* lse, double* scores, double* ratio,
+                     int32_t* band, int32_t* err, double* resid_mass,
+                     int nthreads);
+
 /* ------------------------------------------------------------------------ */
 /* Causal-consistency path search ("DiffuSpec: Unlocking Diffusion Language   */
 /* Models for Speculative Decoding", section 4.2; settings of section 5.3).   */

@@ -59,6 +59,13 @@ MUTANTS = [
     ("cps_ties_lexicographic_last", "        if (ra[i] < rb[i]) return 1;\n        if (ra[i] > rb[i]) return 0;",
      "        if (ra[i] > rb[i]) return 1;\n        if (ra[i] < rb[i]) return 0;", 1),
     ("cps_keeps_zero_probability", "        if (e[n].z == -INFINITY) break;", "", 1),
+    ("len_scan_one_short", "int L = sdvo_accept_length(as, u, Lb);",
+     "int L = sdvo_accept_length(as, u, Lb > 0 ? Lb - 1 : 0);", 1),
+    ("len_bonus_uniform_of_gamma", "tok = sdvo_inverse_cdf(r, V, w[Lb], &R, &t, &c_prev, &c_v);",
+     "tok = sdvo_inverse_cdf(r, V, w[G], &R, &t, &c_prev, &c_v);", 1),
+    ("len_streak_over_gamma", "S[k] = sdvo_streak_score(a + (size_t)k * G, Lb);",
+     "S[k] = sdvo_streak_score(a + (size_t)k * G, G);", 1),
+    ("len_reads_past_length", "        if (r <= Lb)\n", "        if (r <= G)\n", 1),
     ("adl_pace_strict", "int keeps_pace = sa >= sg;", "int keeps_pace = sa > sg;", 1),
     ("adl_ignores_saturation", "int fills = sg >= sk;", "int fills = 1;", 1),
     ("adl_no_clamp_of_generated", "        if (g > kb) g = kb;", "", 1),
@@ -86,6 +93,7 @@ def test_pins_catch_mutant(name, old, new, count, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_greedy_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_cps_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_adl_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_adl_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_len_pins.py")],
                        env=env, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-1500:])
