@@ -36,6 +36,7 @@ SIGNATURES = {
     "sdv_create_ex": (_I, [ctypes.POINTER(_VP), _I, _I, _I, _I, _I, _VP, ctypes.c_uint]),
     "sdv_verify": (_I, [_VP, _VP, _VP, _VP, _F, _U64, _VP, _VP, _VP]),
     "sdv_verify_ex": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP, _VP]),
+    "sdv_verify_len": (_I, [_VP, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP, _VP]),
     "sdv_verify_host": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
     "sdv_sync": (_I, [_VP]),
     "sdv_last_error": (ctypes.c_char_p, [_VP]),
@@ -150,6 +151,20 @@ def sdv_verify_ex(ctx, p_logits, q_logits, drafts, temperature, temperature_per_
         ctx, _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
         _dev_ptr(drafts, torch.int32, "drafts"), float(temperature),
         _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
+        _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
+        _dev_ptr(out_next_token, torch.int32, "out_next_token"),
+        _dev_ptr(out_scores, torch.float32, "out_scores"),
+        _dev_ptr(out_lse, torch.float32, "out_lse"))
+
+
+def sdv_verify_len(ctx, p_logits, q_logits, drafts, draft_len, temperature, temperature_per_seq,
+                   seed, out_sel, out_accept_len, out_next_token, out_scores=None,
+                   out_lse=None) -> int:
+    return load().sdv_verify_len(
+        ctx, _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
+        _dev_ptr(drafts, torch.int32, "drafts"), _dev_ptr(draft_len, torch.int32, "draft_len"),
+        float(temperature), _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
         int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
         _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
         _dev_ptr(out_next_token, torch.int32, "out_next_token"),
@@ -361,7 +376,9 @@ class Verifier:
 
     def __call__(self, p_logits, q_logits, drafts, temperature: float = 1.0, seed: int = 0,
                  temps: Optional[torch.Tensor] = None, scores: bool = False, lse: bool = False,
-                 out: Optional[dict] = None) -> dict:
+                 out: Optional[dict] = None, draft_len: Optional[torch.Tensor] = None) -> dict:
+        """One verification step; `draft_len` (int32 [B] on the device) gives
+        each sequence's draft length (sdv_verify_len), else all are gamma."""
         B, K, G, V = self.B, self.K, self.gamma, self.V
         q_shape = (B, G, V) if self.shared_q else (B, K, G, V)
         if tuple(p_logits.shape) != (B, K, G + 1, V):
@@ -384,9 +401,14 @@ class Verifier:
             if lse:
                 out["lse"] = torch.empty((B, K, G + 1 if self.greedy else 2 * G + 1),
                                          dtype=torch.float32, device=dev)
-        st = sdv_verify_ex(self.ctx, p_logits, q_logits, drafts, temperature, temps, seed,
-                           out["sel"], out["accept_len"], out["next_token"], out.get("scores"),
-                           out.get("lse"))
+        if draft_len is None:
+            st = sdv_verify_ex(self.ctx, p_logits, q_logits, drafts, temperature, temps, seed,
+                               out["sel"], out["accept_len"], out["next_token"], out.get("scores"),
+                               out.get("lse"))
+        else:
+            st = sdv_verify_len(self.ctx, p_logits, q_logits, drafts, draft_len, temperature, temps,
+                                seed, out["sel"], out["accept_len"], out["next_token"],
+                                out.get("scores"), out.get("lse"))
         if st != SDV_OK:
             raise SdvError(st, sdv_last_error(self.ctx))
         return out

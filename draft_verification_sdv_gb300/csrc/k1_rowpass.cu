@@ -49,15 +49,22 @@ __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassA
         const int64_t v1 = min(v0 + a.chunk_vec, a.nvec);
         const uint4* rowv;
         int64_t b;
+        // a sequence with shorter drafts needs no row past its length
+        auto draft_len = [&](int64_t seq) {
+            const int L = a.lens ? __ldg(a.lens + seq) : a.G;
+            return L < 0 || L > a.G ? a.G : L;            // out of range: K2 reports it
+        };
         if (row < a.rows_p) {
             rowv = static_cast<const uint4*>(a.p) + row * a.nvec;
             b = row / rows_per_seq_p;
             // a prefix row (j = 0) of draft k > 0 that the shared one replaces
             const int64_t r = row - b * rows_per_seq_p;
             if ((a.flags & kFlagSharedPrefixRow) && r > a.G && r % (a.G + 1) == 0) return;
+            if (a.lens && r % (a.G + 1) > draft_len(b)) return;
         } else {
             rowv = static_cast<const uint4*>(a.q) + (row - a.rows_p) * a.nvec;
             b = (row - a.rows_p) / rows_per_seq_q;
+            if (a.lens && ((row - a.rows_p) - b * rows_per_seq_q) % a.G >= draft_len(b)) return;
         }
         const float T = a.temps ? __ldg(a.temps + b) : a.temperature;
         const float c = kLog2e / T;

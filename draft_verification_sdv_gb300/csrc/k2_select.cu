@@ -84,9 +84,13 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     const bool greedy = (a.flags & kFlagGreedy) != 0;   // no drafter rows
     const float T = a.temps ? a.temps[b] : a.temperature;
     const float c = kLog2e / T;
+    // this sequence's draft length: positions j >= Lg are not read
+    const int len_in = a.lens ? a.lens[b] : G;
+    const bool len_ok = len_in >= 0 && len_in <= G;
+    const int Lg = len_ok ? len_in : 0;
     if (tid == 0) {
-        s_bad = (isfinite(T) && T > 0.0f) ? 0u : kStatusBadTemp;
-        s_len = G;
+        s_bad = (isfinite(T) && T > 0.0f ? 0u : kStatusBadTemp) | (len_ok ? 0u : kStatusBadDraft);
+        s_len = Lg;
     }
     __syncthreads();
 
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     // waiting for the row pass to finish.
     int32_t x0 = 0;
     float lp0 = 0.0f, lq0 = 0.0f;
-    if (tid < KG) {
+    if (tid < KG && tid - (tid / G) * G < Lg) {
         const int k = tid / G, j = tid - (tid / G) * G;
         x0 = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
         if (x0 >= 0 && x0 < a.V) {
@@ -114,6 +118,14 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     // Acceptance ratio at every drafted token of every draft.
     for (int idx = tid; idx < KG; idx += kSelectThreads) {
         const int k = idx / G, j = idx - (idx / G) * G;
+        if (j >= Lg) {                                    // past this sequence's drafts
+            if (a.out_lse) {
+                float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
+                if (j > Lg) lse[j] = NAN;                 // j == Lg: the bonus row below
+                if (!greedy) lse[G + 1 + j] = NAN;
+            }
+            continue;
+        }
         const int64_t rp = p_row_index(a.flags, b, k, j, K, G);
         const int64_t rq = greedy ? 0 : q_row_index(a.flags, b, k, j, K, G);
         int32_t x = x0;
@@ -158,14 +170,19 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         }
         ratio[idx] = r;
     }
-    // The bonus rows (j = G): validity and LSE, on the last threads (idle
-    // above when K * G leaves them free).
+    // The bonus rows (j = Lg, right after the last draft token; G for full
+    // drafts): validity and LSE, on the last threads (idle above when K * G
+    // leaves them free).
     for (int k = kSelectThreads - 1 - tid; k < K; k += kSelectThreads) {
-        const int64_t rp = seq_p + static_cast<int64_t>(k) * (G + 1) + G;
+        const int64_t rp = p_row_index(a.flags, b, k, Lg, K, G);
         float mp, sp;
         merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);
-        pstat[k * (G + 1) + G] = make_float2(mp, sp);
-        if (a.out_lse) a.out_lse[(static_cast<int64_t>(b) * K + k) * nrow + G] = row_lse(mp, sp, c);
+        pstat[k * (G + 1) + Lg] = make_float2(mp, sp);
+        if (a.out_lse) {
+            float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
+            lse[Lg] = row_lse(mp, sp, c);
+            if (Lg < G) lse[G] = NAN;
+        }
         if (!row_valid(mp, sp)) atomicOr(&s_bad, kStatusBadRow);
     }
     __syncthreads();
@@ -188,7 +205,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     // score well inside the selection tolerance).
     for (int k = tid; k < K; k += kSelectThreads) {
         float prefix = 1.0f, sc = 0.0f;
-        for (int j = 0; j < G; ++j) {
+        for (int j = 0; j < Lg; ++j) {
             prefix *= ratio[k * G + j];
             sc += prefix;
         }
@@ -208,7 +225,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     const int sel = s_sel;
 
     // Left-to-right acceptance of the selected draft: the first rejected j.
-    for (int j = tid; j < G; j += kSelectThreads) {
+    for (int j = tid; j < Lg; j += kSelectThreads) {
         const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u, 0u),
                                       a.seed_lo, a.seed_hi);
         const float u = uniform24(r.x);
@@ -231,18 +248,18 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const float2 ps = pstat[sel * (G + 1) + L];
         t.mp = ps.x;
         t.inv_sp = 1.0f / ps.y;
-        if (L < G && greedy) {
+        if (L < Lg && greedy) {
             t.mode = 3;                                   // p with the rejected token zeroed
             t.zero_id = a.drafts[seq_d + static_cast<int64_t>(sel) * G + L];
             t.row_q = -1;
-        } else if (L < G) {
+        } else if (L < Lg) {
             t.mode = 1;                                   // residual max(0, p - q)
             t.row_q = q_row_index(a.flags, b, sel, L, K, G);
             const float2 qs = qstat[sel * G + L];
             t.mq = qs.x;
             t.inv_sq = 1.0f / qs.y;
         } else {
-            t.mode = 2;                                   // bonus token from p_gamma
+            t.mode = 2;                                   // bonus token from p at Lg
             t.row_q = -1;
         }
         a.tasks[b] = t;

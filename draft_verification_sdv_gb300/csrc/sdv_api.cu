@@ -186,11 +186,13 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
     return SDV_OK;
 }
 
-sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
-                         const int32_t* drafts, float temperature,
-                         const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
-                         int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
-                         float* out_lse) {
+namespace {
+
+sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                       const int32_t* drafts, const int32_t* draft_len, float temperature,
+                       const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
+                       int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
+                       float* out_lse) {
     if (!ctx) return SDV_ERR_ARG;
     ctx->err[0] = 0;
     const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
@@ -213,6 +215,8 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
             return fail(ctx, SDV_ERR_ARG, "argument is not a device pointer");
     if (out_lse && !is_device_ptr(out_lse))
         return fail(ctx, SDV_ERR_ARG, "out_lse is not a device pointer");
+    if (draft_len && ((reinterpret_cast<uintptr_t>(draft_len) & 3u) || !is_device_ptr(draft_len)))
+        return fail(ctx, SDV_ERR_ARG, "draft_len must be a 4-byte aligned device pointer");
 
     RowPassArgs ra;
     ra.p = p_logits;
@@ -229,6 +233,7 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     ra.nvec = ctx->nvec;
     ra.chunk_vec = ctx->chunk_vec;
     ra.items = ctx->items;
+    ra.lens = draft_len;
     cudaEvent_t* ev = nullptr;
     if (ctx->prof_on && ctx->prof_n < kMaxProfSteps) {
         const size_t need = static_cast<size_t>(ctx->prof_n + 1) * 4;
@@ -268,6 +273,7 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     sa.out_lse = out_lse;
     sa.tasks = ctx->tasks;
     sa.status = ctx->status;
+    sa.lens = draft_len;
     e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "select launch");
     if (ev) cudaEventRecord(ev[2], ctx->stream);
@@ -285,6 +291,27 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     if (e != cudaSuccess) return cuda_fail(ctx, e, "sample launch");
     if (ev) cudaEventRecord(ev[3], ctx->stream);
     return SDV_OK;
+}
+
+}  // namespace
+
+sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                         const int32_t* drafts, float temperature,
+                         const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
+                         int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
+                         float* out_lse) {
+    return verify_impl(ctx, p_logits, q_logits, drafts, nullptr, temperature, temperature_per_seq,
+                       seed, out_sel, out_accept_len, out_next_token, out_scores, out_lse);
+}
+
+sdv_status sdv_verify_len(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                          const int32_t* drafts, const int32_t* draft_len, float temperature,
+                          const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
+                          int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
+                          float* out_lse) {
+    if (!draft_len) return ctx ? fail(ctx, SDV_ERR_ARG, "draft_len is null") : SDV_ERR_ARG;
+    return verify_impl(ctx, p_logits, q_logits, drafts, draft_len, temperature, temperature_per_seq,
+                       seed, out_sel, out_accept_len, out_next_token, out_scores, out_lse);
 }
 
 sdv_status sdv_verify(sdv_ctx* ctx, const void* p_logits, const void* q_logits,

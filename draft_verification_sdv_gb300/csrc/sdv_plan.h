@@ -119,6 +119,7 @@ struct RowPassArgs {
     int64_t nvec;           // vectors per row
     int64_t chunk_vec;      // vectors per chunk
     int64_t items;          // rows_total * chunks
+    const int32_t* lens = nullptr;   // [B] draft length per sequence (rows past it are skipped)
 };
 
 // Select / scan (K2): one CTA per sequence.
@@ -140,6 +141,7 @@ struct SelectArgs {
     float* out_lse;         // [B][K][2G+1] or nullptr
     SeqTask* tasks;
     unsigned* status;
+    const int32_t* lens = nullptr;   // [B] draft length per sequence, or nullptr (= G)
 };
 
 // Residual / bonus sampling (K3): a cluster of `cluster` CTAs per sequence,

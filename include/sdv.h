@@ -156,6 +156,28 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
                          float* out_lse);
 
 /*
+ * As sdv_verify_ex, with a draft length per sequence ("DiffuSpec: Unlocking
+ * Diffusion Language Models for Speculative Decoding", sections 4.2-4.3: the
+ * draft length adapts per step, and a path ends at its first EOS).
+ *   draft_len  device int32 [B], 0 <= draft_len[b] <= gamma (required)
+ * The arrays keep their gamma stride; for sequence b only the drafts at
+ * positions j < draft_len[b] count, so the caller may leave the rest as
+ * they are.  The streak scores and the acceptance scan run over those
+ * positions, and with all of them accepted the bonus token comes from the
+ * verifier row at position draft_len[b], drawn with that position's uniform.
+ * Rows past a sequence's length are not read: the p rows j > draft_len[b] and
+ * the q rows j >= draft_len[b].  Their out_lse entries are NaN.  The result
+ * for b equals that of sdv_verify_ex on the drafts cut to draft_len[b].  A
+ * length outside [0, gamma] is a data error for that sequence: its outputs
+ * are -1, and sdv_sync reports SDV_ERR_DEVICE_DATA.
+ */
+sdv_status sdv_verify_len(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                          const int32_t* drafts, const int32_t* draft_len, float temperature,
+                          const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
+                          int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
+                          float* out_lse);
+
+/*
  * End-to-end variant for callers whose data lives in HOST memory: copies the
  * inputs to device buffers owned by the context (allocated on the first call,
  * the size of one batch's inputs), runs sdv_verify_ex, copies the three
