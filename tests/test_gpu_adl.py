@@ -70,9 +70,10 @@ def test_decode_step_chain_search_verify_control():
         w.q_logits[:, :, 17] = -30.0
         w.q_logits[1, 5, 17] = 30.0                  # sequence 1 ends at position 5
         cps = bd.sdv_cps(w.q_logits, tau=0.8, mmax=15, beam=K, eos_id=17)
-        # the caller pads the drafts past EOS with EOS itself
-        drafts = torch.where(cps["paths"] < 0, torch.full_like(cps["paths"], 17), cps["paths"])
-        out = v(w.p_logits, w.q_logits, drafts, temperature=1.0, seed=it)
+        # each sequence is verified at its lattice length; past it the drafts
+        # are not read
+        drafts = torch.where(cps["paths"] < 0, torch.zeros_like(cps["paths"]), cps["paths"])
+        out = v(w.p_logits, w.q_logits, drafts, temperature=1.0, seed=it, draft_len=cps["lat_len"])
         ks.append(ctl.step(cps["lat_len"], out["accept_len"]).clone())
         gens.append(cps["lat_len"].clone())
         accs.append(out["accept_len"].clone())
@@ -80,6 +81,7 @@ def test_decode_step_chain_search_verify_control():
     v.sync()
     assert all(int(g[1]) == 6 for g in gens) and all((g[[0, 2, 3, 4, 5]] == G).all() for g in gens)
     for g, a, k in zip(gens, accs, ks):
+        assert (a <= g).all()                     # nothing past the EOS is accepted
         k_ref = oracle.adl_step(k_ref, g.cpu().numpy(), a.cpu().numpy(), st, W=2, kmin=2, kmax=G,
                                 up=2, down=1)
         assert np.array_equal(k.cpu().numpy(), k_ref)
