@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--cps", action="store_true",
                     help="time the causal-consistency path search on the large-window marginals")
+    ap.add_argument("--decode-step", action="store_true",
+                    help="time one whole decode step over one pass's marginals: path search, "
+                         "verification of the paths at their lattice lengths, draft-length update")
     ap.add_argument("--greedy", action="store_true",
                     help="greedy acceptance: verifier rows only, no drafter rows")
     ap.add_argument("--shared-q", action="store_true",
@@ -491,6 +494,85 @@ ARM_PARTS = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "A
              "0xd49": "Arm Neoverse-N2"}
 
 
+def run_decode_step(args, rank, world):
+    """One decode step of a diffusion drafter's pass, end to end on the GPU:
+    the path search over the marginals q [B, gamma, V] (beam 3, 15
+    candidates, mass 0.8, EOS cut), verification of the beam's K = 3 paths at
+    their lattice lengths (shared marginals, shared prefix row), and the
+    draft-length update from the lattice and accepted lengths.  Large-window
+    shape: B 32, gamma 32, V 152064 bf16, per-sequence temperatures."""
+    from draft_verification_sdv_gb300 import binding as bd
+    bd.load(build=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, K, G, V = args.batch or 32, 3, 32, synth.QWEN_VOCAB
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10_055 + 1000 * rank)
+    sj = 0.3 + 1.7 * torch.arange(G, dtype=torch.float32) / (G - 1)
+    temps = torch.where(torch.rand((B,), generator=g) < 0.5, torch.tensor(0.6), torch.tensor(1.0))
+    w = synth.generate_shared(B, K, G, V, q_sigma=sj.expand(B, G).clone(), temps=temps,
+                              seed=55 + 1000 * rank, device=dev)
+    eos = 151643                                   # the Qwen2.5 end-of-text id
+    v = bd.Verifier(B, K, G, V, w.dtype, shared_q=True, shared_prefix_row=True)
+    ctl = bd.DraftLengthController(B, G, window=2, kmin=4, kmax=G, up=2, down=1, device=dev)
+    cps = bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps)
+    out = None
+
+    def step(i):
+        nonlocal out
+        bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, out=cps)
+        out = v(w.p_logits, w.q_logits, cps["paths"], seed=i, temps=w.temps, out=out,
+                draft_len=cps["lat_len"])
+        ctl.step(cps["lat_len"], out["accept_len"])
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    v.sync()
+    barrier(world)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.25)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    time.sleep(0.2)
+    clocks.stop()
+    v.sync()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    lat = cps["lat_len"].cpu().numpy()
+    acc = out["accept_len"].cpu().numpy()
+    elt = 2
+    rows = B * G + sum(1 + K * int(L) for L in lat) + sum(int(L) for L in lat)   # q, p, q
+    rows += sum(2 if int(a) < int(L) else 1 for a, L in zip(acc, lat))         # the draw
+    gbs = rows * V * elt / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    committed = int(sum(int(a) + 1 for a in acc))
+    v.close()
+    return {"metric": "decode steps per second (path search + verification + draft-length "
+                      "update), sequences x steps / s",
+            "value": world * B / (ms * 1e-3), "unit": "sequence-steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "input_dtype": "bf16", "data": "synthetic marginals and verifier rows (seeded)",
+            "config": {"workload": "large-window marginals B%d K%d gamma%d V%d bf16" % (B, K, G, V),
+                       "beam": K, "mmax": 15, "tau": 0.8, "eos_id": eos,
+                       "lattice_len_mean": float(lat.mean()),
+                       "l2": "inputs %.2f GB > L2 (126 MB): no flush"
+                             % ((w.p_logits.numel() + w.q_logits.numel()) * elt / 1e9)},
+            "committed_tokens_per_s": world * committed / (ms * 1e-3),
+            "hbm": {"step_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak": peak,
+                    "peak_kind": kind, "rows_per_step": rows},
+            "gpu_launches": 6 * args.steps,
+            "clocks": clocks.summary(t0, t1)}
+
+
 def cpu_model() -> str:
     try:
         with open("/proc/cpuinfo") as f:
@@ -593,7 +675,12 @@ def main():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
         return 1
     rank, world, local = dist_setup()
-    res = run_cps(args, rank, world) if args.cps else run_sdv(args, rank, world, local)
+    if args.decode_step:
+        res = run_decode_step(args, rank, world)
+    elif args.cps:
+        res = run_cps(args, rank, world)
+    else:
+        res = run_sdv(args, rank, world, local)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
