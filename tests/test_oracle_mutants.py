@@ -34,7 +34,7 @@ MUTANTS = [
     ("cdf_non_strict", "if (c > t) {", "if (c >= t) {", 1),
     ("residual_transposed", "double d = pv - qv;", "double d = qv - pv;", 1),
     ("residual_unclipped", "r[v] = d > 0.0 ? d : 0.0;", "r[v] = d;", 1),
-    ("bonus_wrong_uniform", "tok = sdvo_inverse_cdf(r, V, w[G], &R, &t, &c_prev, &c_v);",
+    ("bonus_wrong_uniform", "tok = sdvo_inverse_cdf(r, V, w[Lb], &R, &t, &c_prev, &c_v);",
      "tok = sdvo_inverse_cdf(r, V, w[0], &R, &t, &c_prev, &c_v);", 1),
     ("q_lse_from_p_row", "lse[i] = sdvo_row_lse(q_row(q_logits, sh, b, k, r - G - 1), dtype, V, T);",
      "lse[i] = sdvo_row_lse(p_row(p_logits, sh, b, k, r - G - 1), dtype, V, T);", 1),
