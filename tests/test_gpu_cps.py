@@ -225,3 +225,16 @@ def test_cps_deterministic_and_argmax_path():
     one = bd.sdv_cps(q, tau=0.9, mmax=12, beam=1, temperature=0.7)
     torch.cuda.synchronize()
     assert torch.equal(one["paths"][:, 0].long(), q.argmax(-1))
+
+
+def test_cps_largest_lattice():
+    """gamma 1024 positions, 16 candidates, beam 16 (the limits: 190 KB of
+    shared memory for the beam, 256 expansions a step) against the oracle."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(60)
+    q = (torch.randn((2, 1024, 256), generator=gen, device="cuda") * 0.7).to(torch.bfloat16)
+    gpu, orc = run_both(q, 1.0, 0.999, 16, 16)
+    assert compare_cps(gpu, orc, "g1024 w16", _qf(q)) <= 1
+    assert (gpu["npaths"] == 16).all()
+    with pytest.raises(bd.SdvError):
+        bd.sdv_cps(torch.zeros((1, 1025, 64), dtype=torch.bfloat16, device="cuda"))

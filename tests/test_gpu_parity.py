@@ -472,3 +472,15 @@ def test_shared_prefix_row_with_full_q_layout():
 def test_greedy_rejects_shared_q_combination():
     with pytest.raises(bd.SdvError):
         bd.Verifier(2, 2, 2, 64, shared_q=True, greedy=True)
+
+
+def test_largest_select_shape_and_the_limit_beyond_it():
+    """K * gamma near the select kernel's shared-memory limit (64 drafts of
+    128 tokens: 164 KB of row statistics per sequence) against the oracle;
+    one size up is refused at create time."""
+    w = _small(2, 64, 128, 64, dtype=torch.float32, T=1.0, seed=41, zipf=False, p_sigma=1.5)
+    gpu, orc = run_gpu(w, seed=2), run_oracle(w, seed=2)
+    assert gpu["status"] == bd.SDV_OK
+    assert compare(gpu, orc, tag="K64 g128") <= 1
+    with pytest.raises(bd.SdvError):
+        bd.Verifier(1, 128, 128, 64, torch.float32)
