@@ -378,6 +378,32 @@ __device__ __forceinline__ long long ordered_i64(double d) {
     return bits ^ ((bits >> 63) & 0x7fffffffffffffffLL);
 }
 
+// One lattice position as a lane of the beam sees it: the candidate count
+// n (1 at an EOS end), the expanded count nw = min(n, W), the divide
+// constant for e / nw, and expansion e = lane's parent beam, candidate rank
+// and the candidate's raw logit and log-probability.
+struct BeamPos {
+    int n, nw, par, r;
+    unsigned magic;
+    float rl, lp;
+};
+
+__device__ __forceinline__ BeamPos beam_position(const int* nc_s, const float* rl_s, const float* clp_s,
+                                                 int j, int Lc, bool eos_cut, int W, int M, int lane) {
+    BeamPos p;
+    p.n = eos_cut && j == Lc - 1 ? 1 : nc_s[j];          // EOS is kept alone
+    // A parent's expansions come in candidate order (raw logits sorted, ties
+    // by id), so only its first W can be among the W best.
+    p.nw = p.n < W ? p.n : W;
+    // e / nw as a multiply and shift: exact for e < 256 and nw <= 16
+    p.magic = kDivMagic[p.nw];
+    p.par = static_cast<int>((static_cast<unsigned>(lane) * p.magic) >> 16);
+    p.r = lane - p.par * p.nw;
+    p.rl = rl_s[j * M + p.r];                            // r < nw <= M
+    p.lp = clp_s[j * M + p.r];
+    return p;
+}
+
 __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     // dynamic shared memory: the lattice's log-probabilities [G][M] and raw
     // logits [G][M] (float), counts [G], then the back-pointers [G][W] parent
@@ -393,6 +419,7 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     __shared__ double n_key[kCpsMaxBeam];      // the beams being chosen
     __shared__ float n_score[kCpsMaxBeam];
     __shared__ int n_lx[kCpsMaxBeam];
+    __shared__ int s_src[kCpsMaxBeam];         // beam t's expansion (ranked path)
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
     const int G = a.G, W = a.beam, M = a.mmax;
@@ -454,68 +481,76 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     float bscore = 0.0f;
     int blex = 0;
     int ncur = 1;
-    int n_next = nc_s[0];                      // the next position's count, read a step ahead
+    // The per-lane constants of the next position are independent of the
+    // beams, so they are read one position ahead of their use.
+    BeamPos nxt = {};
+    if (Lc > 0 && !empty) nxt = beam_position(nc_s, rl_s, clp_s, 0, Lc, eos_cut, W, M, lane);
     for (int j = 0; j < Lc && !empty; ++j) {
-        const int n = eos_cut && j == Lc - 1 ? 1 : n_next;    // EOS is kept alone
-        n_next = j + 1 < G ? nc_s[j + 1] : 0;
-        // A parent's expansions come in candidate order (raw logits sorted,
-        // ties by id), so only its first W can be among the W best.
-        const int nw = n < W ? n : W;
+        const BeamPos cur = nxt;
+        if (j + 1 < Lc) nxt = beam_position(nc_s, rl_s, clp_s, j + 1, Lc, eos_cut, W, M, lane);
+        const int n = cur.n, nw = cur.nw;
+        const unsigned magic = cur.magic;
         const int E = ncur * nw;
         const int keep = E < W ? E : W;
-        // e / nw as a multiply and shift: exact for e < 256 and nw <= 16
-        const unsigned magic = kDivMagic[nw];
         if (E <= 32) {
-            // one expansion per lane, ranked with shuffles
-            const int e = lane;
-            const int par = static_cast<int>((e * magic) >> 16), r = e - par * nw;
-            const bool valid = e < E;
-            const float rl = rl_s[j * M + r], lp = clp_s[j * M + r];   // r < nw <= M
-            const double key = __shfl_sync(0xffffffffu, bkey, par) + static_cast<double>(rl);
-            const float sc = __shfl_sync(0xffffffffu, bscore, par) + lp;
-            const int lx = __shfl_sync(0xffffffffu, blex, par) * n + r;
-            const long long ord = valid ? ordered_i64(key) : LLONG_MIN;
-            int rank = 0;
-            if (E <= 16) {
-                // all sources at once: independent shuffles, no loop-carried wait
-#pragma unroll
-                for (int src0 = 0; src0 < 16; ++src0) {
-                    const int src = src0 < E ? src0 : lane;        // lane itself adds 0
-                    const long long o2 = __shfl_sync(0xffffffffu, ord, src);
-                    const int l2 = __shfl_sync(0xffffffffu, lx, src);
-                    rank += (o2 > ord) || (o2 == ord && l2 < lx);
+            // one expansion per lane: e = lane takes candidate cur.r of beam cur.par
+            const bool valid = lane < E;
+            const double key = __shfl_sync(0xffffffffu, bkey, cur.par) + static_cast<double>(cur.rl);
+            const float sc = __shfl_sync(0xffffffffu, bscore, cur.par) + cur.lp;
+            // place in lexicographic order of (parent's place, candidate rank): below E
+            const int lx = __shfl_sync(0xffffffffu, blex, cur.par) * nw + cur.r;
+            const long long ord = ordered_i64(key);
+            int src = 0;                       // lane t < keep: the expansion that becomes beam t
+            if (keep <= 8) {
+                // The kept expansions one at a time, best first: the largest
+                // key (its high word, then its low word), ties to the smaller
+                // lexicographic place.  Three warp reductions a round.
+                const unsigned long long u = static_cast<unsigned long long>(ord) ^ 0x8000000000000000ull;
+                const unsigned hi = static_cast<unsigned>(u >> 32), lo = static_cast<unsigned>(u);
+                const unsigned tag = (static_cast<unsigned>(lx) << 5) | static_cast<unsigned>(lane);
+                bool left = valid;
+                for (int t = 0; t < keep; ++t) {
+                    const unsigned m1 = __reduce_max_sync(0xffffffffu, left ? hi : 0u);
+                    const bool c1 = left && hi == m1;
+                    const unsigned m2 = __reduce_max_sync(0xffffffffu, c1 ? lo : 0u);
+                    const bool c2 = c1 && lo == m2;
+                    const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, c2 ? tag : 0xffffffffu) & 31u);
+                    left = left && lane != win;
+                    src = lane == t ? win : src;
                 }
             } else {
-                // four sources per round: their shuffles go out together
+                // every expansion's rank (how many come before it), four
+                // sources a round so that their shuffles go out together
+                const long long o = valid ? ord : LLONG_MIN;
+                int rank = 0;
                 for (int s0 = 0; s0 < E; s0 += 4) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int src = s0 + u < E ? s0 + u : lane;
-                        const long long o2 = __shfl_sync(0xffffffffu, ord, src);
-                        const int l2 = __shfl_sync(0xffffffffu, lx, src);
-                        rank += (o2 > ord) || (o2 == ord && l2 < lx);
+                        const int s = s0 + u < E ? s0 + u : lane;        // lane itself adds 0
+                        const long long o2 = __shfl_sync(0xffffffffu, o, s);
+                        const int l2 = __shfl_sync(0xffffffffu, lx, s);
+                        rank += (o2 > o) || (o2 == o && l2 < lx);
                     }
                 }
+                if (valid && rank < keep) s_src[rank] = lane;
+                __syncwarp();
+                if (lane < keep) src = s_src[lane];
+                __syncwarp();
             }
-            // the kept expansions hand their state to beam slot `rank`
-            if (valid && rank < keep) {
-                bp_parent[j * W + rank] = static_cast<unsigned char>(par);
-                bp_rank[j * W + rank] = static_cast<unsigned char>(r);
-                n_key[rank] = key;
-                n_score[rank] = sc;
-                n_lx[rank] = lx;
-            }
-            __syncwarp();
+            // beam t takes over its expansion's state; its new place among
+            // the kept beams counts the kept places below its own
+            const double nkey = __shfl_sync(0xffffffffu, key, src);
+            const float nsc = __shfl_sync(0xffffffffu, sc, src);
+            const int nlx = __shfl_sync(0xffffffffu, lx, src);
+            const unsigned kept = __reduce_or_sync(0xffffffffu, lane < keep ? 1u << nlx : 0u);
             if (lane < keep) {
-                const int l = n_lx[lane];
-                int pos = 0;
-#pragma unroll
-                for (int t = 0; t < kCpsMaxBeam; ++t) pos += t < keep && n_lx[t] < l;
-                bkey = n_key[lane];
-                bscore = n_score[lane];
-                blex = pos;
+                const int sp = static_cast<int>((static_cast<unsigned>(src) * magic) >> 16);
+                bp_parent[j * W + lane] = static_cast<unsigned char>(sp);
+                bp_rank[j * W + lane] = static_cast<unsigned char>(src - sp * nw);
+                bkey = nkey;
+                bscore = nsc;
+                blex = __popc(kept & ((1u << nlx) - 1u));
             }
-            __syncwarp();
         } else {
             // more expansions than lanes: through shared memory
             if (lane < ncur) {

@@ -176,15 +176,17 @@ def test_cps_halves_equal_whole():
     assert (whole["ncand"][1, 5:] == 0).all()
 
 
+@pytest.mark.parametrize("beam", [3, 7])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
-def test_cps_exact_ties_on_a_coarse_grid(dt):
+def test_cps_exact_ties_on_a_coarse_grid(dt, beam):
     """Logits on a quarter grid: many paths tie exactly in their score; the
-    order must be the tie rule's on both sides, not rounding's."""
+    order must be the tie rule's on both sides, not rounding's.  Beam 3 keeps
+    every step within one warp's lanes; beam 7 also ranks 49 expansions."""
     B, G, V = 6, 8, 2000
     gen = torch.Generator(device="cuda")
     gen.manual_seed(13)
     q = (torch.round(torch.randn((B, G, V), generator=gen, device="cuda") * 4) / 4 * 1.5).to(dt)
-    gpu, orc = run_both(q, torch.tensor([0.6, 1.0, 1.0, 0.8, 1.3, 0.7], device="cuda"), 0.9, 12, 7)
+    gpu, orc = run_both(q, torch.tensor([0.6, 1.0, 1.0, 0.8, 1.3, 0.7], device="cuda"), 0.9, 12, beam)
     assert compare_cps(gpu, orc, "grid", _qf(q)) <= 1
 
 
