@@ -37,6 +37,11 @@ __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassA
     // Let the select kernel launch now: it waits for this grid before it
     // reads any partial.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Launched as a programmatic dependent of the previous step's sample
+    // kernel, this grid may be resident before that kernel ends: wait for it
+    // (and its memory) before reading or writing anything.  A no-op when the
+    // launch is an ordinary one.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t item = (static_cast<int64_t>(blockIdx.x) * kRowPassThreads + threadIdx.x) >> 5;
     const int64_t rows_per_seq_p = static_cast<int64_t>(a.K) * (a.G + 1);
@@ -112,16 +117,21 @@ cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm) {
                       blocks_per_sm, rowpass_kernel<false>, kRowPassThreads, 0);
 }
 
-cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, cudaStream_t s) {
+cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, cudaStream_t s, bool pdl) {
     constexpr int64_t per_cta = kRowPassThreads / 32;
     const int64_t g = (a.items + per_cta - 1) / per_cta;
     if (g < 1 || g > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const int grid = static_cast<int>(g);
-    if (bf16)
-        rowpass_kernel<true><<<grid, kRowPassThreads, 0, s>>>(a);
-    else
-        rowpass_kernel<false><<<grid, kRowPassThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(g));
+    cfg.blockDim = dim3(kRowPassThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (bf16) return cudaLaunchKernelEx(&cfg, rowpass_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, rowpass_kernel<false>, a);
 }
 
 }  // namespace sdv

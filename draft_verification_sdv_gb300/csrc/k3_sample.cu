@@ -81,6 +81,9 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
     const uint32_t rank = cluster_rank();
     const int CL = a.cluster;
     const int64_t b = blockIdx.x / CL;
+    // The next step's row pass, when launched as a programmatic dependent,
+    // may become resident now: it waits for this grid before it starts.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // The tasks are written by the select kernel: wait for it to finish.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const SeqTask t = a.tasks[b];

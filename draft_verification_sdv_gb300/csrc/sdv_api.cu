@@ -246,7 +246,7 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
         ++ctx->prof_n;
     }
     if (ev) cudaEventRecord(ev[0], ctx->stream);
-    cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->stream);
+    cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->stream, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "row pass launch");
     if (ev) cudaEventRecord(ev[1], ctx->stream);
 

@@ -195,11 +195,11 @@ cudaError_t launch_adl(const AdlArgs& a, cudaStream_t s);
 
 // Launchers (defined next to their kernels).  `bf16` selects the element type
 // (bf16 when true, fp32 otherwise).  Each returns the launch's error code.
-// The select and sample kernels are launched as programmatic dependents of
-// the kernel before them on the stream: they may start while it finishes and
-// wait (griddepcontrol.wait) before reading its results; `pdl` = false
+// All three kernels are launched as programmatic dependents of the kernel
+// before them on the stream: they may become resident while it finishes and
+// wait (griddepcontrol.wait) for it before touching memory; `pdl` = false
 // launches them as ordinary stream-ordered kernels.
-cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, cudaStream_t s, bool pdl);
 cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_sample(const SampleArgs& a, bool bf16, int B, int cluster, size_t smem,
                           cudaStream_t s, bool pdl);

@@ -159,7 +159,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     ra.nvec = nvec;
     ra.chunk_vec = chunk_vec;
     ra.items = items;
-    if (launch_rowpass(ra, dtype == SDV_BF16, s) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_rowpass(ra, dtype == SDV_BF16, s, true) != cudaSuccess) return SDV_ERR_CUDA;
 
     SelectArgs sa;
     sa.p = p_logits;
