@@ -413,6 +413,14 @@ class Verifier:
             raise SdvError(st, sdv_last_error(self.ctx))
         return out
 
+    def set_stream(self, stream) -> None:
+        """Enqueue later steps on `stream` (for CUDA-graph capture: the
+        capturing stream).  The caller orders it after earlier steps."""
+        st = sdv_set_stream(self.ctx, stream)
+        if st != SDV_OK:
+            raise SdvError(st, sdv_last_error(self.ctx))
+        self.stream = stream
+
     def sync(self) -> None:
         st = sdv_sync(self.ctx)
         if st != SDV_OK:

@@ -53,6 +53,18 @@
  * reported by the next sdv_sync.  A context is not thread-safe; use one
  * context per stream.  Outputs are a pure function of (inputs, temperature,
  * seed).
+ *
+ * CUDA graphs: sdv_verify, sdv_verify_ex, sdv_verify_len, sdv_cps,
+ * sdv_cps_prune, sdv_cps_beam and sdv_adl_step check their arguments on the
+ * host and enqueue kernels; they allocate nothing, copy nothing and never
+ * wait.  Each may therefore be captured into a CUDA graph, in any capture
+ * mode, when the stream it launches on (the context's, for the verify calls:
+ * see sdv_set_stream) is the capturing stream, with kernel timing off.  Make
+ * one uncaptured call of each shape first (the path search may set a kernel
+ * attribute on its first call with a large lattice).  A replay recomputes the
+ * step from the current contents of the captured buffers, with the scalars of
+ * the capture (temperature, seed, tau, ...).  sdv_verify_host and sdv_sync
+ * wait for the stream and cannot be captured.
  */
 #ifndef SDV_H
 #define SDV_H
@@ -213,7 +225,9 @@ void sdv_destroy(sdv_ctx* ctx);
 sdv_status sdv_plan(const sdv_ctx* ctx, int* rowpass_ctas, int64_t* chunk_vectors,
                     int* chunks_per_row, int* sample_cluster);
 
-/* Replace the stream of a context (a cudaStream_t). */
+/* Replace the stream of a context (a cudaStream_t): later calls enqueue on
+ * it.  The caller orders it after work already enqueued on the old stream.
+ * To capture a step into a CUDA graph, set the capturing stream first. */
 sdv_status sdv_set_stream(sdv_ctx* ctx, void* stream);
 
 /*
