@@ -96,7 +96,10 @@ typedef enum { SDV_BF16 = 0, SDV_F32 = 1 } sdv_dtype;
  * device, enqueuing on `stream` (a cudaStream_t; NULL = the legacy default
  * stream).  Requires B >= 1, K >= 1, gamma >= 1, V >= 1, V * elt % 16 == 0.
  * Allocates the workspace (partial row statistics, per-sequence tasks, a
- * status word: a few MB at most).  On error *out is NULL.
+ * status word: a few MB at most).  The select pass holds about
+ * K * (20 * gamma + 12) bytes per sequence in shared memory; a shape beyond
+ * the device's per-block limit (227 KB on GB300, where K = 64 at gamma = 128
+ * fits) is refused with SDV_ERR_ARG.  On error *out is NULL.
  */
 sdv_status sdv_create(sdv_ctx** out, int B, int K, int gamma, int V,
                       sdv_dtype dtype, void* stream);
