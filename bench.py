@@ -499,8 +499,10 @@ def run_decode_step(args, rank, world):
     the path search over the marginals q [B, gamma, V] (beam 3, 15
     candidates, mass 0.8, EOS cut), verification of the beam's K = 3 paths at
     their lattice lengths (shared marginals, shared prefix row), and the
-    draft-length update from the lattice and accepted lengths.  Large-window
-    shape: B 32, gamma 32, V 152064 bf16, per-sequence temperatures."""
+    draft-length update from the lattice and accepted lengths.  The path
+    search hands the marginal rows' softmax statistics to the verification,
+    which therefore streams only the verifier rows.  Large-window shape: B 32,
+    gamma 32, V 152064 bf16, per-sequence temperatures."""
     from draft_verification_sdv_gb300 import binding as bd
     bd.load(build=True)
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -514,14 +516,14 @@ def run_decode_step(args, rank, world):
     eos = 151643                                   # the Qwen2.5 end-of-text id
     v = bd.Verifier(B, K, G, V, w.dtype, shared_q=True, shared_prefix_row=True)
     ctl = bd.DraftLengthController(B, G, window=2, kmin=4, kmax=G, up=2, down=1, device=dev)
-    cps = bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps)
+    cps = bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, row_stat=True)
     out = None
 
     def step(i):
         nonlocal out
-        bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, out=cps)
+        bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, out=cps, row_stat=True)
         out = v(w.p_logits, w.q_logits, cps["paths"], seed=i, temps=w.temps, out=out,
-                draft_len=cps["lat_len"])
+                draft_len=cps["lat_len"], q_stat=cps["row_stat"])
         ctl.step(cps["lat_len"], out["accept_len"])
 
     for i in range(max(args.warmup, 3)):
@@ -549,7 +551,7 @@ def run_decode_step(args, rank, world):
     lat = cps["lat_len"].cpu().numpy()
     acc = out["accept_len"].cpu().numpy()
     elt = 2
-    rows = B * G + sum(1 + K * int(L) for L in lat) + sum(int(L) for L in lat)   # q, p, q
+    rows = B * G + sum(1 + K * int(L) for L in lat)                            # q once, p
     rows += sum(2 if int(a) < int(L) else 1 for a, L in zip(acc, lat))         # the draw
     gbs = rows * V * elt / (ms * 1e-3) / 1e9
     peak, kind = measured_peaks()
@@ -563,6 +565,8 @@ def run_decode_step(args, rank, world):
             "input_dtype": "bf16", "data": "synthetic marginals and verifier rows (seeded)",
             "config": {"workload": "large-window marginals B%d K%d gamma%d V%d bf16" % (B, K, G, V),
                        "beam": K, "mmax": 15, "tau": 0.8, "eos_id": eos,
+                       "marginal_rows": "streamed once (the path search's statistics feed "
+                                        "the verification)",
                        "lattice_len_mean": float(lat.mean()),
                        "l2": "inputs %.2f GB > L2 (126 MB): no flush"
                              % ((w.p_logits.numel() + w.q_logits.numel()) * elt / 1e9)},

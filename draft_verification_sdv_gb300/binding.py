@@ -37,6 +37,8 @@ SIGNATURES = {
     "sdv_verify": (_I, [_VP, _VP, _VP, _VP, _F, _U64, _VP, _VP, _VP]),
     "sdv_verify_ex": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP, _VP]),
     "sdv_verify_len": (_I, [_VP, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP, _VP]),
+    "sdv_verify_qstat": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP,
+                              _VP]),
     "sdv_verify_host": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
     "sdv_sync": (_I, [_VP]),
     "sdv_last_error": (ctypes.c_char_p, [_VP]),
@@ -49,6 +51,8 @@ SIGNATURES = {
     "sdv_verify_static": (_I, [_I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
     "sdv_cps": (_I, [_I, _I, _I, _I, _VP, _VP, _F, _VP, _F, _I, _I, _I, _VP, _VP, _VP, _VP, _VP,
                      _VP, _VP, _VP]),
+    "sdv_cps_ex": (_I, [_I, _I, _I, _I, _VP, _VP, _F, _VP, _F, _I, _I, _I, _VP, _VP, _VP, _VP,
+                        _VP, _VP, _VP, _VP, _VP]),
     "sdv_cps_prune": (_I, [_I, _I, _I, _I, _VP, _VP, _F, _VP, _F, _I, _VP, _VP, _VP, _VP]),
     "sdv_cps_beam": (_I, [_I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "sdv_adl_state_words": (_I, [_I]),
@@ -158,6 +162,21 @@ def sdv_verify_ex(ctx, p_logits, q_logits, drafts, temperature, temperature_per_
         _dev_ptr(out_lse, torch.float32, "out_lse"))
 
 
+def sdv_verify_qstat(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
+                     temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
+                     out_scores=None, out_lse=None) -> int:
+    return load().sdv_verify_qstat(
+        ctx, _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
+        _dev_ptr(drafts, torch.int32, "drafts"), _dev_ptr(draft_len, torch.int32, "draft_len"),
+        _dev_ptr(q_row_stat, torch.float32, "q_row_stat"), float(temperature),
+        _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
+        _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
+        _dev_ptr(out_next_token, torch.int32, "out_next_token"),
+        _dev_ptr(out_scores, torch.float32, "out_scores"),
+        _dev_ptr(out_lse, torch.float32, "out_lse"))
+
+
 def sdv_verify_len(ctx, p_logits, q_logits, drafts, draft_len, temperature, temperature_per_seq,
                    seed, out_sel, out_accept_len, out_next_token, out_scores=None,
                    out_lse=None) -> int:
@@ -234,14 +253,18 @@ def sdv_verify_static(B, K, gamma, V, dtype, stream, p_logits, q_logits, drafts,
 
 def sdv_cps(q_marginals, tau: float = 0.8, mmax: int = 15, beam: int = 3, eos_id: int = -1,
             temperature: float = 1.0, temps: Optional[torch.Tensor] = None, stream=None,
-            out: Optional[dict] = None) -> dict:
+            out: Optional[dict] = None, row_stat: bool = False) -> dict:
     """Causal-consistency path search over drafter marginals q [B, gamma, V]
     (candidate pruning by cumulative mass, EOS cut, beam by drafter
     confidence).  Enqueues on `stream` (default: the current stream) and
     returns the output tensors; `out` (a dict this returned for the same
-    shapes) reuses them."""
+    shapes) reuses them.  With `row_stat`, out["row_stat"] [B, gamma, 4] holds
+    each marginal row's softmax statistics (sdv_cps_ex), which a Verifier call
+    takes as `q_stat` so that it does not stream the marginals again."""
     B, G, V = q_marginals.shape
     dev = q_marginals.device
+    if out is not None and row_stat and "row_stat" not in out:
+        out["row_stat"] = torch.empty((B, G, 4), dtype=torch.float32, device=dev)
     out = out if out is not None else {
         "cand_ids": torch.empty((B, G, mmax), dtype=torch.int32, device=dev),
         "cand_logp": torch.empty((B, G, mmax), dtype=torch.float32, device=dev),
@@ -252,12 +275,17 @@ def sdv_cps(q_marginals, tau: float = 0.8, mmax: int = 15, beam: int = 3, eos_id
         "npaths": torch.empty((B,), dtype=torch.int32, device=dev),
         "lat_len": torch.empty((B,), dtype=torch.int32, device=dev),
     }
-    st = load().sdv_cps(B, G, V, _dtype_code(q_marginals.dtype), ctypes.c_void_p(_stream_handle(stream)),
-                        _dev_ptr(q_marginals, name="q_marginals"), float(temperature),
-                        _dev_ptr(temps, torch.float32, "temps"), float(tau), int(mmax), int(beam),
-                        int(eos_id), *[_dev_ptr(out[k]) for k in ("cand_ids", "cand_logp", "cand_logit",
-                                                                  "ncand", "paths", "path_logp",
-                                                                  "npaths", "lat_len")])
+    if row_stat and "row_stat" not in out:
+        out["row_stat"] = torch.empty((B, G, 4), dtype=torch.float32, device=dev)
+    st = load().sdv_cps_ex(B, G, V, _dtype_code(q_marginals.dtype),
+                           ctypes.c_void_p(_stream_handle(stream)),
+                           _dev_ptr(q_marginals, name="q_marginals"), float(temperature),
+                           _dev_ptr(temps, torch.float32, "temps"), float(tau), int(mmax), int(beam),
+                           int(eos_id), *[_dev_ptr(out[k]) for k in ("cand_ids", "cand_logp",
+                                                                     "cand_logit", "ncand", "paths",
+                                                                     "path_logp", "npaths",
+                                                                     "lat_len")],
+                           _dev_ptr(out["row_stat"], torch.float32, "row_stat") if row_stat else None)
     if st != SDV_OK:
         raise SdvError(st, "sdv_cps")
     return out
@@ -376,9 +404,13 @@ class Verifier:
 
     def __call__(self, p_logits, q_logits, drafts, temperature: float = 1.0, seed: int = 0,
                  temps: Optional[torch.Tensor] = None, scores: bool = False, lse: bool = False,
-                 out: Optional[dict] = None, draft_len: Optional[torch.Tensor] = None) -> dict:
+                 out: Optional[dict] = None, draft_len: Optional[torch.Tensor] = None,
+                 q_stat: Optional[torch.Tensor] = None) -> dict:
         """One verification step; `draft_len` (int32 [B] on the device) gives
-        each sequence's draft length (sdv_verify_len), else all are gamma."""
+        each sequence's draft length (sdv_verify_len), else all are gamma;
+        `q_stat` (float32 [rows_q, 4], e.g. sdv_cps(..., row_stat=True)
+        ["row_stat"]) supplies the drafter rows' softmax statistics, so the
+        q rows are not streamed (sdv_verify_qstat)."""
         B, K, G, V = self.B, self.K, self.gamma, self.V
         q_shape = (B, G, V) if self.shared_q else (B, K, G, V)
         if tuple(p_logits.shape) != (B, K, G + 1, V):
@@ -401,7 +433,11 @@ class Verifier:
             if lse:
                 out["lse"] = torch.empty((B, K, G + 1 if self.greedy else 2 * G + 1),
                                          dtype=torch.float32, device=dev)
-        if draft_len is None:
+        if q_stat is not None:
+            st = sdv_verify_qstat(self.ctx, p_logits, q_logits, drafts, draft_len, q_stat,
+                                  temperature, temps, seed, out["sel"], out["accept_len"],
+                                  out["next_token"], out.get("scores"), out.get("lse"))
+        elif draft_len is None:
             st = sdv_verify_ex(self.ctx, p_logits, q_logits, drafts, temperature, temps, seed,
                                out["sel"], out["accept_len"], out["next_token"], out.get("scores"),
                                out.get("lse"))

@@ -140,8 +140,18 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const bool x_ok = x >= 0 && x < a.V;
         float mp, sp, mq = 0.0f, sq = 1.0f;
         const float2* prow_part = a.part + rp * a.chunks;
-        merge_rows2(prow_part, greedy ? prow_part : a.part + (a.rows_p + rq) * a.chunks, a.chunks, c,
-                    mp, sp, mq, sq);
+        if (a.q_stat) {
+            // the drafter row's statistics come from the caller (computed by
+            // the path search at the temperature recorded in them)
+            merge_row(prow_part, a.chunks, c, mp, sp);
+            const float4 st = a.q_stat[rq];
+            mq = st.x;
+            sq = st.y;
+            if (st.z != c) atomicOr(&s_bad, kStatusBadStat);
+        } else {
+            merge_rows2(prow_part, greedy ? prow_part : a.part + (a.rows_p + rq) * a.chunks, a.chunks,
+                        c, mp, sp, mq, sq);
+        }
         if (greedy) {
             mq = 0.0f;
             sq = 1.0f;

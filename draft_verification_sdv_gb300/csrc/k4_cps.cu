@@ -333,6 +333,9 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
     }
     float M = s_m[0], S = s_s[0];
     for (int w2 = 1; w2 < NW; ++w2) merge_stat(M, S, s_m[w2], s_s[w2], c);
+    // the row's softmax statistics, for a verification of these marginals
+    // that then need not read the rows again
+    if (lane == 0 && a.row_stat) a.row_stat[row] = make_float4(M, S, c, 0.0f);
     // lane r holds the rank-r candidate; the cut is a running sum of masses
     const int mmax = a.mmax;
     const bool ok = isfinite(M) && isfinite(S) && S > 0.0f;

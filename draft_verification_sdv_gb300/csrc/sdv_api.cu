@@ -189,10 +189,10 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
 namespace {
 
 sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
-                       const int32_t* drafts, const int32_t* draft_len, float temperature,
-                       const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
-                       int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
-                       float* out_lse) {
+                       const int32_t* drafts, const int32_t* draft_len, const float* q_row_stat,
+                       float temperature, const float* temperature_per_seq, uint64_t seed,
+                       int32_t* out_sel, int32_t* out_accept_len, int32_t* out_next_token,
+                       float* out_scores, float* out_lse) {
     if (!ctx) return SDV_ERR_ARG;
     ctx->err[0] = 0;
     const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
@@ -217,6 +217,11 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
         return fail(ctx, SDV_ERR_ARG, "out_lse is not a device pointer");
     if (draft_len && ((reinterpret_cast<uintptr_t>(draft_len) & 3u) || !is_device_ptr(draft_len)))
         return fail(ctx, SDV_ERR_ARG, "draft_len must be a 4-byte aligned device pointer");
+    if (q_row_stat && greedy)
+        return fail(ctx, SDV_ERR_ARG, "greedy acceptance reads no drafter rows: q_row_stat must be null");
+    if (q_row_stat &&
+        ((reinterpret_cast<uintptr_t>(q_row_stat) & 15u) || !is_device_ptr(q_row_stat)))
+        return fail(ctx, SDV_ERR_ARG, "q_row_stat must be a 16-byte aligned device pointer");
 
     RowPassArgs ra;
     ra.p = p_logits;
@@ -232,7 +237,9 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     ra.rows_total = ctx->rows_total;
     ra.nvec = ctx->nvec;
     ra.chunk_vec = ctx->chunk_vec;
-    ra.items = ctx->items;
+    // with the drafter rows' statistics supplied, only the verifier rows are
+    // streamed (the q rows come after them in item order)
+    ra.items = q_row_stat ? ctx->rows_p * ctx->chunks : ctx->items;
     ra.lens = draft_len;
     cudaEvent_t* ev = nullptr;
     if (ctx->prof_on && ctx->prof_n < kMaxProfSteps) {
@@ -274,6 +281,7 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     sa.tasks = ctx->tasks;
     sa.status = ctx->status;
     sa.lens = draft_len;
+    sa.q_stat = reinterpret_cast<const float4*>(q_row_stat);
     e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "select launch");
     if (ev) cudaEventRecord(ev[2], ctx->stream);
@@ -300,8 +308,9 @@ sdv_status sdv_verify_ex(sdv_ctx* ctx, const void* p_logits, const void* q_logit
                          const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
                          int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
                          float* out_lse) {
-    return verify_impl(ctx, p_logits, q_logits, drafts, nullptr, temperature, temperature_per_seq,
-                       seed, out_sel, out_accept_len, out_next_token, out_scores, out_lse);
+    return verify_impl(ctx, p_logits, q_logits, drafts, nullptr, nullptr, temperature,
+                       temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
+                       out_scores, out_lse);
 }
 
 sdv_status sdv_verify_len(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
@@ -310,8 +319,21 @@ sdv_status sdv_verify_len(sdv_ctx* ctx, const void* p_logits, const void* q_logi
                           int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
                           float* out_lse) {
     if (!draft_len) return ctx ? fail(ctx, SDV_ERR_ARG, "draft_len is null") : SDV_ERR_ARG;
-    return verify_impl(ctx, p_logits, q_logits, drafts, draft_len, temperature, temperature_per_seq,
-                       seed, out_sel, out_accept_len, out_next_token, out_scores, out_lse);
+    return verify_impl(ctx, p_logits, q_logits, drafts, draft_len, nullptr, temperature,
+                       temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
+                       out_scores, out_lse);
+}
+
+sdv_status sdv_verify_qstat(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                            const int32_t* drafts, const int32_t* draft_len,
+                            const float* q_row_stat, float temperature,
+                            const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
+                            int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
+                            float* out_lse) {
+    if (!q_row_stat) return ctx ? fail(ctx, SDV_ERR_ARG, "q_row_stat is null") : SDV_ERR_ARG;
+    return verify_impl(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
+                       temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
+                       out_scores, out_lse);
 }
 
 sdv_status sdv_verify(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
@@ -333,10 +355,11 @@ sdv_status sdv_sync(sdv_ctx* ctx) {
     if (h & kStatusTimeout)
         return fail(ctx, SDV_ERR_CUDA, "a bounded device wait gave up (status 0x%x)", h);
     if (h)
-        return fail(ctx, SDV_ERR_DEVICE_DATA, "device data error (status 0x%x:%s%s%s)", h,
+        return fail(ctx, SDV_ERR_DEVICE_DATA, "device data error (status 0x%x:%s%s%s%s)", h,
                     (h & kStatusBadDraft) ? " draft id out of range" : "",
                     (h & kStatusBadRow) ? " non-finite or all -inf row" : "",
-                    (h & kStatusBadTemp) ? " bad per-sequence temperature" : "");
+                    (h & kStatusBadTemp) ? " bad per-sequence temperature" : "",
+                    (h & kStatusBadStat) ? " drafter-row statistics of another temperature" : "");
     return SDV_OK;
 }
 
@@ -487,15 +510,18 @@ sdv_status cps_prune_args(int B, int gamma, int V, sdv_dtype dtype, const void* 
 
 }  // namespace
 
-sdv_status sdv_cps_prune(int B, int gamma, int V, sdv_dtype dtype, void* stream,
-                         const void* q_marginals, float temperature,
-                         const float* temperature_per_seq, float tau, int mmax,
-                         int32_t* out_cand_ids, float* out_cand_logp, float* out_cand_logit,
-                         int32_t* out_ncand) {
+namespace {
+
+sdv_status cps_prune_impl(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                          const void* q_marginals, float temperature,
+                          const float* temperature_per_seq, float tau, int mmax,
+                          int32_t* out_cand_ids, float* out_cand_logp, float* out_cand_logit,
+                          int32_t* out_ncand, float* out_row_stat) {
     if (!out_cand_ids || !out_cand_logp || !out_cand_logit || !out_ncand) return SDV_ERR_ARG;
-    const void* ptrs[6] = {q_marginals,   temperature_per_seq, out_cand_ids,
-                           out_cand_logp, out_cand_logit,      out_ncand};
-    sdv_status st = cps_check(B, gamma, mmax, 1, false, ptrs, 6);
+    if (reinterpret_cast<uintptr_t>(out_row_stat) & 15u) return SDV_ERR_ARG;
+    const void* ptrs[7] = {q_marginals,    temperature_per_seq, out_cand_ids, out_cand_logp,
+                           out_cand_logit, out_ncand,           out_row_stat};
+    sdv_status st = cps_check(B, gamma, mmax, 1, false, ptrs, 7);
     if (st != SDV_OK) return st;
     CpsArgs a{};
     st = cps_prune_args(B, gamma, V, dtype, q_marginals, temperature, temperature_per_seq, tau,
@@ -505,8 +531,21 @@ sdv_status sdv_cps_prune(int B, int gamma, int V, sdv_dtype dtype, void* stream,
     a.cand_logp = out_cand_logp;
     a.cand_logit = out_cand_logit;
     a.ncand = out_ncand;
+    a.row_stat = reinterpret_cast<float4*>(out_row_stat);
     return launch_cps_prune(a, dtype == SDV_BF16, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SDV_OK : SDV_ERR_CUDA;
+}
+
+}  // namespace
+
+sdv_status sdv_cps_prune(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                         const void* q_marginals, float temperature,
+                         const float* temperature_per_seq, float tau, int mmax,
+                         int32_t* out_cand_ids, float* out_cand_logp, float* out_cand_logit,
+                         int32_t* out_ncand) {
+    return cps_prune_impl(B, gamma, V, dtype, stream, q_marginals, temperature,
+                          temperature_per_seq, tau, mmax, out_cand_ids, out_cand_logp,
+                          out_cand_logit, out_ncand, nullptr);
 }
 
 sdv_status sdv_cps_beam(int B, int gamma, int V, int mmax, int beam, int eos_id, void* stream,
@@ -545,14 +584,27 @@ sdv_status sdv_cps(int B, int gamma, int V, sdv_dtype dtype, void* stream,
                    float* out_cand_logp, float* out_cand_logit, int32_t* out_ncand,
                    int32_t* out_paths,
                    float* out_path_logp, int32_t* out_npaths, int32_t* out_lat_len) {
+    return sdv_cps_ex(B, gamma, V, dtype, stream, q_marginals, temperature, temperature_per_seq,
+                      tau, mmax, beam, eos_id, out_cand_ids, out_cand_logp, out_cand_logit,
+                      out_ncand, out_paths, out_path_logp, out_npaths, out_lat_len, nullptr);
+}
+
+sdv_status sdv_cps_ex(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                      const void* q_marginals, float temperature,
+                      const float* temperature_per_seq, float tau, int mmax, int beam,
+                      int eos_id, int32_t* out_cand_ids, float* out_cand_logp,
+                      float* out_cand_logit, int32_t* out_ncand, int32_t* out_paths,
+                      float* out_path_logp, int32_t* out_npaths, int32_t* out_lat_len,
+                      float* out_row_stat) {
     // both halves' argument checks run before either launches
     if (V < 1 || eos_id >= V || beam < 1 || beam > kCpsMaxBeam) return SDV_ERR_ARG;
     if (!out_paths || !out_path_logp || !out_npaths) return SDV_ERR_ARG;
     const void* ptrs[4] = {out_paths, out_path_logp, out_npaths, out_lat_len};
     sdv_status st = cps_check(B, gamma, mmax, beam, true, ptrs, 4);
     if (st != SDV_OK) return st;
-    st = sdv_cps_prune(B, gamma, V, dtype, stream, q_marginals, temperature, temperature_per_seq,
-                       tau, mmax, out_cand_ids, out_cand_logp, out_cand_logit, out_ncand);
+    st = cps_prune_impl(B, gamma, V, dtype, stream, q_marginals, temperature, temperature_per_seq,
+                        tau, mmax, out_cand_ids, out_cand_logp, out_cand_logit, out_ncand,
+                        out_row_stat);
     if (st != SDV_OK) return st;
     return sdv_cps_beam(B, gamma, V, mmax, beam, eos_id, stream, out_cand_ids, out_cand_logp,
                         out_cand_logit, out_ncand, out_paths, out_path_logp, out_npaths,

@@ -37,6 +37,7 @@ enum : unsigned {
     kStatusBadTemp = 4u,     // per-sequence temperature not finite and positive
     kStatusTimeout = 8u,     // a bounded device wait gave up
     kStatusBadLength = 16u,  // a draft length outside [kmin, kmax] given to the controller
+    kStatusBadStat = 32u,    // supplied drafter-row statistics of another temperature
 };
 
 // Adaptive draft length ("DiffuSpec", section 4.3).  A sequence's state is
@@ -142,6 +143,10 @@ struct SelectArgs {
     SeqTask* tasks;
     unsigned* status;
     const int32_t* lens = nullptr;   // [B] draft length per sequence, or nullptr (= G)
+    // [rows_q] drafter-row statistics {max, sum 2^{(l - max) c}, c, 0} given by
+    // the caller (the path search's pruning pass writes them), or nullptr to
+    // merge the row pass's partials of the q rows
+    const float4* q_stat = nullptr;
 };
 
 // Residual / bonus sampling (K3): a cluster of `cluster` CTAs per sequence,
@@ -177,6 +182,7 @@ struct CpsArgs {
     float* path_logp;       // [B][beam]
     int32_t* npaths;        // [B]
     int32_t* lat_len;       // [B] or nullptr
+    float4* row_stat = nullptr;   // [B][G] {max, sum 2^{(l - max) c}, c, 0} or nullptr
 };
 // Pruning (reads q, temps; writes cand_ids, cand_logp, ncand) and the beam
 // (reads and trims the lattice; writes paths, path_logp, npaths, lat_len).

@@ -54,10 +54,10 @@
  * context per stream.  Outputs are a pure function of (inputs, temperature,
  * seed).
  *
- * CUDA graphs: sdv_verify, sdv_verify_ex, sdv_verify_len, sdv_cps,
- * sdv_cps_prune, sdv_cps_beam and sdv_adl_step check their arguments on the
- * host and enqueue kernels; they allocate nothing, copy nothing and never
- * wait.  Each may therefore be captured into a CUDA graph, in any capture
+ * CUDA graphs: sdv_verify, sdv_verify_ex, sdv_verify_len, sdv_verify_qstat,
+ * sdv_cps, sdv_cps_ex, sdv_cps_prune, sdv_cps_beam and sdv_adl_step check
+ * their arguments on the host and enqueue kernels; they allocate nothing,
+ * copy nothing and never wait.  Each may therefore be captured into a CUDA graph, in any capture
  * mode, when the stream it launches on (the context's, for the verify calls:
  * see sdv_set_stream) is the capturing stream, with kernel timing off.  Make
  * one uncaptured call of each shape first (the path search may set a kernel
@@ -193,6 +193,33 @@ sdv_status sdv_verify_len(sdv_ctx* ctx, const void* p_logits, const void* q_logi
                           float* out_lse);
 
 /*
+ * As sdv_verify_len (draft_len may be NULL: every draft has gamma tokens),
+ * with the drafter rows' softmax statistics supplied by the caller instead of
+ * computed here.  In a decode step the path search has just streamed the same
+ * marginals (sdv_cps_ex writes these statistics), so the verification reads
+ * the q rows only at the drafted tokens and, for a rejection, in the residual
+ * draw: one full pass over the marginals per step instead of two.
+ *   q_row_stat  device float [rows_q][4], 16-byte aligned, one entry per q
+ *               row in q_logits' row order ([B][gamma] with
+ *               SDV_FLAG_SHARED_Q, else [B][K][gamma]):
+ *               {m, s, c, 0} with c = log2(e) / T (T the row's sequence's
+ *               temperature, as a float), m the row's largest logit and
+ *               s = sum over the row of 2^((logit - m) * c)
+ * The result is that of sdv_verify_len up to the rounding of s (the sum is
+ * taken in another order).  An entry whose c differs from the c this call
+ * computes for its sequence is a data error for that sequence (outputs -1,
+ * SDV_ERR_DEVICE_DATA from sdv_sync).  A row whose m or s is not finite, or
+ * s <= 0, is a bad row as for sdv_verify_ex.  Not with SDV_FLAG_GREEDY
+ * (which reads no q rows): SDV_ERR_ARG.
+ */
+sdv_status sdv_verify_qstat(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                            const int32_t* drafts, const int32_t* draft_len,
+                            const float* q_row_stat, float temperature,
+                            const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
+                            int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
+                            float* out_lse);
+
+/*
  * End-to-end variant for callers whose data lives in HOST memory: copies the
  * inputs to device buffers owned by the context (allocated on the first call,
  * the size of one batch's inputs), runs sdv_verify_ex, copies the three
@@ -283,6 +310,22 @@ sdv_status sdv_cps(int B, int gamma, int V, sdv_dtype dtype, void* stream,
                    int eos_id, int32_t* out_cand_ids, float* out_cand_logp,
                    float* out_cand_logit, int32_t* out_ncand, int32_t* out_paths,
                    float* out_path_logp, int32_t* out_npaths, int32_t* out_lat_len);
+
+/*
+ * sdv_cps that also writes every marginal row's softmax statistics, as the
+ * pruning pass computes them, to out_row_stat (device float [B][gamma][4],
+ * 16-byte aligned, or NULL): {m, s, c, 0} with c = log2(e) / T, m the row's
+ * largest logit and s = sum of 2^((logit - m) * c).  sdv_verify_qstat takes
+ * them so that the verification of the paths does not stream the marginals a
+ * second time.
+ */
+sdv_status sdv_cps_ex(int B, int gamma, int V, sdv_dtype dtype, void* stream,
+                      const void* q_marginals, float temperature,
+                      const float* temperature_per_seq, float tau, int mmax, int beam,
+                      int eos_id, int32_t* out_cand_ids, float* out_cand_logp,
+                      float* out_cand_logit, int32_t* out_ncand, int32_t* out_paths,
+                      float* out_path_logp, int32_t* out_npaths, int32_t* out_lat_len,
+                      float* out_row_stat);
 
 /*
  * The two halves of sdv_cps, for callers that inspect or reuse the pruned
