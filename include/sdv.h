@@ -202,9 +202,9 @@ sdv_status sdv_verify_len(sdv_ctx* ctx, const void* p_logits, const void* q_logi
  *   q_row_stat  device float [rows_q][4], 16-byte aligned, one entry per q
  *               row in q_logits' row order ([B][gamma] with
  *               SDV_FLAG_SHARED_Q, else [B][K][gamma]):
- *               {m, s, c, 0} with c = log2(e) / T (T the row's sequence's
- *               temperature, as a float), m the row's largest logit and
- *               s = sum over the row of 2^((logit - m) * c)
+ *               {m, s, c, 0} with c = 1.4426950408889634f / T, an fp32
+ *               division (T the row's sequence's temperature), m the row's
+ *               largest logit and s = sum over the row of 2^((logit - m) * c)
  * The result is that of sdv_verify_len up to the rounding of s (the sum is
  * taken in another order).  An entry whose c differs from the c this call
  * computes for its sequence is a data error for that sequence (outputs -1,
@@ -314,8 +314,8 @@ sdv_status sdv_cps(int B, int gamma, int V, sdv_dtype dtype, void* stream,
 /*
  * sdv_cps that also writes every marginal row's softmax statistics, as the
  * pruning pass computes them, to out_row_stat (device float [B][gamma][4],
- * 16-byte aligned, or NULL): {m, s, c, 0} with c = log2(e) / T, m the row's
- * largest logit and s = sum of 2^((logit - m) * c).  sdv_verify_qstat takes
+ * 16-byte aligned, or NULL): {m, s, c, 0} with c = 1.4426950408889634f / T
+ * (fp32), m the row's largest logit and s = sum of 2^((logit - m) * c).  sdv_verify_qstat takes
  * them so that the verification of the paths does not stream the marginals a
  * second time.
  */
