@@ -49,6 +49,14 @@ def test_argument_errors_without_gpu(lib):
         assert lib.sdv_create(ctypes.byref(ctx), B, K, G, V, dt, None) == bd.SDV_ERR_ARG
         assert ctx.value is None
     assert lib.sdv_verify(None, None, None, None, 1.0, 0, None, None, None) == bd.SDV_ERR_ARG
+    assert lib.sdv_verify_qstat(None, None, None, None, None, None, 1.0, None, 0, None, None, None,
+                                None, None) == bd.SDV_ERR_ARG
+    # path search with statistics: shape and limit checks come before any CUDA call
+    for B, G, mmax, beam in [(0, 4, 8, 3), (1, 0, 8, 3), (1, 4, 0, 3), (1, 4, 17, 3), (1, 4, 8, 0),
+                             (1, 4, 8, 17)]:
+        assert lib.sdv_cps_ex(B, G, 64, bd.SDV_BF16, None, None, 1.0, None, 0.8, mmax, beam, -1,
+                              None, None, None, None, None, None, None, None,
+                              None) == bd.SDV_ERR_ARG
     assert lib.sdv_sync(None) == bd.SDV_ERR_ARG
     assert lib.sdv_last_error(None) == b"null context"
     lib.sdv_destroy(None)
