@@ -15,7 +15,9 @@
 // kept candidates are the shortest prefix of the row's list, in order of
 // probability, whose mass reaches tau, capped at mmax; tokens of probability
 // zero are never candidates, and a row with a NaN or +inf logit, or none
-// finite, keeps none.
+// finite, keeps none.  On request it also writes the row's statistics
+// {max, sum 2^{(l - max) c}, c}, so that a verification of the same marginals
+// need not stream them again.
 //
 // cps_beam_kernel, one warp per sequence: the lattice ends at the first
 // position whose most likely candidate is eos_id (kept alone as the last
