@@ -24,6 +24,23 @@ namespace {
 
 constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier wait
 
+// The two halves of a cluster barrier: arrive (no ordering) now, wait later.
+// Used to know that every CTA of the cluster has started before writing to
+// its shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Write two floats to the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ void st_dsmem_f32x2(float2* local, uint32_t rank, float x, float y) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(x), "f"(y) : "memory");
+}
+
 template <bool BF16>
 struct Elems {
     static constexpr int kPerVec = BF16 ? 8 : 4;
@@ -73,14 +90,18 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
     __shared__ float s_total;                      // read by the whole cluster
     __shared__ float s_ok;                         // 1 if the slice arrived
     __shared__ int s_pick, s_last_thread, s_token;
-    __shared__ float s_tot[8];                     // slice totals of the cluster
-    __shared__ int s_all_ok;
+    // (slice total, slice arrived) of every CTA of the cluster, per pass:
+    // each CTA writes its own pair into every CTA's copy
+    __shared__ float2 s_tot2[2][8];
 
     constexpr int EPV = Elems<BF16>::kPerVec;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster_rank();
     const int CL = a.cluster;
     const int64_t b = blockIdx.x / CL;
+    // Half a cluster barrier now; its wait, long after, tells that every CTA
+    // has started, so that the totals may be written into their memory.
+    cluster_arrive_relaxed();
     // The next step's row pass, when launched as a programmatic dependent,
     // may become resident now: it waits for this grid before it starts.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -167,29 +188,27 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         if (tid == kSampleThreads - 1) s_total = incl;
         __syncthreads();
 
-        // Slice totals of the whole cluster, in rank order: thread r reads
-        // rank r's total through distributed shared memory.
+        // Slice totals of the whole cluster, in rank order: thread r writes
+        // this CTA's (total, arrived) into CTA r; after the barrier every CTA
+        // reads its own copy, and no CTA touches another's memory again.
+        if (pass == 0) cluster_wait();
+        if (tid < CL)
+            st_dsmem_f32x2(&s_tot2[pass][rank], static_cast<uint32_t>(tid), s_total, s_ok);
         cluster_sync();
-        if (tid == 0) s_all_ok = 1;
-        __syncthreads();
-        if (tid < CL) {
-            s_tot[tid] = ld_dsmem_f32(&s_total, static_cast<uint32_t>(tid));
-            if (ld_dsmem_f32(&s_ok, static_cast<uint32_t>(tid)) == 0.0f) s_all_ok = 0;
-        }
-        __syncthreads();
         float R = 0.0f, target_excl = 0.0f;
-        const bool all_ok = s_all_ok != 0;
+        bool all_ok = true;
         int owner = -1, last_rank = -1;
         float tot[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) tot[r] = r < CL ? s_tot[r] : 0.0f;
+        for (int r = 0; r < 8; ++r) {
+            const float2 v = r < CL ? s_tot2[pass][r] : make_float2(0.0f, 1.0f);
+            tot[r] = v.x;
+            all_ok = all_ok && v.y != 0.0f;
+        }
         for (int r = 0; r < CL; ++r) R += tot[r];
         // Residual mass zero on this row: every CTA sees the same R, so the
         // whole cluster takes the fallback pass to p together.
-        if (pass == 0 && (t.mode == 1 || t.mode == 3) && R == 0.0f && all_ok) {
-            cluster_sync();
-            continue;
-        }
+        if (pass == 0 && (t.mode == 1 || t.mode == 3) && R == 0.0f && all_ok) continue;
         const float target = t.w * R;
         {
             float run = 0.0f;
@@ -265,7 +284,6 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         } else if (t.mode != 0 && !all_ok && rank == 0 && tid == 0) {
             a.out_tok[b] = -1;
         }
-        cluster_sync();      // no CTA leaves while its totals may still be read
         break;
     }
 }
