@@ -139,6 +139,10 @@ def test_argument_errors():
     v = bd.Verifier(B, K, G, V, shared_q=True)
     with pytest.raises(bd.SdvError):                       # not 16-byte aligned
         v(w.p_logits, w.q_logits, w.drafts, q_stat=stat[1:])
+    with pytest.raises(ValueError):                        # one entry short
+        v(w.p_logits, w.q_logits, w.drafts, q_stat=stat[:B * G * 4 - 4])
+    with pytest.raises(ValueError):                        # not float32
+        v(w.p_logits, w.q_logits, w.drafts, q_stat=stat[:B * G * 4].double())
     v.close()
     g = bd.Verifier(B, K, G, V, greedy=True)
     with pytest.raises(bd.SdvError):                       # greedy reads no q rows
