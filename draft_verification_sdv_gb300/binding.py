@@ -435,7 +435,7 @@ class Verifier:
                                          dtype=torch.float32, device=dev)
         if q_stat is not None:
             rows_q = B * G if self.shared_q else B * K * G
-            if q_stat.dtype != torch.float32 or q_stat.numel() != rows_q * 4:
+            if not self.greedy and (q_stat.dtype != torch.float32 or q_stat.numel() != rows_q * 4):
                 raise ValueError("q_stat must be float32 with %d x 4 entries (one per q row)"
                                  % rows_q)
             st = sdv_verify_qstat(self.ctx, p_logits, q_logits, drafts, draft_len, q_stat,
