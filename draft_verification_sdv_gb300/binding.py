@@ -421,6 +421,9 @@ class Verifier:
             raise ValueError("drafts must be [B,K,gamma]")
         if p_logits.dtype != self.dtype or (q_logits is not None and q_logits.dtype != self.dtype):
             raise TypeError("logits must be %s" % self.dtype)
+        for name, t in (("temps", temps), ("draft_len", draft_len)):
+            if t is not None and t.numel() != B:
+                raise ValueError("%s must have one entry per sequence (%d)" % (name, B))
         dev = p_logits.device
         if out is None:
             out = {

@@ -143,6 +143,11 @@ def test_argument_errors():
         v(w.p_logits, w.q_logits, w.drafts, q_stat=stat[:B * G * 4 - 4])
     with pytest.raises(ValueError):                        # not float32
         v(w.p_logits, w.q_logits, w.drafts, q_stat=stat[:B * G * 4].double())
+    with pytest.raises(ValueError):                        # per-sequence arrays of B entries
+        v(w.p_logits, w.q_logits, w.drafts, draft_len=torch.zeros(B + 1, dtype=torch.int32,
+                                                                  device="cuda"))
+    with pytest.raises(ValueError):
+        v(w.p_logits, w.q_logits, w.drafts, temps=torch.ones(B - 1, device="cuda"))
     v.close()
     g = bd.Verifier(B, K, G, V, greedy=True)
     with pytest.raises(bd.SdvError):                       # greedy reads no q rows
