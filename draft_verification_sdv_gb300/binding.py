@@ -101,6 +101,13 @@ def _dev_ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _per_seq(t: Optional[torch.Tensor], B: int, name: str) -> None:
+    """A per-sequence array must hold one entry per sequence: the library
+    reads B of them."""
+    if t is not None and t.numel() != B:
+        raise ValueError("%s must have one entry per sequence (%d)" % (name, B))
+
+
 def _host_ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
     if t is None:
         return None
@@ -262,6 +269,7 @@ def sdv_cps(q_marginals, tau: float = 0.8, mmax: int = 15, beam: int = 3, eos_id
     each marginal row's softmax statistics (sdv_cps_ex), which a Verifier call
     takes as `q_stat` so that it does not stream the marginals again."""
     B, G, V = q_marginals.shape
+    _per_seq(temps, B, "temps")
     dev = q_marginals.device
     if out is not None and row_stat and "row_stat" not in out:
         out["row_stat"] = torch.empty((B, G, 4), dtype=torch.float32, device=dev)
@@ -303,6 +311,7 @@ def sdv_cps_prune(q_marginals, tau: float = 0.8, mmax: int = 15, temperature: fl
     """The pruning half of sdv_cps: every row's candidate list (no EOS cut).
     `out` (the dict this returns) may be passed back to reuse its tensors."""
     B, G, V = q_marginals.shape
+    _per_seq(temps, B, "temps")
     out = out if out is not None else _cps_lattice(B, G, mmax, q_marginals.device)
     st = load().sdv_cps_prune(B, G, V, _dtype_code(q_marginals.dtype),
                               ctypes.c_void_p(_stream_handle(stream)),
@@ -361,6 +370,8 @@ class DraftLengthController:
     def step(self, gen_len: torch.Tensor, acc_len: torch.Tensor, stream=None) -> torch.Tensor:
         """Record one step's generated and accepted lengths [B] (int32, on the
         controller's device) and return the next draft lengths (self.k)."""
+        _per_seq(gen_len, self.B, "gen_len")
+        _per_seq(acc_len, self.B, "acc_len")
         g = gen_len.to(torch.int32).contiguous()
         a = acc_len.to(torch.int32).contiguous()
         if self.device.type == "cuda":
@@ -421,9 +432,8 @@ class Verifier:
             raise ValueError("drafts must be [B,K,gamma]")
         if p_logits.dtype != self.dtype or (q_logits is not None and q_logits.dtype != self.dtype):
             raise TypeError("logits must be %s" % self.dtype)
-        for name, t in (("temps", temps), ("draft_len", draft_len)):
-            if t is not None and t.numel() != B:
-                raise ValueError("%s must have one entry per sequence (%d)" % (name, B))
+        _per_seq(temps, B, "temps")
+        _per_seq(draft_len, B, "draft_len")
         dev = p_logits.device
         if out is None:
             out = {

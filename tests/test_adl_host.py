@@ -53,3 +53,14 @@ def test_host_controller_errors():
         st = L.sdv_adl_step_host(1, args["window"], args["kmin"], args["kmax"], args["up"],
                                  args["down"], None, None, None, None)
         assert st == bd.SDV_ERR_ARG, kw
+
+
+def test_per_sequence_arrays_must_have_B_entries():
+    """The library reads B lengths; a shorter or longer array is refused
+    before the call."""
+    ctl = bd.DraftLengthController(3, 4, window=2, kmin=2, kmax=8, device="cpu")
+    with pytest.raises(ValueError):
+        ctl.step(torch.tensor([4, 4]), torch.tensor([4, 4, 4]))
+    with pytest.raises(ValueError):
+        ctl.step(torch.tensor([4, 4, 4]), torch.tensor([4, 4, 4, 4]))
+    assert ctl.k.tolist() == [4, 4, 4]
