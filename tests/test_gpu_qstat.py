@@ -132,6 +132,31 @@ def test_statistics_of_another_temperature_are_a_data_error():
     assert (gpu["sel"][[0, 2, 3]] >= 0).all()
 
 
+def test_non_finite_statistics_are_a_bad_row():
+    """A supplied row whose max or sum is not finite, or whose sum is not
+    positive, is reported like a streamed row holding NaN: that sequence's
+    outputs are -1; the others are those of the same step with the rows
+    streamed."""
+    B, K, G, V = 4, 2, 5, 3000
+    w = _shared(B, K, G, V, seed=67)
+    cps = bd.sdv_cps(w.q_logits, tau=0.8, mmax=8, beam=K, row_stat=True)
+    w.drafts = cps["paths"].clamp(min=0).contiguous()
+    stat = cps["row_stat"].clone()
+    stat[1, 2, 0] = float("nan")                          # sequence 1: NaN max
+    stat[3, 0, 1] = 0.0                                   # sequence 3: zero sum
+    gpu = _verify(w, q_stat=stat)
+    ref = _verify(w)
+    assert gpu["status"] == bd.SDV_ERR_DEVICE_DATA
+    for b in (1, 3):
+        assert gpu["sel"][b] == -1 and gpu["accept_len"][b] == -1 and gpu["next_token"][b] == -1
+    orc = _oracle(w)
+    for b in (0, 2):
+        if orc["band"][b]:
+            continue
+        for k in ("sel", "accept_len", "next_token"):
+            assert gpu[k][b] == ref[k][b], (b, k)
+
+
 def test_argument_errors():
     B, K, G, V = 2, 2, 4, 512
     w = _shared(B, K, G, V, seed=65)
