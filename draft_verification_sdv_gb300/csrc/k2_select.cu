@@ -53,6 +53,42 @@ __device__ __forceinline__ void merge_row(const float2* part, int chunks, float 
     merge_rows2(part, part, chunks, c, M, S, m2, s2);
 }
 
+// Merge the `chunks` partials of up to two rows (pb may be null) with a group
+// of L lanes: lane gl merges chunks gl, gl + L, ... in chunk order, kBatch
+// loads of each row in flight, then the lanes combine by a butterfly of
+// shuffles (every lane of the warp executes it; L is the same for all).  An
+// inactive lane contributes nothing.  With L = 1 this is the plain merge in
+// chunk order.
+__device__ __forceinline__ void group_merge2(const float2* pa, const float2* pb, int chunks, float c,
+                                             int L, int gl, bool active, float& Ma, float& Sa,
+                                             float& Mb, float& Sb) {
+    Ma = Mb = -INFINITY;
+    Sa = Sb = 0.0f;
+    if (active) {
+        for (int i0 = gl; i0 < chunks; i0 += kBatch * L) {
+            float2 va[kBatch], vb[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int ch = i0 + u * L;
+                const bool in = ch < chunks;
+                va[u] = in ? __ldcg(pa + ch) : make_float2(-INFINITY, 0.0f);
+                vb[u] = in && pb ? __ldcg(pb + ch) : make_float2(-INFINITY, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                merge_stat(Ma, Sa, va[u].x, va[u].y, c);
+                merge_stat(Mb, Sb, vb[u].x, vb[u].y, c);
+            }
+        }
+    }
+    for (int off = L >> 1; off > 0; off >>= 1) {
+        const float ma = __shfl_xor_sync(0xffffffffu, Ma, off), sa = __shfl_xor_sync(0xffffffffu, Sa, off);
+        const float mb = __shfl_xor_sync(0xffffffffu, Mb, off), sb = __shfl_xor_sync(0xffffffffu, Sb, off);
+        merge_stat(Ma, Sa, ma, sa, c);
+        merge_stat(Mb, Sb, mb, sb, c);
+    }
+}
+
 __device__ __forceinline__ bool row_valid(float M, float S) {
     return isfinite(M) && isfinite(S) && S > 0.0f;
 }
@@ -62,19 +98,24 @@ __device__ __forceinline__ float row_lse(float M, float S, float c) {
     return (M * c + log2f(S)) * kLn2;
 }
 
-template <bool BF16>
+// GROUPED: rows merged by groups of a.merge_lanes lanes (few rows with many
+// chunks); otherwise one thread per row, bonus rows on the last threads.
+template <bool BF16, bool GROUPED>
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int K = a.K, G = a.G;
     const int KG = K * G;
-    // shared memory: merged row statistics (max, sum) of every p row [K][G+1]
-    // and q row [K][G], the ratios [K][G], the scores [K]
+    // shared memory (select_smem_bytes): merged row statistics (max, sum) of
+    // every p row [K][G+1] and q row [K][G], the ratios [K][RS] (an odd row
+    // stride, so that the score loop's threads, one per draft, read distinct
+    // banks), the scores [K]
+    const int RS = G | 1;
     float2* pstat = reinterpret_cast<float2*>(smem_raw);
     float2* qstat = pstat + K * (G + 1);
     float* ratio = reinterpret_cast<float*>(qstat + KG);
     float* score = reinterpret_cast<float*>(
-        smem_raw + ((static_cast<size_t>(K) * (2 * G + 1) * 8 + static_cast<size_t>(KG) * 4 + 15) &
-                    ~size_t(15)));
+        smem_raw + ((static_cast<size_t>(K) * (2 * G + 1) * 8 + static_cast<size_t>(K) * (G + 1) * 4 +
+                     15) & ~size_t(15)));
     __shared__ unsigned s_bad;
     __shared__ int s_len;
     __shared__ int s_sel;
@@ -94,109 +135,221 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     }
     __syncthreads();
 
-    const int64_t seq_p = static_cast<int64_t>(b) * K * (G + 1);   // first p row of b
     const int64_t seq_d = static_cast<int64_t>(b) * K * G;         // first draft of b
     const int nrow = greedy ? G + 1 : 2 * G + 1;        // LSE entries per draft
 
+    if constexpr (!GROUPED) {
     // The drafted token of this thread's first pair and its two logits are
-    // inputs of the step, not results of the row pass: fetch them before
-    // waiting for the row pass to finish.
-    int32_t x0 = 0;
-    float lp0 = 0.0f, lq0 = 0.0f;
-    if (tid < KG && tid - (tid / G) * G < Lg) {
-        const int k = tid / G, j = tid - (tid / G) * G;
-        x0 = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
-        if (x0 >= 0 && x0 < a.V) {
-            lp0 = load_logit(a.p, p_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
-            if (!greedy) lq0 = load_logit(a.q, q_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
+        // inputs of the step, not results of the row pass: fetch them before
+        // waiting for the row pass to finish.
+        int32_t x0 = 0;
+        float lp0 = 0.0f, lq0 = 0.0f;
+        if (tid < KG && tid - (tid / G) * G < Lg) {
+            const int k = tid / G, j = tid - (tid / G) * G;
+            x0 = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
+            if (x0 >= 0 && x0 < a.V) {
+                lp0 = load_logit(a.p, p_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
+                if (!greedy) lq0 = load_logit(a.q, q_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
+            }
         }
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // Let the sample kernel launch: it waits for this grid before reading.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    // Acceptance ratio at every drafted token of every draft.
-    for (int idx = tid; idx < KG; idx += kSelectThreads) {
-        const int k = idx / G, j = idx - (idx / G) * G;
-        if (j >= Lg) {                                    // past this sequence's drafts
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // Let the sample kernel launch: it waits for this grid before reading.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    
+        // Acceptance ratio at every drafted token of every draft.
+        for (int idx = tid; idx < KG; idx += kSelectThreads) {
+            const int k = idx / G, j = idx - (idx / G) * G;
+            if (j >= Lg) {                                    // past this sequence's drafts
+                if (a.out_lse) {
+                    float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
+                    if (j > Lg) lse[j] = NAN;                 // j == Lg: the bonus row below
+                    if (!greedy) lse[G + 1 + j] = NAN;
+                }
+                continue;
+            }
+            const int64_t rp = p_row_index(a.flags, b, k, j, K, G);
+            const int64_t rq = greedy ? 0 : q_row_index(a.flags, b, k, j, K, G);
+            int32_t x = x0;
+            float lp = lp0, lq = lq0;
+            if (idx != tid) {
+                x = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
+                if (x >= 0 && x < a.V) {
+                    lp = load_logit(a.p, rp * a.V + x, BF16);
+                    if (!greedy) lq = load_logit(a.q, rq * a.V + x, BF16);
+                }
+            }
+            const bool x_ok = x >= 0 && x < a.V;
+            float mp, sp, mq = 0.0f, sq = 1.0f;
+            const float2* prow_part = a.part + rp * a.chunks;
+            if (a.q_stat) {
+                // the drafter row's statistics come from the caller (computed by
+                // the path search at the temperature recorded in them)
+                merge_row(prow_part, a.chunks, c, mp, sp);
+                const float4 st = a.q_stat[rq];
+                mq = st.x;
+                sq = st.y;
+                if (st.z != c) atomicOr(&s_bad, kStatusBadStat);
+            } else {
+                merge_rows2(prow_part, greedy ? prow_part : a.part + (a.rows_p + rq) * a.chunks, a.chunks,
+                            c, mp, sp, mq, sq);
+            }
+            if (greedy) {
+                mq = 0.0f;
+                sq = 1.0f;
+            }
+            pstat[k * (G + 1) + j] = make_float2(mp, sp);
+            qstat[idx] = make_float2(mq, sq);
             if (a.out_lse) {
                 float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
-                if (j > Lg) lse[j] = NAN;                 // j == Lg: the bonus row below
-                if (!greedy) lse[G + 1 + j] = NAN;
+                lse[j] = row_lse(mp, sp, c);
+                if (!greedy) lse[G + 1 + j] = row_lse(mq, sq, c);
             }
-            continue;
+            float r = 0.0f;
+            if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
+                atomicOr(&s_bad, kStatusBadRow);
+            } else if (!x_ok) {
+                atomicOr(&s_bad, kStatusBadDraft);
+            } else if (greedy) {
+                // greedy acceptance: the ratio is the verifier probability p(x)
+                const float d = (lp - mp) * c - log2f(sp);
+                r = d >= 0.0f ? 1.0f : ex2(d);
+            } else if (lq == -INFINITY) {
+                r = 1.0f;                                           // q(x) = 0 <= p(x)
+            } else {
+                const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
+                r = d >= 0.0f ? 1.0f : ex2(d);                      // q <= p accepts at once
+            }
+            ratio[k * RS + j] = r;
         }
-        const int64_t rp = p_row_index(a.flags, b, k, j, K, G);
-        const int64_t rq = greedy ? 0 : q_row_index(a.flags, b, k, j, K, G);
-        int32_t x = x0;
-        float lp = lp0, lq = lq0;
-        if (idx != tid) {
-            x = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
-            if (x >= 0 && x < a.V) {
-                lp = load_logit(a.p, rp * a.V + x, BF16);
-                if (!greedy) lq = load_logit(a.q, rq * a.V + x, BF16);
+        // The bonus rows (j = Lg, right after the last draft token; G for full
+        // drafts): validity and LSE, on the last threads (idle above when K * G
+        // leaves them free).
+        for (int k = kSelectThreads - 1 - tid; k < K; k += kSelectThreads) {
+            const int64_t rp = p_row_index(a.flags, b, k, Lg, K, G);
+            float mp, sp;
+            merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);
+            pstat[k * (G + 1) + Lg] = make_float2(mp, sp);
+            if (a.out_lse) {
+                float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
+                lse[Lg] = row_lse(mp, sp, c);
+                if (Lg < G) lse[G] = NAN;
+            }
+            if (!row_valid(mp, sp)) atomicOr(&s_bad, kStatusBadRow);
+        }
+        __syncthreads();
+    
+    } else {
+    // Rows are merged by groups of L lanes (L = a.merge_lanes, a power of two
+        // up to 32, the same for every CTA): lane i of a group merges chunks i,
+        // i + L, ... in order, then the group combines its lanes by a butterfly.
+        // Items are the K * G pairs (p row and q row of a drafted token), then
+        // the K bonus rows (p at position Lg).  Every thread runs the same number
+        // of rounds, so the butterfly's shuffles see the whole warp.
+        const int L = a.merge_lanes;
+        const int gid = tid / L, gl = tid & (L - 1);
+        const int ngroups = kSelectThreads / L;
+        const int nitems = KG + K;
+    
+        // The drafted token of this group's first pair and its two logits are
+        // inputs of the step, not results of the row pass: fetch them before
+        // waiting for the row pass to finish.
+        int32_t x0 = 0;
+        float lp0 = 0.0f, lq0 = 0.0f;
+        if (gl == 0 && gid < KG && gid - (gid / G) * G < Lg) {
+            const int k = gid / G, j = gid - (gid / G) * G;
+            x0 = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
+            if (x0 >= 0 && x0 < a.V) {
+                lp0 = load_logit(a.p, p_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
+                if (!greedy) lq0 = load_logit(a.q, q_row_index(a.flags, b, k, j, K, G) * a.V + x0, BF16);
             }
         }
-        const bool x_ok = x >= 0 && x < a.V;
-        float mp, sp, mq = 0.0f, sq = 1.0f;
-        const float2* prow_part = a.part + rp * a.chunks;
-        if (a.q_stat) {
-            // the drafter row's statistics come from the caller (computed by
-            // the path search at the temperature recorded in them)
-            merge_row(prow_part, a.chunks, c, mp, sp);
-            const float4 st = a.q_stat[rq];
-            mq = st.x;
-            sq = st.y;
-            if (st.z != c) atomicOr(&s_bad, kStatusBadStat);
-        } else {
-            merge_rows2(prow_part, greedy ? prow_part : a.part + (a.rows_p + rq) * a.chunks, a.chunks,
-                        c, mp, sp, mq, sq);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // Let the sample kernel launch: it waits for this grid before reading.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    
+        for (int base = 0; base < nitems; base += ngroups) {
+            const int item = base + gid;
+            const bool is_pair = item < KG;
+            const bool is_bonus = !is_pair && item < nitems;
+            const int k = is_pair ? item / G : item - KG;
+            const int j = is_pair ? item - k * G : Lg;
+            // a pair past this sequence's drafts reads nothing
+            const bool active = is_bonus || (is_pair && j < Lg);
+            const int64_t rp = active ? p_row_index(a.flags, b, k, j, K, G) : 0;
+            const int64_t rq = is_pair && !greedy ? q_row_index(a.flags, b, k, j, K, G) : 0;
+            const bool merge_q = is_pair && !greedy && !a.q_stat;
+            float mp, sp, mq, sq;
+            group_merge2(a.part + rp * a.chunks, merge_q ? a.part + (a.rows_p + rq) * a.chunks : nullptr,
+                         a.chunks, c, L, gl, active, mp, sp, mq, sq);
+            if (gl != 0) continue;
+            float* lse = a.out_lse ? a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow : nullptr;
+            if (is_bonus) {
+                // the bonus row (j = Lg, right after the last draft token; G for
+                // full drafts): validity and LSE
+                pstat[k * (G + 1) + Lg] = make_float2(mp, sp);
+                if (lse) {
+                    lse[Lg] = row_lse(mp, sp, c);
+                    if (Lg < G) lse[G] = NAN;
+                }
+                if (!row_valid(mp, sp)) atomicOr(&s_bad, kStatusBadRow);
+                continue;
+            }
+            if (!is_pair) continue;
+            if (!active) {                                    // past this sequence's drafts
+                if (lse) {
+                    if (j > Lg) lse[j] = NAN;                 // j == Lg: the bonus row
+                    if (!greedy) lse[G + 1 + j] = NAN;
+                }
+                continue;
+            }
+            // acceptance ratio at the drafted token
+            int32_t x = x0;
+            float lp = lp0, lq = lq0;
+            if (item != gid) {
+                x = a.drafts[seq_d + static_cast<int64_t>(k) * G + j];
+                if (x >= 0 && x < a.V) {
+                    lp = load_logit(a.p, rp * a.V + x, BF16);
+                    if (!greedy) lq = load_logit(a.q, rq * a.V + x, BF16);
+                }
+            }
+            const bool x_ok = x >= 0 && x < a.V;
+            if (greedy) {
+                mq = 0.0f;
+                sq = 1.0f;
+            } else if (a.q_stat) {
+                // the drafter row's statistics come from the caller (computed by
+                // the path search at the temperature recorded in them)
+                const float4 st = a.q_stat[rq];
+                mq = st.x;
+                sq = st.y;
+                if (st.z != c) atomicOr(&s_bad, kStatusBadStat);
+            }
+            pstat[k * (G + 1) + j] = make_float2(mp, sp);
+            qstat[item] = make_float2(mq, sq);
+            if (lse) {
+                lse[j] = row_lse(mp, sp, c);
+                if (!greedy) lse[G + 1 + j] = row_lse(mq, sq, c);
+            }
+            float r = 0.0f;
+            if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
+                atomicOr(&s_bad, kStatusBadRow);
+            } else if (!x_ok) {
+                atomicOr(&s_bad, kStatusBadDraft);
+            } else if (greedy) {
+                // greedy acceptance: the ratio is the verifier probability p(x)
+                const float d = (lp - mp) * c - log2f(sp);
+                r = d >= 0.0f ? 1.0f : ex2(d);
+            } else if (lq == -INFINITY) {
+                r = 1.0f;                                           // q(x) = 0 <= p(x)
+            } else {
+                const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
+                r = d >= 0.0f ? 1.0f : ex2(d);                      // q <= p accepts at once
+            }
+            ratio[k * RS + j] = r;
         }
-        if (greedy) {
-            mq = 0.0f;
-            sq = 1.0f;
-        }
-        pstat[k * (G + 1) + j] = make_float2(mp, sp);
-        qstat[idx] = make_float2(mq, sq);
-        if (a.out_lse) {
-            float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
-            lse[j] = row_lse(mp, sp, c);
-            if (!greedy) lse[G + 1 + j] = row_lse(mq, sq, c);
-        }
-        float r = 0.0f;
-        if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
-            atomicOr(&s_bad, kStatusBadRow);
-        } else if (!x_ok) {
-            atomicOr(&s_bad, kStatusBadDraft);
-        } else if (greedy) {
-            // greedy acceptance: the ratio is the verifier probability p(x)
-            const float d = (lp - mp) * c - log2f(sp);
-            r = d >= 0.0f ? 1.0f : ex2(d);
-        } else if (lq == -INFINITY) {
-            r = 1.0f;                                           // q(x) = 0 <= p(x)
-        } else {
-            const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
-            r = d >= 0.0f ? 1.0f : ex2(d);                      // q <= p accepts at once
-        }
-        ratio[idx] = r;
+        __syncthreads();
+    
     }
-    // The bonus rows (j = Lg, right after the last draft token; G for full
-    // drafts): validity and LSE, on the last threads (idle above when K * G
-    // leaves them free).
-    for (int k = kSelectThreads - 1 - tid; k < K; k += kSelectThreads) {
-        const int64_t rp = p_row_index(a.flags, b, k, Lg, K, G);
-        float mp, sp;
-        merge_row(a.part + rp * a.chunks, a.chunks, c, mp, sp);
-        pstat[k * (G + 1) + Lg] = make_float2(mp, sp);
-        if (a.out_lse) {
-            float* lse = a.out_lse + (static_cast<int64_t>(b) * K + k) * nrow;
-            lse[Lg] = row_lse(mp, sp, c);
-            if (Lg < G) lse[G] = NAN;
-        }
-        if (!row_valid(mp, sp)) atomicOr(&s_bad, kStatusBadRow);
-    }
-    __syncthreads();
-
     if (s_bad) {
         if (tid == 0) {
             a.out_sel[b] = -1;
@@ -216,7 +369,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     for (int k = tid; k < K; k += kSelectThreads) {
         float prefix = 1.0f, sc = 0.0f;
         for (int j = 0; j < Lg; ++j) {
-            prefix *= ratio[k * G + j];
+            prefix *= ratio[k * RS + j];
             sc += prefix;
         }
         score[k] = sc;
@@ -224,12 +377,29 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     }
     __syncthreads();
 
-    // Self-selection: first draft with the largest expected streak.
-    if (tid == 0) {
-        int best = 0;
-        for (int k = 1; k < K; ++k)
-            if (score[k] > score[best]) best = k;
-        s_sel = best;
+    // Self-selection: first draft with the largest expected streak (warp 0:
+    // each lane the first maximum of its drafts, then a butterfly that keeps
+    // the larger score, on equal scores the lower k).
+    if (tid < 32) {
+        float best = -INFINITY;
+        int bk = K;
+        for (int k = tid; k < K; k += 32) {
+            const float sc = score[k];
+            if (bk == K || sc > best) {
+                best = sc;
+                bk = k;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+            const int ok = __shfl_xor_sync(0xffffffffu, bk, off);
+            if (ok < K && (bk == K || ob > best || (ob == best && ok < bk))) {
+                best = ob;
+                bk = ok;
+            }
+        }
+        if (tid == 0) s_sel = bk;
     }
     __syncthreads();
     const int sel = s_sel;
@@ -239,7 +409,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u, 0u),
                                       a.seed_lo, a.seed_hi);
         const float u = uniform24(r.x);
-        const float aj = ratio[sel * G + j];
+        const float aj = ratio[sel * RS + j];
         const bool accepted = (aj >= 1.0f) || (u < aj);
         if (!accepted) atomicMin(&s_len, j);
     }
@@ -279,11 +449,16 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
 }  // namespace
 
 cudaError_t setup_select(size_t smem) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem));
+    const int n = static_cast<int>(smem);
+    cudaError_t e = cudaFuncSetAttribute(select_kernel<true, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, n);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(select_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, n);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(select_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, n);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(select_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, n);
+    return e;
 }
 
 cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s, bool pdl) {
@@ -297,8 +472,11 @@ cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStrea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (bf16) return cudaLaunchKernelEx(&cfg, select_kernel<true>, a);
-    return cudaLaunchKernelEx(&cfg, select_kernel<false>, a);
+    const bool grouped = a.merge_lanes > 1;
+    if (bf16) return grouped ? cudaLaunchKernelEx(&cfg, select_kernel<true, true>, a)
+                             : cudaLaunchKernelEx(&cfg, select_kernel<true, false>, a);
+    return grouped ? cudaLaunchKernelEx(&cfg, select_kernel<false, true>, a)
+                   : cudaLaunchKernelEx(&cfg, select_kernel<false, false>, a);
 }
 
 }  // namespace sdv

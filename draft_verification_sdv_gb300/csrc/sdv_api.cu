@@ -139,9 +139,7 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
     ctx->rp_grid = static_cast<int>((ctx->items + (kRowPassThreads / 32) - 1) / (kRowPassThreads / 32));
 
     // Select plan.
-    ctx->sel_smem = align_up(static_cast<size_t>(K) * (2 * gamma + 1) * 8 +
-                                 static_cast<size_t>(K) * gamma * 4, 16) +
-                    static_cast<size_t>(K) * 4;
+    ctx->sel_smem = select_smem_bytes(K, gamma);
     // Sample plan: up to 8 CTAs per sequence, each holding a slice of one or
     // two rows in shared memory.
     int cl = 8;
@@ -282,6 +280,7 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     sa.status = ctx->status;
     sa.lens = draft_len;
     sa.q_stat = reinterpret_cast<const float4*>(q_row_stat);
+    sa.merge_lanes = select_merge_lanes(ctx->K, ctx->G, ctx->chunks);
     e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "select launch");
     if (ev) cudaEventRecord(ev[2], ctx->stream);

@@ -143,6 +143,9 @@ struct SelectArgs {
     SeqTask* tasks;
     unsigned* status;
     const int32_t* lens = nullptr;   // [B] draft length per sequence, or nullptr (= G)
+    // lanes that merge one row's chunk partials together: a power of two,
+    // at most 32 (select_merge_lanes)
+    int merge_lanes = 1;
     // [rows_q] drafter-row statistics {max, sum 2^{(l - max) c}, c, 0} given by
     // the caller (the path search's pruning pass writes them), or nullptr to
     // merge the row pass's partials of the q rows
@@ -249,6 +252,27 @@ inline void plan_rowpass_chunks(int64_t rows, int64_t nvec, int64_t resident_war
     *chunks = static_cast<int>((nvec + cv - 1) / cv);
 }
 constexpr int kSelectThreads = 512;
+
+// Dynamic shared memory of the select kernel for K drafts of G tokens: row
+// statistics [K][2G+1] float2, ratios [K][G+1] float, then (16-byte
+// aligned) the scores [K] float.
+inline size_t select_smem_bytes(int K, int G) {
+    const size_t head = static_cast<size_t>(K) * (2 * G + 1) * 8 + static_cast<size_t>(K) * (G + 1) * 4;
+    return ((head + 15) & ~size_t(15)) + static_cast<size_t>(K) * 4;
+}
+
+// Lanes per row merge in the select kernel: the largest power of two up to
+// 32, and up to the chunk count, for which the K * G pairs and K bonus rows
+// of a sequence all fit the CTA's threads in one round.  Few rows with many
+// chunks each (the latency cases) get whole warps; the large batches keep
+// one thread per row.
+inline int select_merge_lanes(int K, int G, int chunks) {
+    const int64_t items = static_cast<int64_t>(K) * G + K;
+    int lanes = 1;
+    while (lanes < 32 && lanes < chunks && items * (2 * lanes) <= kSelectThreads) lanes *= 2;
+    return lanes;
+}
+
 constexpr int kSampleThreads = 512;
 
 }  // namespace sdv

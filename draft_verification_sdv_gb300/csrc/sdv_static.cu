@@ -128,9 +128,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     int cl = 8;
     while (cl > 1 && cl > nvec) cl >>= 1;
     const int64_t slice_vec = (nvec + cl - 1) / cl;
-    const size_t sel_smem = round_up(static_cast<size_t>(K) * (2 * gamma + 1) * 8 +
-                                         static_cast<size_t>(K) * gamma * 4, 16) +
-                            static_cast<size_t>(K) * 4;
+    const size_t sel_smem = select_smem_bytes(K, gamma);
     const size_t smp_smem = static_cast<size_t>(2) * slice_vec * 16;
     if (sel_smem > static_cast<size_t>(sd->smem_optin) - 4096 ||
         smp_smem > static_cast<size_t>(sd->smem_optin) - 4096)
@@ -173,6 +171,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     sa.G = gamma;
     sa.V = V;
     sa.chunks = chunks;
+    sa.merge_lanes = select_merge_lanes(K, gamma, chunks);
     sa.flags = 0u;
     sa.rows_p = rows_p;
     sa.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
