@@ -98,6 +98,45 @@ __device__ __forceinline__ float row_lse(float M, float S, float c) {
     return (M * c + log2f(S)) * kLn2;
 }
 
+// The drafter row's statistics of a pair: none under greedy acceptance, the
+// caller's when supplied (an entry of another temperature is a data error),
+// else those merged from the row pass's partials (left as they are).
+__device__ __forceinline__ void pair_q_stat(const SelectArgs& a, bool greedy, int64_t rq, float c,
+                                            float& mq, float& sq, unsigned* bad) {
+    if (greedy) {
+        mq = 0.0f;
+        sq = 1.0f;
+    } else if (a.q_stat) {
+        const float4 st = a.q_stat[rq];
+        mq = st.x;
+        sq = st.y;
+        if (st.z != c) atomicOr(bad, kStatusBadStat);
+    }
+}
+
+// Acceptance ratio of a drafted token from its two logits and the rows'
+// statistics: p(x) under greedy acceptance, else min(1, p/q) in
+// exact-difference log form.  A bad row or token id sets its flag; the ratio
+// is then 0 and unused.
+__device__ __forceinline__ float pair_ratio(bool greedy, bool x_ok, float lp, float lq, float mp,
+                                            float sp, float mq, float sq, float c, unsigned* bad) {
+    if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
+        atomicOr(bad, kStatusBadRow);
+        return 0.0f;
+    }
+    if (!x_ok) {
+        atomicOr(bad, kStatusBadDraft);
+        return 0.0f;
+    }
+    if (greedy) {
+        const float d = (lp - mp) * c - log2f(sp);
+        return d >= 0.0f ? 1.0f : ex2(d);
+    }
+    if (lq == -INFINITY) return 1.0f;                       // q(x) = 0 <= p(x)
+    const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
+    return d >= 0.0f ? 1.0f : ex2(d);                       // q <= p accepts at once
+}
+
 // GROUPED: rows merged by groups of a.merge_lanes lanes (few rows with many
 // chunks); otherwise one thread per row, bonus rows on the last threads.
 template <bool BF16, bool GROUPED>
@@ -139,7 +178,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     const int nrow = greedy ? G + 1 : 2 * G + 1;        // LSE entries per draft
 
     if constexpr (!GROUPED) {
-    // The drafted token of this thread's first pair and its two logits are
+        // The drafted token of this thread's first pair and its two logits are
         // inputs of the step, not results of the row pass: fetch them before
         // waiting for the row pass to finish.
         int32_t x0 = 0;
@@ -155,7 +194,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         asm volatile("griddepcontrol.wait;" ::: "memory");
         // Let the sample kernel launch: it waits for this grid before reading.
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    
+
         // Acceptance ratio at every drafted token of every draft.
         for (int idx = tid; idx < KG; idx += kSelectThreads) {
             const int k = idx / G, j = idx - (idx / G) * G;
@@ -181,22 +220,11 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
             const bool x_ok = x >= 0 && x < a.V;
             float mp, sp, mq = 0.0f, sq = 1.0f;
             const float2* prow_part = a.part + rp * a.chunks;
-            if (a.q_stat) {
-                // the drafter row's statistics come from the caller (computed by
-                // the path search at the temperature recorded in them)
+            if (greedy || a.q_stat)
                 merge_row(prow_part, a.chunks, c, mp, sp);
-                const float4 st = a.q_stat[rq];
-                mq = st.x;
-                sq = st.y;
-                if (st.z != c) atomicOr(&s_bad, kStatusBadStat);
-            } else {
-                merge_rows2(prow_part, greedy ? prow_part : a.part + (a.rows_p + rq) * a.chunks, a.chunks,
-                            c, mp, sp, mq, sq);
-            }
-            if (greedy) {
-                mq = 0.0f;
-                sq = 1.0f;
-            }
+            else
+                merge_rows2(prow_part, a.part + (a.rows_p + rq) * a.chunks, a.chunks, c, mp, sp, mq, sq);
+            pair_q_stat(a, greedy, rq, c, mq, sq, &s_bad);
             pstat[k * (G + 1) + j] = make_float2(mp, sp);
             qstat[idx] = make_float2(mq, sq);
             if (a.out_lse) {
@@ -204,22 +232,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
                 lse[j] = row_lse(mp, sp, c);
                 if (!greedy) lse[G + 1 + j] = row_lse(mq, sq, c);
             }
-            float r = 0.0f;
-            if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
-                atomicOr(&s_bad, kStatusBadRow);
-            } else if (!x_ok) {
-                atomicOr(&s_bad, kStatusBadDraft);
-            } else if (greedy) {
-                // greedy acceptance: the ratio is the verifier probability p(x)
-                const float d = (lp - mp) * c - log2f(sp);
-                r = d >= 0.0f ? 1.0f : ex2(d);
-            } else if (lq == -INFINITY) {
-                r = 1.0f;                                           // q(x) = 0 <= p(x)
-            } else {
-                const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
-                r = d >= 0.0f ? 1.0f : ex2(d);                      // q <= p accepts at once
-            }
-            ratio[k * RS + j] = r;
+            ratio[k * RS + j] = pair_ratio(greedy, x_ok, lp, lq, mp, sp, mq, sq, c, &s_bad);
         }
         // The bonus rows (j = Lg, right after the last draft token; G for full
         // drafts): validity and LSE, on the last threads (idle above when K * G
@@ -237,7 +250,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
             if (!row_valid(mp, sp)) atomicOr(&s_bad, kStatusBadRow);
         }
         __syncthreads();
-    
+
     } else {
     // Rows are merged by groups of L lanes (L = a.merge_lanes, a power of two
         // up to 32, the same for every CTA): lane i of a group merges chunks i,
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         const int gid = tid / L, gl = tid & (L - 1);
         const int ngroups = kSelectThreads / L;
         const int nitems = KG + K;
-    
+
         // The drafted token of this group's first pair and its two logits are
         // inputs of the step, not results of the row pass: fetch them before
         // waiting for the row pass to finish.
@@ -266,7 +279,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
         asm volatile("griddepcontrol.wait;" ::: "memory");
         // Let the sample kernel launch: it waits for this grid before reading.
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    
+
         for (int base = 0; base < nitems; base += ngroups) {
             const int item = base + gid;
             const bool is_pair = item < KG;
@@ -313,42 +326,17 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
                 }
             }
             const bool x_ok = x >= 0 && x < a.V;
-            if (greedy) {
-                mq = 0.0f;
-                sq = 1.0f;
-            } else if (a.q_stat) {
-                // the drafter row's statistics come from the caller (computed by
-                // the path search at the temperature recorded in them)
-                const float4 st = a.q_stat[rq];
-                mq = st.x;
-                sq = st.y;
-                if (st.z != c) atomicOr(&s_bad, kStatusBadStat);
-            }
+            pair_q_stat(a, greedy, rq, c, mq, sq, &s_bad);
             pstat[k * (G + 1) + j] = make_float2(mp, sp);
             qstat[item] = make_float2(mq, sq);
             if (lse) {
                 lse[j] = row_lse(mp, sp, c);
                 if (!greedy) lse[G + 1 + j] = row_lse(mq, sq, c);
             }
-            float r = 0.0f;
-            if (!row_valid(mp, sp) || !row_valid(mq, sq)) {
-                atomicOr(&s_bad, kStatusBadRow);
-            } else if (!x_ok) {
-                atomicOr(&s_bad, kStatusBadDraft);
-            } else if (greedy) {
-                // greedy acceptance: the ratio is the verifier probability p(x)
-                const float d = (lp - mp) * c - log2f(sp);
-                r = d >= 0.0f ? 1.0f : ex2(d);
-            } else if (lq == -INFINITY) {
-                r = 1.0f;                                           // q(x) = 0 <= p(x)
-            } else {
-                const float d = ((lp - mp) - (lq - mq)) * c - log2f(sp / sq);
-                r = d >= 0.0f ? 1.0f : ex2(d);                      // q <= p accepts at once
-            }
-            ratio[k * RS + j] = r;
+            ratio[k * RS + j] = pair_ratio(greedy, x_ok, lp, lq, mp, sp, mq, sq, c, &s_bad);
         }
         __syncthreads();
-    
+
     }
     if (s_bad) {
         if (tid == 0) {
