@@ -205,13 +205,4 @@ __device__ __forceinline__ void cluster_sync() {
                      : "memory");
 }
 
-// Read a float from the shared memory of CTA `rank` of this cluster.
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 }  // namespace sdv
