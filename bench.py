@@ -67,6 +67,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the bench workload alone (no per_config block)")
     return ap.parse_args()
 
 
@@ -226,6 +228,93 @@ def step_bytes(w: synth.Workload, accept_len, greedy: bool = False,
 # the CUDA path
 # ---------------------------------------------------------------------------
 
+def measure_verify(bd, w: synth.Workload, args, stream, greedy: bool = False,
+                   prefix_row: bool = False, world: int = 1, steps: int = None) -> dict:
+    """Time `steps` verification steps of workload w on `stream` (CUDA events),
+    then a second pass with per-kernel events.  Inputs smaller than twice the
+    L2 would stay cached from one step to the next: then the L2 is flushed (a
+    write larger than it) before every step, outside the timed region, and
+    each step is timed alone."""
+    dev = w.p_logits.device
+    steps = args.steps if steps is None else steps
+    # the inputs were made on torch's current stream; the steps run on
+    # `stream` (non-blocking): order them after the inputs
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
+    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q,
+                    greedy=greedy, shared_prefix_row=prefix_row)
+    out = None
+
+    def step():
+        nonlocal out
+        out = v(w.p_logits, None if greedy else w.q_logits, w.drafts, temperature=w.temperature,
+                seed=w.seed, temps=w.temps, out=out)
+
+    for _ in range(max(args.warmup, 3) if args.warmup > 0 else 0):
+        step()
+    v.sync()
+    torch.cuda.synchronize()
+    barrier(world)
+    sb0 = step_bytes(w, [w.gamma] * w.B, greedy=greedy, shared_prefix_row=prefix_row)
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
+    flush_buf = None
+    if sb0["k1"] < 2 * l2_bytes:
+        flush_buf = torch.empty(max(2 * l2_bytes, 256 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def flush():
+        if flush_buf is not None:
+            with torch.cuda.stream(stream):
+                flush_buf.zero_()
+
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.time()
+    if flush_buf is None:
+        # K steps back to back on the context's stream, nothing between the
+        # kernels (the select and sample kernels launch as programmatic
+        # dependents of the kernel before them).
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_total = ev0.elapsed_time(ev1)
+    else:
+        pairs = []
+        for _ in range(steps):
+            flush()
+            e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e_a.record(stream)
+            step()
+            e_b.record(stream)
+            pairs.append((e_a, e_b))
+        torch.cuda.synchronize()
+        ms_total = sum(e_a.elapsed_time(e_b) for e_a, e_b in pairs)
+    t1 = time.time()
+    barrier(world)
+    # Second pass of K steps with CUDA events around each kernel (the events
+    # serialise the kernels): per-kernel durations for the roofline.
+    bd.sdv_profile_enable(v.ctx, True)
+    for _ in range(steps):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    bd.sdv_profile_enable(v.ctx, False)
+    v.sync()
+    ms_kernels, nprof = bd.sdv_profile_read(v.ctx)
+    accept_len = out["accept_len"].cpu().tolist()
+    l2 = ("inputs %.2f GB > L2 (%d MB): no flush" % (sb0["k1"] / 1e9, l2_bytes >> 20)
+          if flush_buf is None else
+          "inputs %.4f GB < 2x L2 (%d MB): L2 flushed by a %d MB write before every step, "
+          "outside the timed region; each step timed alone"
+          % (sb0["k1"] / 1e9, l2_bytes >> 20, flush_buf.numel() * 4 >> 20))
+    del flush_buf
+    return {"verifier": v, "out": out, "ms_total": ms_total, "steps": steps, "t0": t0, "t1": t1,
+            "ms_kernels": ms_kernels, "nprof": nprof, "accept_len": accept_len, "l2": l2,
+            "flushed": sb0["k1"] < 2 * l2_bytes}
+
+
 def run_sdv(args, rank, world, local):
     from draft_verification_sdv_gb300 import binding as bd
     bd.load(build=True)
@@ -237,82 +326,17 @@ def run_sdv(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
     # drafts from one pass's marginals also share the prefix row (j = 0)
     prefix_row = bool(w.shared_q)
-    v = bd.Verifier(w.B, w.K, w.gamma, w.V, w.dtype, stream=stream, shared_q=w.shared_q,
-                    greedy=args.greedy, shared_prefix_row=prefix_row)
     if args.greedy:
         w.q_logits = None
         torch.cuda.empty_cache()
-    out = None
-
-    def step():
-        nonlocal out
-        out = v(w.p_logits, w.q_logits, w.drafts, temperature=w.temperature, seed=w.seed,
-                temps=w.temps, out=out)
-
-    for _ in range(max(args.warmup, 3) if args.warmup > 0 else 0):
-        step()
-    v.sync()
-    torch.cuda.synchronize()
-    barrier(world)
-
-    # Inputs smaller than twice the L2 would stay cached from one step to the
-    # next: then the L2 is flushed (a write larger than it) before every step,
-    # outside the timed region, and each step is timed alone.
-    sb0 = step_bytes(w, [w.gamma] * w.B, greedy=args.greedy, shared_prefix_row=prefix_row)
-    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
-    flush_buf = None
-    if sb0["k1"] < 2 * l2_bytes:
-        flush_buf = torch.empty(max(2 * l2_bytes, 256 << 20) // 4, dtype=torch.int32, device=dev)
-
-    def flush():
-        if flush_buf is not None:
-            with torch.cuda.stream(stream):
-                flush_buf.zero_()
 
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.25)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.time()
-    if flush_buf is None:
-        # Timed region: K steps back to back on the context's stream, nothing
-        # between the kernels (the select and sample kernels launch as
-        # programmatic dependents of the kernel before them).
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        ms_total = ev0.elapsed_time(ev1)
-    else:
-        pairs = []
-        for _ in range(args.steps):
-            flush()
-            e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e_a.record(stream)
-            step()
-            e_b.record(stream)
-            pairs.append((e_a, e_b))
-        torch.cuda.synchronize()
-        ms_total = sum(e_a.elapsed_time(e_b) for e_a, e_b in pairs)
-    t1 = time.time()
-    barrier(world)
-    # Second timed pass of K steps with CUDA events around each kernel (the
-    # events serialise the kernels): per-kernel durations for the roofline.
-    bd.sdv_profile_enable(v.ctx, True)
-    for _ in range(args.steps):
-        flush()
-        step()
-    torch.cuda.synchronize()
-    bd.sdv_profile_enable(v.ctx, False)
-    time.sleep(0.2)
-    clocks.stop()
-    v.sync()
-    ms_kernels, nprof = bd.sdv_profile_read(v.ctx)
-    ms_max = max_over_ranks(ms_total, world)
-    accept_len = out["accept_len"].cpu().tolist()
+    m = measure_verify(bd, w, args, stream, greedy=args.greedy, prefix_row=prefix_row, world=world)
+    v, out = m["verifier"], m["out"]
+    ms_kernels, nprof, accept_len = m["ms_kernels"], m["nprof"], m["accept_len"]
+    ms_max = max_over_ranks(m["ms_total"], world)
     tokens_per_step = w.B * w.K * w.gamma
     value = world * tokens_per_step * args.steps / (ms_max / 1e3)
     ms_step = ms_max / args.steps
@@ -352,11 +376,7 @@ def run_sdv(args, rank, world, local):
                                 "[B,gamma,V] shared by the K drafts" if w.shared_q else "[B,K,gamma,V]"),
                    "prefix_row": "one per sequence" if prefix_row else "one per draft",
                    "temperatures": "per-sequence {0.6, 1.0}" if w.temps is not None else w.temperature,
-                   "l2": ("inputs %.2f GB > L2 (%d MB): no flush" % (sb["k1"] / 1e9, l2_bytes >> 20)
-                          if flush_buf is None else
-                          "inputs %.4f GB < 2x L2 (%d MB): L2 flushed by a %d MB write before "
-                          "every step, outside the timed region; each step timed alone"
-                          % (sb["k1"] / 1e9, l2_bytes >> 20, flush_buf.numel() * 4 >> 20)),
+                   "l2": m["l2"],
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "1 GPU"},
         "committed_tokens_per_s": world * sum(int(L) + 1 for L in accept_len) * args.steps / (ms_max / 1e3),
         "hbm": {"step_gbs": round(step_gbs, 1), "frac": round(step_gbs / peak, 4),
@@ -366,7 +386,7 @@ def run_sdv(args, rank, world, local):
                                                "each kernel on the context stream"},
         "roofline": roofline,
         "gpu_launches": 3 * args.steps,      # in the timed region (row pass, select, sample)
-        "clocks": clocks.summary(t0, t1),
+        "clocks": clocks.summary(m["t0"], m["t1"]),
     }
 
     # End to end through the host-buffer entry point: inputs copied from pinned
@@ -397,20 +417,86 @@ def run_sdv(args, rank, world, local):
                          "steps": args.e2e_steps, "ms_per_step": te * 1e3 / args.e2e_steps}
         del hp, hq
 
-    # The oracle as it stands on the host cores, bounded sample (rank 0, N = 1).
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.greedy:
-        result["cpu_baseline"] = cpu_baseline(w)
+    # The outputs of the timed step again, with scores and row LSE, for the
+    # parity check of the cpu_baseline leg.
+    gpu = v(w.p_logits, None if args.greedy else w.q_logits, w.drafts, temperature=w.temperature,
+            seed=w.seed, temps=w.temps, scores=True, lse=True)
+    v.sync()
+    gpu = {k: t.cpu().numpy() for k, t in gpu.items()}
     v.close()
+
+    # The oracle as it stands on the host cores, bounded sample (rank 0, N = 1),
+    # and its parity with the GPU's outputs on the same sequences.
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.greedy:
+        result["cpu_baseline"], result["parity"] = cpu_baseline(w, gpu)
+
+    # The other workloads, timed in the same run (single-GPU line only).
+    if (rank == 0 and world == 1 and not args.no_per_config and not args.greedy and
+            not args.shared_q and args.batch is None and args.workload == DEFAULT_WORKLOAD):
+        del w
+        torch.cuda.empty_cache()
+        result["per_config"] = per_config(bd, args, stream, clocks, peak, peak_kind)
+    time.sleep(0.2)
+    clocks.stop()
     return result
 
 
-def run_cps(args, rank, world):
+def per_config(bd, args, stream, clocks, peak, peak_kind) -> dict:
+    """Workloads 1-4 (the tiny exact case and the single stream as latencies
+    with the L2 flushed before every step; the self-selection sweep and the
+    serving batch as throughput), the whole decode step and the path search,
+    each timed as its own line would time it, with the clocks of its window."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    res = {}
+    for idx in (1, 2, 3, 4):
+        w = synth.workload(idx, device=dev, seed=idx)
+        m = measure_verify(bd, w, args, stream)
+        m["verifier"].close()
+        ms = m["ms_total"] / m["steps"]
+        sb = step_bytes(w, m["accept_len"])
+        k1 = m["ms_kernels"][0]
+        e = {"workload": w.name, "ms_per_step": ms,
+             "draft_tokens_per_s": w.B * w.K * w.gamma / (ms * 1e-3),
+             "kernel_ms": {"rowpass": k1, "select": m["ms_kernels"][1],
+                           "sample": m["ms_kernels"][2]},
+             "l2": m["l2"], "clocks": clocks.summary(m["t0"], m["t1"])}
+        if not m["flushed"]:
+            rp = sb["k1"] / (k1 * 1e-3) / 1e9
+            st = sb["total"] / (ms * 1e-3) / 1e9
+            e.update({"rowpass_gbs": round(rp, 1), "rowpass_frac": round(rp / peak, 4),
+                      "step_gbs": round(st, 1), "step_frac": round(st / peak, 4),
+                      "peak": peak, "peak_kind": peak_kind})
+        else:
+            e["latency_us"] = round(ms * 1e3, 2)
+        res[str(idx)] = e
+        del w, m
+        torch.cuda.empty_cache()
+    ds = run_decode_step(args, 0, 1, bd=bd, clocks=clocks)
+    res["decode_step"] = {"workload": ds["config"]["workload"], "ms_per_step": ds["ms_per_step"],
+                          "sequence_steps_per_s": ds["value"], "step_gbs": ds["hbm"]["step_gbs"],
+                          "step_frac": ds["hbm"]["frac"], "peak_kind": ds["hbm"]["peak_kind"],
+                          "clocks": ds["clocks"]}
+    torch.cuda.empty_cache()
+    cps_args = argparse.Namespace(**vars(args))
+    cps_args.no_e2e = True
+    cps_args.no_cpu_baseline = True
+    cp = run_cps(cps_args, 0, 1, bd=bd, clocks=clocks)
+    res["path_search"] = {"workload": cp["config"]["workload"], "ms_per_step": cp["ms_per_step"],
+                          "rows_per_s": cp["value"], "kernel_ms": cp["kernel_ms"],
+                          "prune_gbs": cp["roofline"]["achieved"], "prune_frac": cp["roofline"]["frac"],
+                          "clocks": cp["clocks"]}
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_cps(args, rank, world, bd=None, clocks=None):
     """Path search over the drafter marginals of the large-window shape
     (B 32, gamma 32, V 152064 bf16, per-sequence temperatures): beam 3, at most
     15 candidates, mass 0.8.  One step = sdv_cps (pruning of every row, then
     the beam).  The q rows (311 MB) exceed the L2, so no flush is needed."""
-    from draft_verification_sdv_gb300 import binding as bd
-    bd.load(build=True)
+    if bd is None:
+        from draft_verification_sdv_gb300 import binding as bd
+        bd.load(build=True)
     dev = torch.device("cuda", torch.cuda.current_device())
     w = synth.workload_shared(B=args.batch or 32, device=dev, seed=55 + 1000 * rank)
     q, temps = w.q_logits, w.temps
@@ -438,9 +524,11 @@ def run_cps(args, rank, world):
         step()
     torch.cuda.synchronize()
     barrier(world)
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    time.sleep(0.25)
+    own_clocks = clocks is None
+    if own_clocks:
+        clocks = ClockSampler(dev.index)
+        clocks.start()
+        time.sleep(0.25)
     barrier(world)
     t0 = time.time()
     ms = timed(step, args.steps)
@@ -451,8 +539,9 @@ def run_cps(args, rank, world):
     ms_prune = timed(lambda: bd.sdv_cps_prune(q, tau, mmax, temps=temps, out=lat), args.steps)
     paths_out = dict(out)
     ms_beam = timed(lambda: bd.sdv_cps_beam(lat, V, beam, out=paths_out), args.steps)
-    time.sleep(0.2)
-    clocks.stop()
+    if own_clocks:
+        time.sleep(0.2)
+        clocks.stop()
     row_bytes = q.numel() * q.element_size()
     peak, kind = measured_peaks()
     gbs = row_bytes / (ms_prune * 1e-3) / 1e9
@@ -526,7 +615,7 @@ ARM_PARTS = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "A
              "0xd49": "Arm Neoverse-N2"}
 
 
-def run_decode_step(args, rank, world):
+def run_decode_step(args, rank, world, bd=None, clocks=None):
     """One decode step of a diffusion drafter's pass, end to end on the GPU:
     the path search over the marginals q [B, gamma, V] (beam 3, 15
     candidates, mass 0.8, EOS cut), verification of the beam's K = 3 paths at
@@ -535,8 +624,9 @@ def run_decode_step(args, rank, world):
     search hands the marginal rows' softmax statistics to the verification,
     which therefore streams only the verifier rows.  Large-window shape: B 32,
     gamma 32, V 152064 bf16, per-sequence temperatures."""
-    from draft_verification_sdv_gb300 import binding as bd
-    bd.load(build=True)
+    if bd is None:
+        from draft_verification_sdv_gb300 import binding as bd
+        bd.load(build=True)
     dev = torch.device("cuda", torch.cuda.current_device())
     B, K, G, V = args.batch or 32, 3, 32, synth.QWEN_VOCAB
     g = torch.Generator(device="cpu")
@@ -563,9 +653,11 @@ def run_decode_step(args, rank, world):
     torch.cuda.synchronize()
     v.sync()
     barrier(world)
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    time.sleep(0.25)
+    own_clocks = clocks is None
+    if own_clocks:
+        clocks = ClockSampler(dev.index)
+        clocks.start()
+        time.sleep(0.25)
     stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -576,8 +668,9 @@ def run_decode_step(args, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
-    time.sleep(0.2)
-    clocks.stop()
+    if own_clocks:
+        time.sleep(0.2)
+        clocks.stop()
     v.sync()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     lat = cps["lat_len"].cpu().numpy()
@@ -589,6 +682,9 @@ def run_decode_step(args, rank, world):
     peak, kind = measured_peaks()
     committed = int(sum(int(a) + 1 for a in acc))
     v.close()
+    l2_note = "inputs %.2f GB > L2 (%d MB): no flush" % (
+        (w.p_logits.numel() + w.q_logits.numel()) * elt / 1e9, l2_mb(dev))
+    del w, cps, out
     return {"metric": "decode steps per second (path search + verification + draft-length "
                       "update), sequences x steps / s",
             "value": world * B / (ms * 1e-3), "unit": "sequence-steps/s", "n_gpus": world,
@@ -600,8 +696,7 @@ def run_decode_step(args, rank, world):
                        "marginal_rows": "streamed once (the path search's statistics feed "
                                         "the verification)",
                        "lattice_len_mean": float(lat.mean()),
-                       "l2": "inputs %.2f GB > L2 (%d MB): no flush"
-                             % ((w.p_logits.numel() + w.q_logits.numel()) * elt / 1e9, l2_mb(dev))},
+                       "l2": l2_note},
             "committed_tokens_per_s": world * committed / (ms * 1e-3),
             "hbm": {"step_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak": peak,
                     "peak_kind": kind, "rows_per_step": rows},
@@ -629,24 +724,67 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def cpu_baseline(w: synth.Workload):
+BAND_KINDS = {1: "accept", 2: "cdf", 4: "select", 8: "resid"}
+
+
+def parity_block(gpu: dict, orc: dict) -> dict:
+    """The GPU's outputs against the oracle's on the same sequences: decisions
+    (selected draft, accepted length, emitted token) must be equal outside the
+    oracle's 1e-5 boundary band; band trials are counted by kind, with how
+    many still agree; row LSE and streak scores within 1e-4 relative."""
+    import numpy as np
+    n = len(orc["sel"])
+    mism, band, agree, errs = 0, 0, 0, 0
+    kinds = {name: 0 for name in BAND_KINDS.values()}
+    lse_err = score_err = 0.0
+    for b in range(n):
+        got = (int(gpu["sel"][b]), int(gpu["accept_len"][b]), int(gpu["next_token"][b]))
+        if orc["err"][b]:
+            errs += 1
+            mism += got != (-1, -1, -1)
+            continue
+        exp = (int(orc["sel"][b]), int(orc["accept_len"][b]), int(orc["next_token"][b]))
+        lo = orc["lse"][b][..., :gpu["lse"][b].shape[-1]]
+        lse_err = max(lse_err, float(np.max(np.abs(gpu["lse"][b] - lo) / np.maximum(1.0, np.abs(lo)))))
+        so = orc["scores"][b]
+        score_err = max(score_err, float(np.max(np.abs(gpu["scores"][b] - so) /
+                                                np.maximum(np.abs(so), 1e-2))))
+        if orc["band"][b]:
+            band += 1
+            agree += got == exp
+            for bit, name in BAND_KINDS.items():
+                if orc["band"][b] & bit:
+                    kinds[name] += 1
+            continue
+        mism += got != exp
+    return {"checked": n, "mismatches": mism, "band_trials": band, "band": kinds,
+            "band_agree": agree, "data_errors": errs, "lse_max_rel_err": lse_err,
+            "score_max_rel_err": score_err,
+            "bar": "sel, accept_len, next_token equal outside the 1e-5 boundary band; "
+                   "LSE and scores within 1e-4 relative"}
+
+
+def cpu_baseline(w: synth.Workload, gpu: dict = None):
+    """The oracle on every sequence of the batch, one host thread per sequence
+    (its time is the CPU baseline), then its single-thread rate on the first
+    sequence; with the GPU's outputs of the same step, also the parity block."""
     import oracle
     cores = os.cpu_count() or 1
-    S = max(1, min(cores, w.B))
-    p, q, d, t = synth.to_oracle_arrays(w, list(range(S)))
-    nt = min(S, oracle.max_threads()) if oracle.max_threads() > 1 else 1
+    p, q, d, t = synth.to_oracle_arrays(w)
+    nt = min(w.B, oracle.max_threads()) if oracle.max_threads() > 1 else 1
     t0 = time.perf_counter()
-    oracle.verify(p, q, d, t, w.seed, nthreads=nt)
+    orc = oracle.verify(p, q, d, t, w.seed, nthreads=nt)
     dt = time.perf_counter() - t0
     # the same oracle on one thread, first sequence only
     t1 = time.perf_counter()
     oracle.verify(p[:1], q[:1], d[:1], t[:1], w.seed, nthreads=1)
     dt1 = time.perf_counter() - t1
-    return {"value": S * w.K * w.gamma / dt, "unit": UNIT, "cores": nt, "kind": "oracle",
+    base = {"value": w.B * w.K * w.gamma / dt, "unit": UNIT, "cores": nt, "kind": "oracle",
             "single_thread": w.K * w.gamma / dt1, "cpu": "%s, %d cores" % (cpu_model(), cores),
-            "sample": "first %d of %d sequences of the same workload, one thread per sequence "
+            "sample": "all %d sequences of the same workload, one thread per sequence "
                       "(%.1f s wall); single_thread: the first sequence on one thread "
-                      "(%.1f s)" % (S, w.B, dt, dt1)}
+                      "(%.1f s)" % (w.B, dt, dt1)}
+    return base, (parity_block(gpu, orc) if gpu is not None else None)
 
 
 # ---------------------------------------------------------------------------

@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "SDV_OK", 1: "SDV_ERR_ARG", 2: "SDV_ERR_CUDA", 3: "SDV_ERR_OO
                 4: "SDV_ERR_DEVICE_DATA", 5: "SDV_ERR_SCRATCH"}
 STATIC_SCRATCH_BYTES = 8 << 20
 SDV_STATUS_BAD_LENGTH = 16
+SDV_HOOK_SAMPLE_NO_COPY = 1
 
 # Every entry point of include/sdv.h, with its ctypes signature.
 _VP, _I, _I64, _U64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
@@ -46,6 +47,7 @@ SIGNATURES = {
     "sdv_plan": (_I, [_VP, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I),
                       ctypes.POINTER(_I)]),
     "sdv_set_stream": (_I, [_VP, _VP]),
+    "sdv_set_test_hooks": (_I, [_VP, ctypes.c_uint]),
     "sdv_profile_enable": (_I, [_VP, _I]),
     "sdv_profile_read": (_I, [_VP, ctypes.POINTER(_F), ctypes.POINTER(_I)]),
     "sdv_verify_static": (_I, [_I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
@@ -389,6 +391,11 @@ class DraftLengthController:
 
 def sdv_set_stream(ctx, stream) -> int:
     return load().sdv_set_stream(ctx, ctypes.c_void_p(_stream_handle(stream)))
+
+
+def sdv_set_test_hooks(ctx, hooks: int) -> int:
+    """Fault-path test hooks of a context (SDV_HOOK_* bits; 0 = none)."""
+    return load().sdv_set_test_hooks(ctx, int(hooks))
 
 
 class Verifier:

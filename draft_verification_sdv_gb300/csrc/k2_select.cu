@@ -437,16 +437,15 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
 }  // namespace
 
 cudaError_t setup_select(size_t smem) {
-    const int n = static_cast<int>(smem);
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<true, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, n);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(select_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, n);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(select_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, n);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(select_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, n);
-    return e;
+    const void* fns[4] = {reinterpret_cast<const void*>(select_kernel<true, false>),
+                          reinterpret_cast<const void*>(select_kernel<true, true>),
+                          reinterpret_cast<const void*>(select_kernel<false, false>),
+                          reinterpret_cast<const void*>(select_kernel<false, true>)};
+    for (const void* f : fns) {
+        const cudaError_t e = raise_smem_limit(f, smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s, bool pdl) {

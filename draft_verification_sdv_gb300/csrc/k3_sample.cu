@@ -120,17 +120,23 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
     }
     __syncthreads();
     if (t.mode != 0 && nv > 0) {
+        // test hook: the barrier is armed but no copy is issued, so the wait
+        // below runs out after a few polls with nothing in flight
+        const bool no_copy = (a.hooks & kHookSampleNoCopy) != 0;
+        const uint32_t polls = no_copy ? kTestPolls : kMaxPolls;
         if (tid == 0) {
             const uint32_t bytes = static_cast<uint32_t>(nv) * 16u;
             mbar_arrive_expect_tx(&bar, t.mode == 1 ? 2u * bytes : bytes);
-            bulk_g2s(sp, static_cast<const uint4*>(a.p) + t.row_p * a.nvec + sv0, bytes, &bar);
-            if (t.mode == 1)
-                bulk_g2s(sq, static_cast<const uint4*>(a.q) + t.row_q * a.nvec + sv0, bytes, &bar);
+            if (!no_copy) {
+                bulk_g2s(sp, static_cast<const uint4*>(a.p) + t.row_p * a.nvec + sv0, bytes, &bar);
+                if (t.mode == 1)
+                    bulk_g2s(sq, static_cast<const uint4*>(a.q) + t.row_q * a.nvec + sv0, bytes, &bar);
+            }
         }
-        if (!mbar_wait_bounded(&bar, 0, kMaxPolls)) {
+        if (!mbar_wait_bounded(&bar, 0, polls)) {
             // Give the copies a second bounded chance to land before the
             // shared memory is released, and report the timeout.
-            mbar_wait_bounded(&bar, 0, kMaxPolls);
+            mbar_wait_bounded(&bar, 0, polls);
             if (tid == 0) {
                 s_ok = 0.0f;
                 atomicOr(a.status, kStatusTimeout);
@@ -282,6 +288,9 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
                 a.out_tok[b] = tok >= 0 ? static_cast<int32_t>(sv0 * EPV + tok) : -1;
             }
         } else if (t.mode != 0 && !all_ok && rank == 0 && tid == 0) {
+            // a slice never arrived: no output of this sequence is reported
+            a.out_sel[b] = -1;
+            a.out_len[b] = -1;
             a.out_tok[b] = -1;
         }
         break;
@@ -291,11 +300,9 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
 }  // namespace
 
 cudaError_t setup_sample(size_t smem) {
-    cudaError_t e = cudaFuncSetAttribute(sample_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(sample_kernel<true>), smem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(sample_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem));
+    return raise_smem_limit(reinterpret_cast<const void*>(sample_kernel<false>), smem);
 }
 
 cudaError_t launch_sample(const SampleArgs& a, bool bf16, int B, int cluster, size_t smem,

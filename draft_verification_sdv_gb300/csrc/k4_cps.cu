@@ -677,8 +677,7 @@ cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(a.G) * a.mmax * 8 + static_cast<size_t>(a.G) * 4 +
                         static_cast<size_t>(3) * a.G * a.beam;
     if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            cps_beam_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(cps_beam_kernel), smem);
         if (e != cudaSuccess) return e;
     }
     // An ordinary stream-ordered launch: as a programmatic dependent of the

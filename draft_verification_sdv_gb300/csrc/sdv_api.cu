@@ -4,7 +4,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "../../include/sdv.h"
@@ -40,6 +43,8 @@ struct sdv_ctx {
     int32_t* hs_drafts;
     float* hs_temps;
     int32_t* hs_out;
+    // fault-path test hooks (sdv_set_test_hooks)
+    unsigned hooks;
     // kernel timing: 4 events per recorded step
     bool prof_on;
     std::vector<cudaEvent_t> prof_ev;
@@ -50,6 +55,8 @@ struct sdv_ctx {
 static_assert(SDV_FLAG_SHARED_Q == sdv::kFlagSharedQ && SDV_FLAG_GREEDY == sdv::kFlagGreedy &&
                   SDV_FLAG_SHARED_PREFIX_ROW == sdv::kFlagSharedPrefixRow,
               "public layout flags and kernel flags must agree");
+static_assert(SDV_HOOK_SAMPLE_NO_COPY == sdv::kHookSampleNoCopy,
+              "public test hooks and kernel hooks must agree");
 
 namespace {
 
@@ -73,16 +80,26 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kMaxProfSteps = 65536;
 
-bool is_device_ptr(const void* p) {
-    cudaPointerAttributes at;
-    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}  // namespace
+
+namespace sdv {
+
+cudaError_t raise_smem_limit(const void* func, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, size_t> limit;   // (kernel, device) -> bytes
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& cur = limit[std::make_pair(func, dev)];
+    if (bytes <= cur) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes));
+    if (e == cudaSuccess) cur = bytes;
+    return e;
 }
 
-}  // namespace
+}  // namespace sdv
 
 extern "C" {
 
@@ -289,7 +306,10 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     ma.p = p_logits;
     ma.q = q_logits;
     ma.tasks = ctx->tasks;
+    ma.out_sel = out_sel;
+    ma.out_len = out_accept_len;
     ma.out_tok = out_next_token;
+    ma.hooks = ctx->hooks;
     ma.status = ctx->status;
     ma.nvec = ctx->nvec;
     ma.slice_vec = ctx->slice_vec;
@@ -649,6 +669,14 @@ sdv_status sdv_adl_step(int B, int window, int kmin, int kmax, int up, int down,
         if (p && !is_device_ptr(p)) return SDV_ERR_ARG;
     AdlArgs a{B, window, kmin, kmax, up, down, gen_len, acc_len, k, state, status};
     return launch_adl(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
+}
+
+sdv_status sdv_set_test_hooks(sdv_ctx* ctx, unsigned hooks) {
+    if (!ctx) return SDV_ERR_ARG;
+    if (hooks & ~static_cast<unsigned>(SDV_HOOK_SAMPLE_NO_COPY))
+        return fail(ctx, SDV_ERR_ARG, "unknown test hook bits 0x%x", hooks);
+    ctx->hooks = hooks;
+    return SDV_OK;
 }
 
 sdv_status sdv_set_stream(sdv_ctx* ctx, void* stream) {

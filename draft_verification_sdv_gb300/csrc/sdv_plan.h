@@ -154,16 +154,30 @@ struct SelectArgs {
 
 // Residual / bonus sampling (K3): a cluster of `cluster` CTAs per sequence,
 // each staging `slice_vec` vectors of the row(s) in shared memory.
+// A bounded wait that gives up (kStatusTimeout) leaves the sequence's three
+// outputs at -1.
 struct SampleArgs {
     const void* p;
     const void* q;
     const SeqTask* tasks;
+    int32_t* out_sel;
+    int32_t* out_len;
     int32_t* out_tok;
     unsigned* status;
     int64_t nvec;
     int64_t slice_vec;
     int cluster;
+    unsigned hooks = 0;     // kHook* bits (fault-path tests)
 };
+
+// Fault-path test hooks (the public SDV_HOOK_* values).
+enum : unsigned {
+    // the sample kernel arms its barrier for the row copies but issues none,
+    // and polls it only kTestPolls times: its bounded wait runs out with no
+    // copy in flight, which exercises the timeout path safely
+    kHookSampleNoCopy = 1u,
+};
+constexpr uint32_t kTestPolls = 16;
 
 // Causal-consistency path search (k4_cps.cu): prune kernel over the B*G
 // drafter rows, then one warp per sequence for the beam.
@@ -212,9 +226,26 @@ cudaError_t launch_rowpass(const RowPassArgs& a, bool bf16, cudaStream_t s, bool
 cudaError_t launch_select(const SelectArgs& a, bool bf16, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_sample(const SampleArgs& a, bool bf16, int B, int cluster, size_t smem,
                           cudaStream_t s, bool pdl);
-// Per-kernel set-up (shared-memory opt-in), once per device.
+// Per-kernel set-up (shared-memory opt-in): raise the kernels' dynamic
+// shared-memory limit on the current device to at least `smem`.
 cudaError_t setup_select(size_t smem);
 cudaError_t setup_sample(size_t smem);
+// The dynamic shared-memory limit of kernel `func` on the current device is
+// process-wide state: contexts of different shapes share it.  This raises it
+// to `bytes` when it is lower and never lowers it, so that setting up a
+// context for a small shape cannot break the launches of one made earlier for
+// a larger shape.  Thread-safe (one lock around the per-device record).
+cudaError_t raise_smem_limit(const void* func, size_t bytes);
+
+// True when `p` is device (or managed) memory of some device.
+inline bool is_device_ptr(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
 // Resident blocks per SM of the row-pass kernel.
 cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm);
 

@@ -1,20 +1,21 @@
 // sdv_static.cu -- sdv_verify_static: the verification step for callers that
 // cannot allocate device memory.
 //
-// Some callers may not call cudaMalloc at all: code running inside a CUDA
-// graph capture that forbids allocation, a host process whose device memory is
-// owned entirely by another allocator (a serving engine's pool), or a plug-in
-// loaded into such a process.  For them this entry point runs the same three
-// kernels as sdv_verify_ex (row pass, select/scan, sample), but their scratch
-// -- the row-pass partials, the per-sequence tasks and the status word --
-// lives in one file-scope static device array of kStaticScratchBytes, which
-// every GPU that loads this library holds until the process exits.  The
-// caller still owns and passes every input and output.
+// Some callers may not call cudaMalloc at all: a host process whose device
+// memory is owned entirely by another allocator (a serving engine's pool), a
+// plug-in loaded into such a process, or code that runs where allocation is
+// forbidden.  For them this entry point runs the same three kernels as
+// sdv_verify_ex (row pass, select/scan, sample), but their scratch -- the
+// row-pass partials, the per-sequence tasks and the status word -- lives in
+// one file-scope static device array of kStaticScratchBytes, which every GPU
+// that loads this library holds until the process exits.  The caller still
+// owns and passes every input and output.
 //
 // Set-up: the first call on a device (with that device current) resolves the
-// device address of the array with cudaGetSymbolAddress; make that first call
-// before any stream capture.  No call allocates: no cudaMalloc, no cudaFree,
-// no allocating library routine.
+// device address of the array with cudaGetSymbolAddress and raises the
+// kernels' shared-memory limits; make that first call before any stream
+// capture.  No call allocates: no cudaMalloc, no cudaFree, no allocating
+// library routine.
 //
 // Every call shares the one array and leaves its contents behind; the status
 // word is cleared at the start of each call and everything else is written
@@ -66,6 +67,12 @@ cudaError_t setup_device(int dev, StaticDevice** out) {
         if (e == cudaSuccess) e = rowpass_occupancy(true, &bps_bf16);
         if (e != cudaSuccess) return e;
         if (bps_f32 < 1 || bps_bf16 < 1 || optin <= 4096) return cudaErrorInvalidConfiguration;
+        // Let both kernels take up to the device's opt-in limit, once: the
+        // limit is only ever raised, so launches that ask for less, from here
+        // or from any context, are not disturbed.
+        e = setup_select(static_cast<size_t>(optin) - 4096);
+        if (e == cudaSuccess) e = setup_sample(static_cast<size_t>(optin) - 4096);
+        if (e != cudaSuccess) return e;
         d.scratch = ptr;
         d.nsm = nsm;
         d.smem_optin = optin;
@@ -93,8 +100,18 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
         return SDV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits)) & 15u)
         return SDV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(drafts) | reinterpret_cast<uintptr_t>(out_sel) |
+         reinterpret_cast<uintptr_t>(out_accept_len) | reinterpret_cast<uintptr_t>(out_next_token) |
+         reinterpret_cast<uintptr_t>(temperature_per_seq)) & 3u)
+        return SDV_ERR_ARG;
     if (!temperature_per_seq && !(std::isfinite(temperature) && temperature > 0.0f))
         return SDV_ERR_ARG;
+    // every pointer must be device memory: a host pointer is refused here,
+    // before anything is enqueued
+    const void* ptrs[7] = {p_logits, q_logits, drafts, out_sel, out_accept_len, out_next_token,
+                           temperature_per_seq};
+    for (const void* ptr : ptrs)
+        if (ptr && !is_device_ptr(ptr)) return SDV_ERR_ARG;
 
     // Scratch layout in the static array: partials, tasks, status word.
     const int64_t nvec = static_cast<int64_t>(V) * elt / 16;
@@ -133,11 +150,6 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     if (sel_smem > static_cast<size_t>(sd->smem_optin) - 4096 ||
         smp_smem > static_cast<size_t>(sd->smem_optin) - 4096)
         return SDV_ERR_ARG;
-    // Let both kernels take up to the device's opt-in limit (raising the
-    // limit never disturbs a launch that asks for less).
-    if (setup_select(static_cast<size_t>(sd->smem_optin) - 4096) != cudaSuccess ||
-        setup_sample(static_cast<size_t>(sd->smem_optin) - 4096) != cudaSuccess)
-        return SDV_ERR_CUDA;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return SDV_ERR_CUDA;
@@ -189,6 +201,8 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     ma.p = p_logits;
     ma.q = q_logits;
     ma.tasks = tasks;
+    ma.out_sel = out_sel;
+    ma.out_len = out_accept_len;
     ma.out_tok = out_next_token;
     ma.status = status;
     ma.nvec = nvec;

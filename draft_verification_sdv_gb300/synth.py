@@ -259,17 +259,17 @@ def workload(idx: int, device="cpu", seed: Optional[int] = None,
 
 def to_oracle_arrays(w: Workload, seqs: Optional[Sequence[int]] = None):
     """Host numpy copies of (a sample of) a workload in the oracle's formats:
-    bf16 logits as raw uint16 words, float32 as is."""
+    bf16 logits as raw uint16 words, float32 as is (q is None when the
+    workload has no drafter rows)."""
     import numpy as np
     sl = slice(None) if seqs is None else list(seqs)
-    p = w.p_logits[sl].detach().cpu().contiguous()
-    q = w.q_logits[sl].detach().cpu().contiguous()
-    if p.dtype == torch.bfloat16:
-        p = p.view(torch.int16).numpy().view(np.uint16)
-        q = q.view(torch.int16).numpy().view(np.uint16)
-    else:
-        p, q = p.numpy(), q.numpy()
-    if w.shared_q:          # the oracle takes the full layout: q broadcast over k
+    def host(x):
+        x = x[sl].detach().cpu().contiguous()
+        return x.view(torch.int16).numpy().view(np.uint16) if x.dtype == torch.bfloat16 else x.numpy()
+
+    p = host(w.p_logits)
+    q = None if w.q_logits is None else host(w.q_logits)     # none under greedy acceptance
+    if w.shared_q and q is not None:    # the oracle takes the full layout: q broadcast over k
         q = np.ascontiguousarray(np.broadcast_to(q[:, None], (q.shape[0], w.K) + q.shape[1:]))
     d = w.drafts[sl].detach().cpu().numpy().astype(np.int32)
     t = np.asarray(w.temps_list(), dtype=np.float64)

@@ -237,7 +237,10 @@ sdv_status sdv_verify_host(sdv_ctx* ctx, const void* p_logits_host,
 /*
  * Wait for the context's stream and return the device-side status of every
  * step enqueued since the previous sdv_sync (then cleared): SDV_OK,
- * SDV_ERR_DEVICE_DATA or SDV_ERR_CUDA.
+ * SDV_ERR_DEVICE_DATA or SDV_ERR_CUDA.  SDV_ERR_CUDA with the text "a bounded
+ * device wait gave up" means that the sampling pass waited for its row copy
+ * longer than its poll limit; it then wrote -1 to all three outputs of the
+ * sequences concerned, and the context stays usable.
  */
 sdv_status sdv_sync(sdv_ctx* ctx);
 
@@ -254,6 +257,19 @@ void sdv_destroy(sdv_ctx* ctx);
  * size) of the sampling pass.  Any pointer may be NULL. */
 sdv_status sdv_plan(const sdv_ctx* ctx, int* rowpass_ctas, int64_t* chunk_vectors,
                     int* chunks_per_row, int* sample_cluster);
+
+/*
+ * Fault-path test hook (not part of the method; the pages have no
+ * counterpart).  With SDV_HOOK_SAMPLE_NO_COPY set, the sampling pass of later
+ * steps arms its barrier for the row copy but issues no copy and polls only a
+ * few times, so that its bounded wait runs out with nothing in flight: the
+ * step writes -1 to every sequence's three outputs and sdv_sync returns
+ * SDV_ERR_CUDA ("a bounded device wait gave up").  This is how the timeout
+ * path is tested without faulting or hanging a GPU.  hooks = 0 restores
+ * normal steps; unknown bits give SDV_ERR_ARG.
+ */
+#define SDV_HOOK_SAMPLE_NO_COPY 1u
+sdv_status sdv_set_test_hooks(sdv_ctx* ctx, unsigned hooks);
 
 /* Replace the stream of a context (a cudaStream_t): later calls enqueue on
  * it.  The caller orders it after work already enqueued on the old stream.
@@ -388,12 +404,13 @@ sdv_status sdv_adl_step(int B, int window, int kmin, int kmax, int up, int down,
  * allocate device memory.  The pages have no counterpart to this entry point:
  * it exists for deployment, not for the method.
  *
- * Who needs it: code that must not call cudaMalloc -- work recorded into a
- * CUDA graph or run where allocation is forbidden, a process whose device
- * memory belongs entirely to another allocator (a serving engine's pool), a
- * plug-in loaded into such a process.  sdv_create allocates a workspace; this
- * call does not.  It takes no context and allocates nothing: no cudaMalloc,
- * no cudaFree, no allocating library routine.
+ * Who needs it: code that must not call cudaMalloc -- a process whose device
+ * memory belongs entirely to another allocator (a serving engine's pool, which
+ * would otherwise see memory vanish behind its back), a plug-in loaded into
+ * such a process, code that runs where allocation is forbidden.  sdv_create
+ * allocates a workspace; this call does not.  It takes no context and
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
  *
  * Scratch: the row-pass partials, per-sequence tasks and status word live in
  * one static device array of SDV_STATIC_SCRATCH_BYTES (8 MiB), which every GPU
@@ -403,16 +420,20 @@ sdv_status sdv_adl_step(int B, int window, int kmin, int kmax, int up, int down,
  * B*K*(2*gamma+1) must stay below about one million rows).
  *
  * Set-up: the first call on a device, with that device current, looks up the
- * device address of the array (cudaGetSymbolAddress) and the device's limits.
- * Make that first call before any stream capture.
+ * device address of the array (cudaGetSymbolAddress), the device's limits,
+ * and raises the kernels' shared-memory limits.  Make that first call before
+ * any stream capture.
  *
  * Arguments: as sdv_verify_ex, with the shape (B, K, gamma, V, dtype) and the
  * stream (a cudaStream_t, NULL = legacy default stream) passed on every call;
- * all tensors are caller-owned device memory.  Outputs are the same values
- * sdv_verify_ex writes.  Argument errors return SDV_ERR_ARG and nothing is
- * enqueued.  The call only enqueues; there is no sdv_sync for it: a sequence
- * with bad data (draft id out of range, non-finite row, bad per-sequence
- * temperature) gets -1 in all three outputs.
+ * all tensors are caller-owned device memory (logits 16-byte aligned, the
+ * int32 / float arrays 4-byte aligned).  Outputs are the same values
+ * sdv_verify_ex writes.  Argument errors -- including a host pointer or a
+ * misaligned one -- return SDV_ERR_ARG and nothing is enqueued.  The call only
+ * enqueues; there is no sdv_sync for it: a sequence with bad data (draft id
+ * out of range, non-finite row, bad per-sequence temperature), or whose
+ * sampling pass gave up waiting for its row copy, gets -1 in all three
+ * outputs.
  *
  * Sharing: every call uses the same array and leaves its contents behind (the
  * status word is cleared at the start of each call; the rest is written before

@@ -18,3 +18,17 @@ def oracle_lib():
     import oracle
     oracle.lib()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Boundary-band counts of every oracle comparison of the run (see
+    tests/band_report.py), printed even under -q."""
+    try:
+        import band_report
+    except ImportError:
+        return
+    if not band_report.RECORDS:
+        return
+    terminalreporter.write_sep("-", "oracle parity: trials checked and boundary-band counts by kind")
+    for line in band_report.table():
+        terminalreporter.write_line(line)

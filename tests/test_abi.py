@@ -57,6 +57,18 @@ def test_argument_errors_without_gpu(lib):
         assert lib.sdv_cps_ex(B, G, 64, bd.SDV_BF16, None, None, 1.0, None, 0.8, mmax, beam, -1,
                               None, None, None, None, None, None, None, None,
                               None) == bd.SDV_ERR_ARG
+    # the allocation-free entry point: alignment of the int32 / float arrays is
+    # checked before anything touches the device (fake, never dereferenced
+    # addresses: 16-byte aligned logits, then one 4-byte array off by 2)
+    base = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000]
+    for i in range(2, 6):
+        ptrs = list(base)
+        ptrs[i] += 2
+        assert lib.sdv_verify_static(2, 2, 3, 64, bd.SDV_BF16, None, ptrs[0], ptrs[1], ptrs[2], 1.0,
+                                     None, 0, ptrs[3], ptrs[4], ptrs[5]) == bd.SDV_ERR_ARG
+    assert lib.sdv_verify_static(2, 2, 3, 64, bd.SDV_BF16, None, base[0], base[1], base[2], 1.0,
+                                 0x70002, 0, base[3], base[4], base[5]) == bd.SDV_ERR_ARG
+    assert lib.sdv_set_test_hooks(None, 0) == bd.SDV_ERR_ARG
     assert lib.sdv_sync(None) == bd.SDV_ERR_ARG
     assert lib.sdv_last_error(None) == b"null context"
     lib.sdv_destroy(None)

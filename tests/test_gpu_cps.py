@@ -190,19 +190,17 @@ def test_cps_exact_ties_on_a_coarse_grid(dt, beam):
     assert compare_cps(gpu, orc, "grid", _qf(q)) <= 1
 
 
-def test_cps_four_warp_rows_full_size_sampled():
+def test_cps_four_warp_rows_full_size():
     """The bench's shape (1024 rows: one CTA of 4 warps per row) against the
-    oracle on sampled sequences, and a smaller many-row case in full."""
+    oracle on every sequence, and a smaller many-row case in full."""
     w = synth.workload_shared(B=32, device="cuda", seed=57)
     g = bd.sdv_cps(w.q_logits, tau=0.8, mmax=15, beam=3, temps=w.temps)
     torch.cuda.synchronize()
     gpu = {k: v.cpu().numpy() for k, v in g.items()}
     import oracle
-    seqs = [0, 13, 31]
-    qh = _host(w.q_logits[seqs])
-    orc = oracle.cps(qh, w.temps[seqs].cpu().numpy(), 0.8, 15, 3, nthreads=oracle.max_threads())
-    sub = {k: v[seqs] for k, v in gpu.items()}
-    assert compare_cps(sub, orc, "full-size", _qf(w.q_logits[seqs])) <= 1
+    orc = oracle.cps(_host(w.q_logits), w.temps.cpu().numpy(), 0.8, 15, 3,
+                     nthreads=oracle.max_threads())
+    assert compare_cps(gpu, orc, "full-size", _qf(w.q_logits)) <= 2
     del w, g
     torch.cuda.empty_cache()
     # 20 x 32 = 640 rows, all compared, bf16 and fp32

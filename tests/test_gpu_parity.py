@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import band_report
 from draft_verification_sdv_gb300 import binding as bd
 from draft_verification_sdv_gb300 import synth
 
@@ -42,32 +43,52 @@ def run_gpu(w: synth.Workload, seed=None, stream=None, greedy=False, shared_pref
     return res
 
 
-def run_oracle(w: synth.Workload, seqs=None, seed=None, greedy=False):
+def run_oracle(w: synth.Workload, seqs=None, seed=None, greedy=False, lens=None):
+    """The oracle on the whole batch in one call over all host threads (one
+    thread per sequence), or on the listed sequences, each keeping its own b
+    in the uniform keying."""
     import oracle
     p, q, d, t = synth.to_oracle_arrays(w, seqs)
     seed = w.seed if seed is None else seed
-    if greedy:
-        if seqs is None:
-            return oracle.verify_greedy(p, d, t, seed, nthreads=oracle.max_threads())
-        outs = [oracle.verify_greedy(p[i:i + 1], d[i:i + 1], t[i:i + 1], seed, b0=b, nthreads=1)
-                for i, b in enumerate(seqs)]
-        return {k: np.concatenate([o[k] for o in outs]) for k in outs[0]}
+    nt = oracle.max_threads()
     if seqs is None:
-        return oracle.verify(p, q, d, t, seed, nthreads=oracle.max_threads())
-    # sampled sequences keep their own b in the uniform keying
-    outs = [oracle.verify(p[i:i + 1], q[i:i + 1], d[i:i + 1], t[i:i + 1], seed, b0=b,
-                          nthreads=1) for i, b in enumerate(seqs)]
+        if greedy:
+            return oracle.verify_greedy(p, d, t, seed, nthreads=nt, lens=lens)
+        return oracle.verify(p, q, d, t, seed, nthreads=nt, lens=lens)
+    outs = []
+    for i, b in enumerate(seqs):
+        ln = None if lens is None else lens[b:b + 1]
+        if greedy:
+            outs.append(oracle.verify_greedy(p[i:i + 1], d[i:i + 1], t[i:i + 1], seed, b0=b,
+                                             nthreads=nt, lens=ln))
+        else:
+            outs.append(oracle.verify(p[i:i + 1], q[i:i + 1], d[i:i + 1], t[i:i + 1], seed, b0=b,
+                                      nthreads=nt, lens=ln))
     return {k: np.concatenate([o[k] for o in outs]) for k in outs[0]}
 
 
-BAND_NAMES = {1: "accept", 2: "cdf", 4: "select", 8: "resid"}
+BAND_NAMES = band_report.KINDS
 
 
-def compare(gpu, orc, seqs=None, tag=""):
-    """Assert parity; return the number of boundary-band trials (their kinds
-    are printed)."""
+def full_size_bounds(n: int) -> dict:
+    """Band bounds of a full-size Qwen-vocabulary batch of n sequences.  The
+    acceptance, selection and residual-mass kinds are rare (at most 2).  The
+    CDF kind is not: a draw that lands on a token of mass below 1e-5 of the
+    row's total lies wholly inside the band, and 152064-token rows hold many
+    such tokens (their share of the draws is about sum_v min(p_v, 2e-5),
+    around a tenth here), so it is bounded by a quarter of the trials."""
+    return {"accept": 2, "select": 2, "resid": 2, "cdf": max(2, n // 4)}
+
+
+def compare(gpu, orc, seqs=None, tag="", max_kind=None):
+    """Assert parity on every listed sequence (all by default) and return the
+    number of boundary-band trials as a band_report.BandCount (kinds and the
+    band trials on which the GPU still agrees attached); the count is
+    recorded for the run's summary.  Data-error trials must be -1 on both
+    sides.  max_kind, when given, bounds the trials of each band kind: an int
+    for every kind, or a dict by kind name."""
     seqs = list(range(len(orc["sel"]))) if seqs is None else list(seqs)
-    n_band = 0
+    n_band = n_agree = 0
     kinds = {}
     for i, b in enumerate(seqs):
         if orc["err"][i]:
@@ -80,18 +101,27 @@ def compare(gpu, orc, seqs=None, tag=""):
         so, sg = orc["scores"][i], gpu["scores"][b]
         assert np.all(np.abs(sg - so) <= SCORE_RTOL * np.abs(so) + 1e-6), \
             "%s b=%d scores %s vs %s" % (tag, b, sg, so)
+        got = (int(gpu["sel"][b]), int(gpu["accept_len"][b]), int(gpu["next_token"][b]))
+        exp = (int(orc["sel"][i]), int(orc["accept_len"][i]), int(orc["next_token"][i]))
         if orc["band"][i]:
             n_band += 1
+            n_agree += got == exp
             for bit, name in BAND_NAMES.items():
                 if orc["band"][i] & bit:
                     kinds[name] = kinds.get(name, 0) + 1
             continue
-        got = (int(gpu["sel"][b]), int(gpu["accept_len"][b]), int(gpu["next_token"][b]))
-        exp = (int(orc["sel"][i]), int(orc["accept_len"][i]), int(orc["next_token"][i]))
         assert got == exp, "%s b=%d (sel, L, token) gpu %s oracle %s" % (tag, b, got, exp)
+    count = band_report.BandCount(n_band, checked=len(seqs), kinds=kinds, band_agree=n_agree,
+                                  tag=tag)
+    band_report.record(count)
     if n_band:
-        print("%s: %d of %d trials in the boundary band %s" % (tag, n_band, len(seqs), kinds))
-    return n_band
+        print("%s: %d of %d trials in the boundary band %s, %d of them still equal"
+              % (tag, n_band, len(seqs), kinds, n_agree))
+    if max_kind is not None:
+        for name, n in kinds.items():
+            bound = max_kind[name] if isinstance(max_kind, dict) else max_kind
+            assert n <= bound, "%s: %d trials in the %s band (bound %d)" % (tag, n, name, bound)
+    return count
 
 
 def _small(B, K, G, V, dtype=torch.bfloat16, T=1.0, seed=0, temps=None, identical=(),
@@ -171,34 +201,31 @@ def test_self_selection_workload_full():
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads: sampled sequences against the oracle, properties on all
+# full-size workloads: every sequence against the oracle
 # ---------------------------------------------------------------------------
 
-def test_serving_workload_sampled():
+def test_serving_workload_full():
     w = synth.workload(4, device="cuda")
     gpu = run_gpu(w)
     assert gpu["status"] == bd.SDV_OK
     G = w.gamma
     ident = set(w.identical)
     assert len(ident) == 19
-    for b in range(w.B):
-        assert 0 <= gpu["sel"][b] < w.K and 0 <= gpu["accept_len"][b] <= G
-        assert 0 <= gpu["next_token"][b] < w.V
-        if b in ident:                      # q == p: full acceptance, streak gamma, draft 0
-            assert gpu["accept_len"][b] == G and gpu["sel"][b] == 0
-            assert np.all(gpu["scores"][b] == G)
-    rng = np.random.default_rng(4)
-    seqs = sorted(set(rng.choice(w.B, 5, replace=False).tolist()) | {sorted(ident)[0]})
-    orc = run_oracle(w, seqs)
-    assert compare(gpu, orc, seqs, tag="serving") <= 1
+    for b in ident:                          # q == p: full acceptance, streak gamma, draft 0
+        assert gpu["accept_len"][b] == G and gpu["sel"][b] == 0
+        assert np.all(gpu["scores"][b] == G)
+    orc = run_oracle(w)
+    nb = compare(gpu, orc, tag="serving B64 K8 g16 (all 64)",
+                 max_kind=full_size_bounds(64))
+    assert nb <= 64 // 4 + 6
+    del w
+    torch.cuda.empty_cache()
 
 
-def test_large_window_workload_sampled():
+def test_large_window_workload_full():
     w = synth.workload(5, device="cuda")
     gpu = run_gpu(w)
     assert gpu["status"] == bd.SDV_OK
-    assert ((gpu["accept_len"] >= 0) & (gpu["accept_len"] <= w.gamma)).all()
-    assert ((gpu["next_token"] >= 0) & (gpu["next_token"] < w.V)).all()
     # the residual token carries residual mass: p > q at that id
     for b in range(w.B):
         L, k, x = int(gpu["accept_len"][b]), int(gpu["sel"][b]), int(gpu["next_token"][b])
@@ -208,9 +235,10 @@ def test_large_window_workload_sampled():
             lp = float(w.p_logits[b, k, L, x]) / T - lse[L]
             lq = float(w.q_logits[b, k, L, x]) / T - lse[w.gamma + 1 + L]
             assert lp > lq - 1e-6
-    seqs = [0, 13, 31]
-    orc = run_oracle(w, seqs)
-    assert compare(gpu, orc, seqs, tag="large-window") <= 1
+    orc = run_oracle(w)
+    nb = compare(gpu, orc, tag="large-window B32 K16 g32 (all 32)",
+                 max_kind=full_size_bounds(32))
+    assert nb <= 32 // 4 + 6
     del w
     torch.cuda.empty_cache()
 
@@ -376,17 +404,18 @@ def test_shared_marginals_equal_full_layout_bitwise():
         assert np.array_equal(shared[k], ref[k]), k
 
 
-def test_shared_marginals_large_window_sampled():
-    """The shared-marginal bench configuration at full size: sampled
-    sequences against the oracle, and the shared prefix-row layout (what the
-    bench line uses) bit-identical to reading every prefix row."""
+def test_shared_marginals_large_window_full():
+    """The shared-marginal bench configuration at full size: every sequence
+    against the oracle, and the shared prefix-row layout (what the bench line
+    uses) bit-identical to reading every prefix row."""
     w = synth.workload_shared(device="cuda")
     gpu = run_gpu(w)
     assert gpu["status"] == bd.SDV_OK
-    assert ((gpu["accept_len"] >= 0) & (gpu["accept_len"] <= w.gamma)).all()
-    seqs = [3, 30]
-    orc = run_oracle(w, seqs)
-    assert compare(gpu, orc, seqs, tag="shared large-window") <= 1
+    orc = run_oracle(w)
+    nb = compare(gpu, orc, tag="shared-marginal B32 K16 g32 (all 32)",
+                 max_kind=full_size_bounds(32))
+    assert nb <= 32 // 4 + 6
+    del orc
     pre = run_gpu(w, shared_prefix_row=True)
     for k in ("sel", "accept_len", "next_token", "scores", "lse"):
         assert np.array_equal(pre[k], gpu[k]), k
@@ -419,13 +448,16 @@ def test_greedy_small_shapes(shape):
             assert gpu["next_token"][b] != d[b, k, L]
 
 
-def test_greedy_large_window_sampled():
+def test_greedy_large_window_full():
     w = synth.workload(5, device="cuda")
+    w.q_logits = None                        # greedy acceptance reads no drafter rows
+    torch.cuda.empty_cache()
     gpu = run_gpu(w, greedy=True)
     assert gpu["status"] == bd.SDV_OK
-    seqs = [5, 21]
-    orc = run_oracle(w, seqs, greedy=True)
-    assert compare(gpu, orc, seqs, tag="greedy large-window") <= 1
+    orc = run_oracle(w, greedy=True)
+    nb = compare(gpu, orc, tag="greedy large-window (all 32)",
+                 max_kind=full_size_bounds(32))
+    assert nb <= 32 // 4 + 6
     del w
     torch.cuda.empty_cache()
 

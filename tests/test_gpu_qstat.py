@@ -17,7 +17,7 @@ import torch
 
 from draft_verification_sdv_gb300 import binding as bd
 from draft_verification_sdv_gb300 import synth
-from test_gpu_parity import compare, _small
+from test_gpu_parity import compare, full_size_bounds, _small
 
 pytestmark = pytest.mark.gpu
 
@@ -180,17 +180,19 @@ def test_argument_errors():
     g.close()
 
 
-def test_bench_size_sampled():
+def test_bench_size_full():
     """The decode step's shape: 32 sequences, 3 paths of 32 tokens over
-    152064-token marginals, per-sequence temperatures."""
+    152064-token marginals, per-sequence temperatures; every sequence against
+    the oracle."""
     w = synth.workload_shared(B=32, K=3, gamma=32, device="cuda", seed=66)
     cps = bd.sdv_cps(w.q_logits, tau=0.8, mmax=15, beam=3, temps=w.temps, row_stat=True)
     w.drafts = cps["paths"].clamp(min=0).contiguous()
     lens = cps["lat_len"].cpu().numpy()
     gpu = _verify(w, q_stat=cps["row_stat"], lens=lens, seed=w.seed, shared_prefix_row=True)
     assert gpu["status"] == bd.SDV_OK
-    seqs = [0, 13, 31]
-    orc = _oracle(w, lens, seed=w.seed, seqs=seqs)
-    assert compare(gpu, orc, seqs, tag="qstat bench size") <= 1
+    orc = _oracle(w, lens, seed=w.seed)
+    nb = compare(gpu, orc, tag="qstat decode-step shape (all 32)",
+                 max_kind=full_size_bounds(32))
+    assert nb <= 32 // 4 + 6
     del w, cps
     torch.cuda.empty_cache()
