@@ -5,13 +5,14 @@
 // a path is scored by drafter confidence alone: the sum of its per-position
 // log-probabilities.
 //
-// cps_prune_kernel, one CTA per drafter row q[b, j, :]: each warp streams a
-// contiguous share of the row (eight 16-byte loads in flight per lane),
-// keeping the online softmax statistics (max, sum 2^{(l - max) c}) and the
-// warp's 16 largest logits (ties to the lower id) as one key per lane.  Only
-// a vector holding a value at or above the list's last entry enters the
-// (rare, warp-uniform) insertion path, so the pass costs about what the
-// statistics cost.  Warp 0 then merges the warps' lists and statistics.  The
+// cps_prune_kernel, one CTA per drafter row q[b, j, :]: the warps take the
+// row's 4 KB chunks one after another from a shared counter (eight 16-byte
+// loads in flight per lane), keeping the online softmax statistics (max,
+// sum 2^{(l - max) c}) and the warp's 16 largest logits (ties to the lower
+// id) as one key per lane.  Only a vector holding a value at or above a
+// floor the row's 16th best is known to reach enters the (rare, warp-uniform)
+// insertion path; a warp busy inserting simply claims fewer chunks.  Warp 0
+// then merges the warps' lists and statistics.  The
 // kept candidates are the shortest prefix of the row's list, in order of
 // probability, whose mass reaches tau, capped at mmax; tokens of probability
 // zero are never candidates, and a row with a NaN or +inf logit, or none
@@ -195,14 +196,22 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
     const float c = kLog2e / T;
     const uint4* rowv = static_cast<const uint4*>(a.q) + row * a.nvec;
     constexpr int EPV = BF16 ? 8 : 4;
-    const int64_t per_warp = (a.nvec + NW - 1) / NW;
-    const int64_t v0 = warp * per_warp;
-    const int64_t v1 = v0 + per_warp < a.nvec ? v0 + per_warp : a.nvec;
+    // The row is cut into chunks of two half-batches (64 * kHalf vectors);
+    // warp w starts on chunk w and then takes the next unclaimed one, so a
+    // warp busy with candidates (most of a row's best logits often sit in a
+    // few chunks) streams less and the warps of a row end together.
+    constexpr int64_t kChunk = 64 * kHalf;
+    const int64_t v1 = a.nvec;
+    const int nchunks = static_cast<int>((a.nvec + kChunk - 1) / kChunk);
 
     // No kernel launches as this one's programmatic dependent, but with this
     // trigger back-to-back pruning passes measured 0.060 ms against 0.064 ms.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (tid == 0) s_floor = order_key(-INFINITY);
+    __shared__ int s_next;            // next unclaimed chunk of the row
+    if (tid == 0) {
+        s_floor = order_key(-INFINITY);
+        s_next = NW;
+    }
     __syncthreads();
 
     uint64_t mine = 0;                // this lane's slot of the warp's list
@@ -217,9 +226,10 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
             m = vm;
         }
         if (m != -INFINITY) {
+            const float nmc = -(m * c);
             float t[kHalf];
 #pragma unroll
-            for (int u = 0; u < kHalf; ++u) t[u] = vec_exp_sum<BF16>(w[u], m, c);
+            for (int u = 0; u < kHalf; ++u) t[u] = vec_exp_sum_fma<BF16>(w[u], c, nmc);
 #pragma unroll
             for (int h = kHalf / 2; h > 0; h >>= 1)
 #pragma unroll
@@ -297,17 +307,36 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
             w[u] = idx < v1 ? ld_stream(rowv + idx) : make_uint4(ninf, ninf, ninf, ninf);
         }
     };
-    // Two half-batches in turn: one is in flight while the other is
-    // processed, so the loads continue through the candidate work.  Every
-    // lane runs the same number of iterations (warp-wide votes inside).
+    // The two half-batches of a chunk in turn: while one is processed the
+    // other is in flight, and the next chunk is claimed and its first half
+    // loaded before the second half of this one is processed, so the loads
+    // continue through the candidate work.  Every lane of a warp runs the same
+    // iterations (warp-wide votes inside).
     uint4 wa[kHalf], wb[kHalf];
-    int64_t base = v0 + lane;
+    int chunk = warp;
+    int64_t base = chunk * kChunk + lane;
     load(wa, base);
-    for (; base - lane < v1; base += 64 * kHalf) {
-        load(wb, base + 32 * kHalf);
+    load(wb, base + 32 * kHalf);
+    {
+        // A floor for the whole row before any warp builds its list: the
+        // 16th largest lane maximum of a warp's first half-batch is a value
+        // that 16 logits of the row reach.  The largest of the warps' floors
+        // gates every warp from the start.
+        const float f = warp_16th(vec_max_n<BF16, kHalf>(wa), lane);
+        if (lane == 0 && f != -INFINITY) atomicMax(&s_floor, order_key(f));
+    }
+    __syncthreads();
+    while (chunk < nchunks) {
+        int next = 0;
+        if (lane == 0) next = atomicAdd(&s_next, 1);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        const int64_t nbase = next * kChunk + lane;
         process(wa, base);
-        load(wa, base + 64 * kHalf);
+        load(wa, nbase);
         process(wb, base + 32 * kHalf);
+        load(wb, nbase + 32 * kHalf);
+        chunk = next;
+        base = nbase;
     }
     // row statistics: warp, then CTA
 #pragma unroll
