@@ -107,28 +107,6 @@ __device__ __forceinline__ float vec_exp_sum(const uint4& v, float m, float c) {
     }
 }
 
-// The same sum with each exponent formed by one fused multiply-add,
-// l * c + nmc with nmc = -(m * c): one instruction fewer per logit than the
-// exact-difference form above, at a rounding error of about one unit in the
-// last place of |l * c| in the exponent (a relative error near 1e-6 in each
-// term for logits of a few tens).
-template <bool BF16>
-__device__ __forceinline__ float vec_exp_sum_fma(const uint4& v, float c, float nmc) {
-    if constexpr (BF16) {
-        const float e0 = ex2(fmaf(bf16_lo(v.x), c, nmc)), e1 = ex2(fmaf(bf16_hi(v.x), c, nmc));
-        const float e2 = ex2(fmaf(bf16_lo(v.y), c, nmc)), e3 = ex2(fmaf(bf16_hi(v.y), c, nmc));
-        const float e4 = ex2(fmaf(bf16_lo(v.z), c, nmc)), e5 = ex2(fmaf(bf16_hi(v.z), c, nmc));
-        const float e6 = ex2(fmaf(bf16_lo(v.w), c, nmc)), e7 = ex2(fmaf(bf16_hi(v.w), c, nmc));
-        return ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
-    } else {
-        const float e0 = ex2(fmaf(__uint_as_float(v.x), c, nmc));
-        const float e1 = ex2(fmaf(__uint_as_float(v.y), c, nmc));
-        const float e2 = ex2(fmaf(__uint_as_float(v.z), c, nmc));
-        const float e3 = ex2(fmaf(__uint_as_float(v.w), c, nmc));
-        return (e0 + e1) + (e2 + e3);
-    }
-}
-
 // Merge two partial softmax statistics (max m, sum s of 2^{(l - m) c}).
 // NaN sums propagate; an empty partial (s == 0) contributes nothing.
 __device__ __forceinline__ void merge_stat(float& m, float& s, float m2, float s2, float c) {
