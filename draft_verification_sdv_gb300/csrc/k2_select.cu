@@ -354,14 +354,32 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     // Expected accepted streak of every draft (fp32 prefix products: GB300's
     // fp64 rate is a small fraction of its fp32 rate, and fp32 keeps the
     // score well inside the selection tolerance).
-    for (int k = tid; k < K; k += kSelectThreads) {
-        float prefix = 1.0f, sc = 0.0f;
-        for (int j = 0; j < Lg; ++j) {
-            prefix *= ratio[k * RS + j];
-            sc += prefix;
+    // One warp per draft: the prefix products of 32 positions at a time by a
+    // warp scan, their sum by a butterfly.
+    {
+        const int lane = tid & 31, warp = tid >> 5;
+        for (int k = warp; k < K; k += kSelectThreads / 32) {
+            float carry = 1.0f, sc = 0.0f;
+            for (int j0 = 0; j0 < Lg; j0 += 32) {
+                const bool in = j0 + lane < Lg;
+                float pr = in ? ratio[k * RS + j0 + lane] : 1.0f;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, pr, off);
+                    if (lane >= off) pr *= y;
+                }
+                pr *= carry;
+                float part = in ? pr : 0.0f;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+                sc += part;
+                carry = __shfl_sync(0xffffffffu, pr, 31);
+            }
+            if (lane == 0) {
+                score[k] = sc;
+                if (a.out_scores) a.out_scores[static_cast<int64_t>(b) * K + k] = sc;
+            }
         }
-        score[k] = sc;
-        if (a.out_scores) a.out_scores[static_cast<int64_t>(b) * K + k] = sc;
     }
     __syncthreads();
 
@@ -378,8 +396,10 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
                 bk = k;
             }
         }
+        // lanes >= K hold no draft: only the steps below K can change lane 0
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
+            if (off >= K) continue;
             const float ob = __shfl_xor_sync(0xffffffffu, best, off);
             const int ok = __shfl_xor_sync(0xffffffffu, bk, off);
             if (ok < K && (bk == K || ob > best || (ob == best && ok < bk))) {
@@ -393,29 +413,40 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
     const int sel = s_sel;
 
     // Left-to-right acceptance of the selected draft: the first rejected j.
-    for (int j = tid; j < Lg; j += kSelectThreads) {
+    // Thread j also keeps the sampling uniform of position j (up to Lg, the
+    // bonus position), so that the thread of the first rejection writes the
+    // task without drawing again.
+    float my_w = 0.0f;
+    for (int j = tid; j <= Lg; j += kSelectThreads) {
         const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(b), 0u, 0u),
                                       a.seed_lo, a.seed_hi);
-        const float u = uniform24(r.x);
-        const float aj = ratio[sel * RS + j];
-        const bool accepted = (aj >= 1.0f) || (u < aj);
-        if (!accepted) atomicMin(&s_len, j);
+        if (j == tid) my_w = uniform24(r.y);
+        if (j < Lg) {
+            const float u = uniform24(r.x);
+            const float aj = ratio[sel * RS + j];
+            const bool accepted = (aj >= 1.0f) || (u < aj);
+            if (!accepted) atomicMin(&s_len, j);
+        }
     }
     __syncthreads();
 
-    if (tid == 0) {
-        const int L = s_len;
+    const int L = s_len;
+    if (tid == (L < kSelectThreads ? L : 0)) {
         a.out_sel[b] = sel;
         a.out_len[b] = L;
-        const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(L), static_cast<uint32_t>(b), 0u, 0u),
-                                      a.seed_lo, a.seed_hi);
         SeqTask t = {};
-        t.w = uniform24(r.y);
+        if (L < kSelectThreads) {
+            t.w = my_w;
+        } else {
+            const uint4 r = philox4x32_10(
+                make_uint4(static_cast<uint32_t>(L), static_cast<uint32_t>(b), 0u, 0u), a.seed_lo,
+                a.seed_hi);
+            t.w = uniform24(r.y);
+        }
         t.c = c;
         t.row_p = p_row_index(a.flags, b, sel, L, K, G);
         const float2 ps = pstat[sel * (G + 1) + L];
-        t.mp = ps.x;
-        t.inv_sp = 1.0f / ps.y;
+        t.off_p = -(ps.x * c) - log2f(ps.y);
         if (L < Lg && greedy) {
             t.mode = 3;                                   // p with the rejected token zeroed
             t.zero_id = a.drafts[seq_d + static_cast<int64_t>(sel) * G + L];
@@ -424,8 +455,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
             t.mode = 1;                                   // residual max(0, p - q)
             t.row_q = q_row_index(a.flags, b, sel, L, K, G);
             const float2 qs = qstat[sel * G + L];
-            t.mq = qs.x;
-            t.inv_sq = 1.0f / qs.y;
+            t.off_q = -(qs.x * c) - log2f(qs.y);
         } else {
             t.mode = 2;                                   // bonus token from p at Lg
             t.row_q = -1;

@@ -55,8 +55,9 @@ __device__ __forceinline__ float elem(const uint4& v, int e) {
 }
 
 // Sampling weights of the elements of vector i of the slice: p, or the
-// residual max(0, p - q); the element at slice position zero_pos (if any)
-// gets weight 0 (greedy replacement: the rejected token is excluded).
+// residual max(0, p - q), each probability 2^(l * c + off) of its row; the
+// element at slice position zero_pos (if any) gets weight 0 (greedy
+// replacement: the rejected token is excluded).
 template <bool BF16>
 __device__ __forceinline__ void weights(const uint4* sp, const uint4* sq, int i, bool resid,
                                         int zero_pos, const SeqTask& t,
@@ -65,12 +66,12 @@ __device__ __forceinline__ void weights(const uint4* sp, const uint4* sq, int i,
     const uint4 pv = sp[i];
 #pragma unroll
     for (int e = 0; e < EPV; ++e)
-        w[e] = i * EPV + e == zero_pos ? 0.0f : ex2((elem<BF16>(pv, e) - t.mp) * t.c) * t.inv_sp;
+        w[e] = i * EPV + e == zero_pos ? 0.0f : ex2(fmaf(elem<BF16>(pv, e), t.c, t.off_p));
     if (resid) {
         const uint4 qv = sq[i];
 #pragma unroll
         for (int e = 0; e < EPV; ++e)
-            w[e] = fmaxf(w[e] - ex2((elem<BF16>(qv, e) - t.mq) * t.c) * t.inv_sq, 0.0f);
+            w[e] = fmaxf(w[e] - ex2(fmaf(elem<BF16>(qv, e), t.c, t.off_q)), 0.0f);
     }
 }
 

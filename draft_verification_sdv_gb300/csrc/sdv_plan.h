@@ -92,6 +92,9 @@ __host__ __device__ inline int32_t adl_update(int32_t* st, int W, int kmin, int 
 // mode 0: nothing to draw (data error); 1: residual max(0, p - q) of rows
 // (row_p, row_q); 2: bonus draw from row_p alone; 3: greedy replacement, row_p
 // with the token zero_id zeroed out.
+// The probability of token v of a row is 2^(l_v * c + off) with
+// off = -(max * c) - log2(sum 2^{(l - max) c}): one fused multiply-add and
+// one exponential per logit.
 struct SeqTask {
     int mode;
     int zero_id;
@@ -99,8 +102,8 @@ struct SeqTask {
     int64_t row_q;      // row index within the q buffer
     float w;            // sampling uniform
     float c;            // log2(e) / T
-    float mp, inv_sp;   // row max and 1 / sum 2^{(l - max) c} of the p row
-    float mq, inv_sq;   // same for the q row (residual only)
+    float off_p;        // exponent offset of the p row
+    float off_q;        // exponent offset of the q row (residual only)
 };
 
 // Row pass (K1): rows are split into `chunks` fixed chunks of `chunk_vec`
