@@ -12,7 +12,8 @@
 // is zero (p == q up to rounding) the draw falls back to p.
 //
 // Only the one or two rows chosen per sequence are re-read.  A cluster of
-// `cluster` CTAs shares a sequence: each stages its slice of the row(s) in
+// `cluster` CTAs (8, or 16 for batches of at most 16 sequences where the
+// device can schedule clusters that wide) shares a sequence: each stages its slice of the row(s) in
 // shared memory with one bulk (TMA) copy per row, forms the weights on the
 // fly, scans them, and the CTAs exchange slice totals through distributed
 // shared memory; the CTA whose slice holds the target finds the token.
@@ -23,6 +24,7 @@ namespace sdv {
 namespace {
 
 constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier wait
+constexpr int kMaxCluster = 16;            // CTAs per sequence (16 is a non-portable cluster size)
 
 // The two halves of a cluster barrier: arrive (no ordering) now, wait later.
 // Used to know that every CTA of the cluster has started before writing to
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
     __shared__ int s_pick, s_last_thread, s_token;
     // (slice total, slice arrived) of every CTA of the cluster, per pass:
     // each CTA writes its own pair into every CTA's copy
-    __shared__ float2 s_tot2[2][8];
+    __shared__ float2 s_tot2[2][kMaxCluster];
 
     constexpr int EPV = Elems<BF16>::kPerVec;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -205,9 +207,9 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         float R = 0.0f, target_excl = 0.0f;
         bool all_ok = true;
         int owner = -1, last_rank = -1;
-        float tot[8];
+        float tot[kMaxCluster];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < kMaxCluster; ++r) {
             const float2 v = r < CL ? s_tot2[pass][r] : make_float2(0.0f, 1.0f);
             tot[r] = v.x;
             all_ok = all_ok && v.y != 0.0f;
@@ -301,9 +303,38 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
 }  // namespace
 
 cudaError_t setup_sample(size_t smem) {
-    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(sample_kernel<true>), smem);
-    if (e != cudaSuccess) return e;
-    return raise_smem_limit(reinterpret_cast<const void*>(sample_kernel<false>), smem);
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(sample_kernel<true>), smem);
+    if (e == cudaSuccess) e = raise_smem_limit(reinterpret_cast<const void*>(sample_kernel<false>), smem);
+    // clusters of 16 CTAs (beyond the portable 8) for small batches
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sample_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sample_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+int sample_max_cluster() { return kMaxCluster; }
+
+int sample_active_clusters(bool bf16, int cluster, size_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+    cfg.blockDim = dim3(kSampleThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = bf16 ? cudaOccupancyMaxActiveClusters(&n, sample_kernel<true>, &cfg)
+                               : cudaOccupancyMaxActiveClusters(&n, sample_kernel<false>, &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 cudaError_t launch_sample(const SampleArgs& a, bool bf16, int B, int cluster, size_t smem,

@@ -157,9 +157,9 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
 
     // Select plan.
     ctx->sel_smem = select_smem_bytes(K, gamma);
-    // Sample plan: up to 8 CTAs per sequence, each holding a slice of one or
-    // two rows in shared memory.
-    int cl = 8;
+    // Sample plan: up to 8 CTAs per sequence (16 for a small batch), each
+    // holding a slice of one or two rows in shared memory.
+    int cl = B <= kWideSampleMaxB ? sample_max_cluster() : 8;
     while (cl > 1 && cl > ctx->nvec) cl >>= 1;
     ctx->cluster = cl;
     ctx->slice_vec = (ctx->nvec + cl - 1) / cl;
@@ -171,6 +171,18 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
     }
     e = setup_select(ctx->sel_smem > 0 ? ctx->sel_smem : 16);
     if (e == cudaSuccess) e = setup_sample(ctx->smp_smem);
+    if (e == cudaSuccess && ctx->cluster > 8 &&
+        sample_active_clusters(ctx->bf16, ctx->cluster, ctx->smp_smem) < 1) {
+        // a cluster that wide cannot be scheduled here: the portable 8
+        ctx->cluster = 8;
+        ctx->slice_vec = (ctx->nvec + 7) / 8;
+        ctx->smp_smem = static_cast<size_t>(2) * ctx->slice_vec * 16;
+        if (ctx->smp_smem > smem_cap) {
+            sdv_destroy(ctx);
+            return SDV_ERR_ARG;
+        }
+        e = setup_sample(ctx->smp_smem);
+    }
     if (e != cudaSuccess) {
         sdv_destroy(ctx);
         return SDV_ERR_CUDA;

@@ -249,6 +249,13 @@ inline bool is_device_ptr(const void* p) {
     }
     return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
 }
+// Largest CTAs per sequence of the sampling pass, and how many clusters of
+// `cluster` CTAs with `smem` bytes each the device can hold at once (0: none).
+int sample_max_cluster();
+int sample_active_clusters(bool bf16, int cluster, size_t smem);
+// Sequences up to which the sampling pass uses clusters of 16 CTAs (more
+// sequences keep 8, so that all clusters of a batch fit the GPU at once).
+constexpr int kWideSampleMaxB = 16;
 // Resident blocks per SM of the row-pass kernel.
 cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm);
 
