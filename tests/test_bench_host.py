@@ -77,3 +77,49 @@ def test_traffic_figures_of_the_committed_summaries(which):
     assert V * 2 <= t <= 1.02 * V * 2
     # a different source hash is not taken
     assert bench.traffic_per_row(profile, sources[:1]) is None or len(sources) == 1
+
+
+def _trial(sel, L, tok, band=0, err=0, lse=0.0, score=1.0):
+    return dict(sel=sel, L=L, tok=tok, band=band, err=err, lse=lse, score=score)
+
+
+def _as_arrays(trials, gpu_shift=None):
+    import numpy as np
+    n = len(trials)
+    orc = {"sel": np.array([t["sel"] for t in trials]), "accept_len": np.array([t["L"] for t in trials]),
+           "next_token": np.array([t["tok"] for t in trials]), "band": np.array([t["band"] for t in trials]),
+           "err": np.array([t["err"] for t in trials]),
+           "lse": np.array([[t["lse"], t["lse"]] for t in trials]),
+           "scores": np.array([[t["score"]] for t in trials])}
+    gpu = {k: orc[k].copy() for k in ("sel", "accept_len", "next_token")}
+    gpu["lse"] = orc["lse"].astype(np.float32).copy()
+    gpu["scores"] = orc["scores"].astype(np.float32).copy()
+    for i in range(n):
+        if orc["err"][i]:
+            gpu["sel"][i] = gpu["accept_len"][i] = gpu["next_token"][i] = -1
+    if gpu_shift:
+        for i, k, dv in gpu_shift:
+            gpu[k][i] += dv
+    return gpu, orc
+
+
+def test_parity_block_counts_mismatches_and_band_kinds():
+    """The bench's parity block: a decision that differs outside the band is
+    a mismatch; inside the band it is counted by kind (a trial may hold
+    several) and as agreeing or not; data errors must be -1 on the GPU."""
+    trials = [_trial(0, 3, 7), _trial(1, 0, 5), _trial(2, 4, 9, band=1 | 8), _trial(0, 2, 4, band=2),
+              _trial(-1, -1, -1, err=1), _trial(3, 1, 11, band=4)]
+    gpu, orc = _as_arrays(trials, gpu_shift=[(1, "next_token", 1), (3, "accept_len", 1)])
+    p = bench.parity_block(gpu, orc)
+    assert p["checked"] == 6 and p["data_errors"] == 1
+    assert p["mismatches"] == 1                       # trial 1; trial 3 differs inside the band
+    assert p["band_trials"] == 3 and p["band_agree"] == 2
+    assert p["band"] == {"accept": 1, "cdf": 1, "select": 1, "resid": 1}
+    assert p["lse_max_rel_err"] == 0.0 and p["score_max_rel_err"] == 0.0
+
+
+def test_parity_block_flags_a_data_error_the_gpu_missed():
+    trials = [_trial(-1, -1, -1, err=2), _trial(0, 1, 3)]
+    gpu, orc = _as_arrays(trials)
+    gpu["sel"][0] = 0                                  # the GPU did not report the bad row
+    assert bench.parity_block(gpu, orc)["mismatches"] == 1
