@@ -5,14 +5,16 @@
 // a path is scored by drafter confidence alone: the sum of its per-position
 // log-probabilities.
 //
-// cps_prune_kernel, one CTA per drafter row q[b, j, :]: the warps take the
-// row's 4 KB chunks one after another from a shared counter (eight 16-byte
+// cps_prune_kernel, one CTA per drafter row q[b, j, :]: the row is cut into
+// 4 KB chunks and warp w takes chunks w, w + NW, w + 2 NW, ... (eight 16-byte
 // loads in flight per lane), keeping the online softmax statistics (max,
 // sum 2^{(l - max) c}) and the warp's 16 largest logits (ties to the lower
-// id) as one key per lane.  Only a vector holding a value at or above a
-// floor the row's 16th best is known to reach enters the (rare, warp-uniform)
-// insertion path; a warp busy inserting simply claims fewer chunks.  Warp 0
-// then merges the warps' lists and statistics.  The
+// id) as one key per lane.  The interleaving spreads a row's first chunks,
+// where the best logits often sit, over all its warps; it is fixed, so every
+// sum is taken in the same order on every run.  Only a vector holding a
+// value at or above a floor the row's 16th best is known to reach enters the
+// (rare, warp-uniform) insertion path.  Warp 0 then merges the warps' lists
+// and statistics.  The
 // kept candidates are the shortest prefix of the row's list, in order of
 // probability, whose mass reaches tau, capped at mmax; tokens of probability
 // zero are never candidates, and a row with a NaN or +inf logit, or none
@@ -221,9 +223,8 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
     const uint4* rowv = static_cast<const uint4*>(a.q) + row * a.nvec;
     constexpr int EPV = BF16 ? 8 : 4;
     // The row is cut into chunks of two half-batches (64 * kHalf vectors);
-    // warp w starts on chunk w and then takes the next unclaimed one, so a
-    // warp busy with candidates (most of a row's best logits often sit in a
-    // few chunks) streams less and the warps of a row end together.
+    // warp w takes chunks w, w + NW, ...: a fixed order, so that the row's
+    // sums round the same way on every run.
     constexpr int64_t kChunk = 64 * kHalf;
     const int64_t v1 = a.nvec;
     const int nchunks = static_cast<int>((a.nvec + kChunk - 1) / kChunk);
@@ -231,11 +232,7 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
     // No kernel launches as this one's programmatic dependent, but with this
     // trigger back-to-back pruning passes measured 0.060 ms against 0.064 ms.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ int s_next;            // next unclaimed chunk of the row
-    if (tid == 0) {
-        s_floor = order_key(-INFINITY);
-        s_next = NW;
-    }
+    if (tid == 0) s_floor = order_key(-INFINITY);
     __syncthreads();
 
     uint64_t mine = 0;                // this lane's slot of the warp's list
@@ -332,9 +329,9 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
         }
     };
     // The two half-batches of a chunk in turn: while one is processed the
-    // other is in flight, and the next chunk is claimed and its first half
-    // loaded before the second half of this one is processed, so the loads
-    // continue through the candidate work.  Every lane of a warp runs the same
+    // other is in flight, and the next chunk's first half is loaded before
+    // the second half of this one is processed, so the loads continue
+    // through the candidate work.  Every lane of a warp runs the same
     // iterations (warp-wide votes inside).
     uint4 wa[kHalf], wb[kHalf];
     int chunk = warp;
@@ -351,9 +348,7 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
     }
     __syncthreads();
     while (chunk < nchunks) {
-        int next = 0;
-        if (lane == 0) next = atomicAdd(&s_next, 1);
-        next = __shfl_sync(0xffffffffu, next, 0);
+        const int next = chunk + NW;
         const int64_t nbase = next * kChunk + lane;
         process(wa, base);
         load(wa, nbase);

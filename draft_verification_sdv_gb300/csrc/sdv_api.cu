@@ -45,6 +45,13 @@ struct sdv_ctx {
     int32_t* hs_out;
     // fault-path test hooks (sdv_set_test_hooks)
     unsigned hooks;
+    // what the last row pass left in the partials (sdv_rowpass): 0 nothing,
+    // 1 the verifier rows, 2 the verifier and drafter rows; its temperature
+    // arguments and draft lengths
+    int rows_ready;
+    float rows_T;
+    const float* rows_temps;
+    const int32_t* rows_lens;
     // kernel timing: 4 events per recorded step
     bool prof_on;
     std::vector<cudaEvent_t> prof_ev;
@@ -215,33 +222,36 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
 
 namespace {
 
-sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
-                       const int32_t* drafts, const int32_t* draft_len, const float* q_row_stat,
-                       float temperature, const float* temperature_per_seq, uint64_t seed,
-                       int32_t* out_sel, int32_t* out_accept_len, int32_t* out_next_token,
-                       float* out_scores, float* out_lse) {
-    if (!ctx) return SDV_ERR_ARG;
-    ctx->err[0] = 0;
-    const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
-    if (!p_logits || (!q_logits && !greedy) || !drafts || !out_sel || !out_accept_len ||
-        !out_next_token)
-        return fail(ctx, SDV_ERR_ARG, "null pointer argument");
+// Argument checks of a row pass (logits and temperatures).
+sdv_status check_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logits, bool need_q,
+                      float temperature, const float* temperature_per_seq) {
+    if (!p_logits || (need_q && !q_logits)) return fail(ctx, SDV_ERR_ARG, "null pointer argument");
     if ((reinterpret_cast<uintptr_t>(p_logits) | reinterpret_cast<uintptr_t>(q_logits)) & 15u)
         return fail(ctx, SDV_ERR_ARG, "logit buffers must be 16-byte aligned");
-    if ((reinterpret_cast<uintptr_t>(drafts) | reinterpret_cast<uintptr_t>(out_sel) |
-         reinterpret_cast<uintptr_t>(out_accept_len) | reinterpret_cast<uintptr_t>(out_next_token) |
-         reinterpret_cast<uintptr_t>(temperature_per_seq) | reinterpret_cast<uintptr_t>(out_scores) |
-         reinterpret_cast<uintptr_t>(out_lse)) & 3u)
+    if (reinterpret_cast<uintptr_t>(temperature_per_seq) & 3u)
         return fail(ctx, SDV_ERR_ARG, "int32 / float buffers must be 4-byte aligned");
     if (!temperature_per_seq && !(std::isfinite(temperature) && temperature > 0.0f))
         return fail(ctx, SDV_ERR_ARG, "temperature must be finite and > 0");
-    const void* ptrs[8] = {p_logits, q_logits, drafts, out_sel, out_accept_len, out_next_token,
-                           temperature_per_seq, out_scores};
+    const void* ptrs[3] = {p_logits, q_logits, temperature_per_seq};
     for (const void* p : ptrs)
-        if (p && !is_device_ptr(p))
-            return fail(ctx, SDV_ERR_ARG, "argument is not a device pointer");
-    if (out_lse && !is_device_ptr(out_lse))
-        return fail(ctx, SDV_ERR_ARG, "out_lse is not a device pointer");
+        if (p && !is_device_ptr(p)) return fail(ctx, SDV_ERR_ARG, "argument is not a device pointer");
+    return SDV_OK;
+}
+
+// Argument checks of a selection and draw.
+sdv_status check_finish(sdv_ctx* ctx, const int32_t* drafts, const int32_t* draft_len,
+                        const float* q_row_stat, int32_t* out_sel, int32_t* out_accept_len,
+                        int32_t* out_next_token, float* out_scores, float* out_lse) {
+    const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
+    if (!drafts || !out_sel || !out_accept_len || !out_next_token)
+        return fail(ctx, SDV_ERR_ARG, "null pointer argument");
+    if ((reinterpret_cast<uintptr_t>(drafts) | reinterpret_cast<uintptr_t>(out_sel) |
+         reinterpret_cast<uintptr_t>(out_accept_len) | reinterpret_cast<uintptr_t>(out_next_token) |
+         reinterpret_cast<uintptr_t>(out_scores) | reinterpret_cast<uintptr_t>(out_lse)) & 3u)
+        return fail(ctx, SDV_ERR_ARG, "int32 / float buffers must be 4-byte aligned");
+    const void* ptrs[6] = {drafts, out_sel, out_accept_len, out_next_token, out_scores, out_lse};
+    for (const void* p : ptrs)
+        if (p && !is_device_ptr(p)) return fail(ctx, SDV_ERR_ARG, "argument is not a device pointer");
     if (draft_len && ((reinterpret_cast<uintptr_t>(draft_len) & 3u) || !is_device_ptr(draft_len)))
         return fail(ctx, SDV_ERR_ARG, "draft_len must be a 4-byte aligned device pointer");
     if (q_row_stat && greedy)
@@ -249,7 +259,14 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     if (q_row_stat &&
         ((reinterpret_cast<uintptr_t>(q_row_stat) & 15u) || !is_device_ptr(q_row_stat)))
         return fail(ctx, SDV_ERR_ARG, "q_row_stat must be a 16-byte aligned device pointer");
+    return SDV_OK;
+}
 
+// Enqueue the row pass: every verifier row, and the drafter rows when
+// `with_q`; rows past a draft length are skipped when `draft_len` is given.
+cudaError_t enqueue_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                         const int32_t* draft_len, bool with_q, float temperature,
+                         const float* temperature_per_seq, bool pdl) {
     RowPassArgs ra;
     ra.p = p_logits;
     ra.q = q_logits;
@@ -264,26 +281,26 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     ra.rows_total = ctx->rows_total;
     ra.nvec = ctx->nvec;
     ra.chunk_vec = ctx->chunk_vec;
-    // with the drafter rows' statistics supplied, only the verifier rows are
-    // streamed (the q rows come after them in item order)
-    ra.items = q_row_stat ? ctx->rows_p * ctx->chunks : ctx->items;
+    // without the drafter rows only the verifier rows are streamed (the q
+    // rows come after them in item order)
+    ra.items = with_q ? ctx->items : ctx->rows_p * ctx->chunks;
     ra.lens = draft_len;
-    cudaEvent_t* ev = nullptr;
-    if (ctx->prof_on && ctx->prof_n < kMaxProfSteps) {
-        const size_t need = static_cast<size_t>(ctx->prof_n + 1) * 4;
-        while (ctx->prof_ev.size() < need) {
-            cudaEvent_t x;
-            if (cudaEventCreate(&x) != cudaSuccess) return fail(ctx, SDV_ERR_CUDA, "event create");
-            ctx->prof_ev.push_back(x);
-        }
-        ev = &ctx->prof_ev[static_cast<size_t>(ctx->prof_n) * 4];
-        ++ctx->prof_n;
+    const cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->stream, pdl);
+    if (e == cudaSuccess) {
+        ctx->rows_ready = with_q ? 2 : 1;
+        ctx->rows_T = temperature;
+        ctx->rows_temps = temperature_per_seq;
+        ctx->rows_lens = draft_len;
     }
-    if (ev) cudaEventRecord(ev[0], ctx->stream);
-    cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->stream, ev == nullptr);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "row pass launch");
-    if (ev) cudaEventRecord(ev[1], ctx->stream);
+    return e;
+}
 
+// Enqueue the selection / scan and the draw on the partials of the last row pass.
+sdv_status enqueue_finish(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                          const int32_t* drafts, const int32_t* draft_len, const float* q_row_stat,
+                          float temperature, const float* temperature_per_seq, uint64_t seed,
+                          int32_t* out_sel, int32_t* out_accept_len, int32_t* out_next_token,
+                          float* out_scores, float* out_lse, cudaEvent_t* ev) {
     SelectArgs sa;
     sa.p = p_logits;
     sa.q = q_logits;
@@ -310,7 +327,7 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     sa.lens = draft_len;
     sa.q_stat = reinterpret_cast<const float4*>(q_row_stat);
     sa.merge_lanes = select_merge_lanes(ctx->K, ctx->G, ctx->chunks);
-    e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream, ev == nullptr);
+    cudaError_t e = launch_select(sa, ctx->bf16, ctx->sel_smem, ctx->stream, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "select launch");
     if (ev) cudaEventRecord(ev[2], ctx->stream);
 
@@ -330,6 +347,42 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     if (e != cudaSuccess) return cuda_fail(ctx, e, "sample launch");
     if (ev) cudaEventRecord(ev[3], ctx->stream);
     return SDV_OK;
+}
+
+sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                       const int32_t* drafts, const int32_t* draft_len, const float* q_row_stat,
+                       float temperature, const float* temperature_per_seq, uint64_t seed,
+                       int32_t* out_sel, int32_t* out_accept_len, int32_t* out_next_token,
+                       float* out_scores, float* out_lse) {
+    if (!ctx) return SDV_ERR_ARG;
+    ctx->err[0] = 0;
+    const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
+    sdv_status st = check_rows(ctx, p_logits, q_logits, !greedy, temperature, temperature_per_seq);
+    if (st == SDV_OK)
+        st = check_finish(ctx, drafts, draft_len, q_row_stat, out_sel, out_accept_len,
+                          out_next_token, out_scores, out_lse);
+    if (st != SDV_OK) return st;
+
+    cudaEvent_t* ev = nullptr;
+    if (ctx->prof_on && ctx->prof_n < kMaxProfSteps) {
+        const size_t need = static_cast<size_t>(ctx->prof_n + 1) * 4;
+        while (ctx->prof_ev.size() < need) {
+            cudaEvent_t x;
+            if (cudaEventCreate(&x) != cudaSuccess) return fail(ctx, SDV_ERR_CUDA, "event create");
+            ctx->prof_ev.push_back(x);
+        }
+        ev = &ctx->prof_ev[static_cast<size_t>(ctx->prof_n) * 4];
+        ++ctx->prof_n;
+    }
+    if (ev) cudaEventRecord(ev[0], ctx->stream);
+    // with the drafter rows' statistics supplied, only the verifier rows are streamed
+    const cudaError_t e = enqueue_rows(ctx, p_logits, q_logits, draft_len, !greedy && !q_row_stat,
+                                       temperature, temperature_per_seq, ev == nullptr);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "row pass launch");
+    if (ev) cudaEventRecord(ev[1], ctx->stream);
+    return enqueue_finish(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
+                          temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
+                          out_scores, out_lse, ev);
 }
 
 }  // namespace
@@ -372,6 +425,47 @@ sdv_status sdv_verify(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
                       int32_t* out_accept_len, int32_t* out_next_token) {
     return sdv_verify_ex(ctx, p_logits, q_logits, drafts, temperature, nullptr, seed, out_sel,
                          out_accept_len, out_next_token, nullptr, nullptr);
+}
+
+sdv_status sdv_rowpass(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                       float temperature, const float* temperature_per_seq, int with_q_rows) {
+    if (!ctx) return SDV_ERR_ARG;
+    ctx->err[0] = 0;
+    const bool with_q = with_q_rows != 0 && (ctx->flags & SDV_FLAG_GREEDY) == 0;
+    const sdv_status st = check_rows(ctx, p_logits, q_logits, with_q, temperature, temperature_per_seq);
+    if (st != SDV_OK) return st;
+    const cudaError_t e = enqueue_rows(ctx, p_logits, q_logits, nullptr, with_q, temperature,
+                                       temperature_per_seq, true);
+    return e == cudaSuccess ? SDV_OK : cuda_fail(ctx, e, "row pass launch");
+}
+
+sdv_status sdv_verify_from_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
+                                const int32_t* drafts, const int32_t* draft_len,
+                                const float* q_row_stat, float temperature,
+                                const float* temperature_per_seq, uint64_t seed,
+                                int32_t* out_sel, int32_t* out_accept_len,
+                                int32_t* out_next_token, float* out_scores, float* out_lse) {
+    if (!ctx) return SDV_ERR_ARG;
+    ctx->err[0] = 0;
+    const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
+    if (ctx->rows_ready == 0)
+        return fail(ctx, SDV_ERR_ARG, "no row pass has been enqueued on this context");
+    if (!greedy && !q_row_stat && ctx->rows_ready < 2)
+        return fail(ctx, SDV_ERR_ARG,
+                    "the row pass streamed no drafter rows: pass their statistics (q_row_stat)");
+    if (temperature_per_seq != ctx->rows_temps ||
+        (!temperature_per_seq && temperature != ctx->rows_T))
+        return fail(ctx, SDV_ERR_ARG, "temperatures differ from those of the row pass");
+    if (ctx->rows_lens && draft_len != ctx->rows_lens)
+        return fail(ctx, SDV_ERR_ARG, "draft lengths differ from those of the row pass");
+    sdv_status st = check_rows(ctx, p_logits, q_logits, !greedy, temperature, temperature_per_seq);
+    if (st == SDV_OK)
+        st = check_finish(ctx, drafts, draft_len, q_row_stat, out_sel, out_accept_len,
+                          out_next_token, out_scores, out_lse);
+    if (st != SDV_OK) return st;
+    return enqueue_finish(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
+                          temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
+                          out_scores, out_lse, nullptr);
 }
 
 sdv_status sdv_sync(sdv_ctx* ctx) {

@@ -212,6 +212,23 @@ def test_cps_four_warp_rows_full_size():
         assert compare_cps(gpu, orc, "640 rows %s" % q.dtype, _qf(q)) <= 1
 
 
+def test_cps_full_size_is_deterministic():
+    """Every output of the path search, the row statistics included, is the
+    same bit for bit on every run at the bench's size (152064-logit rows of
+    many chunks per warp)."""
+    w = synth.workload_shared(B=32, device="cuda", seed=59)
+    runs = []
+    for _ in range(3):
+        o = bd.sdv_cps(w.q_logits, tau=0.8, mmax=15, beam=3, temps=w.temps, row_stat=True)
+        torch.cuda.synchronize()
+        runs.append({k: t.clone() for k, t in o.items()})
+    for r in runs[1:]:
+        for k in runs[0]:
+            assert torch.equal(runs[0][k], r[k]), k
+    del w, runs
+    torch.cuda.empty_cache()
+
+
 def test_cps_deterministic_and_argmax_path():
     gen = torch.Generator(device="cuda")
     gen.manual_seed(59)
