@@ -34,14 +34,15 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kRowPassThreads) rowpass_kernel(const RowPassArgs a) {
-    // Let the select kernel launch now: it waits for this grid before it
-    // reads any partial.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the previous step's sample
     // kernel, this grid may be resident before that kernel ends: wait for it
     // (and its memory) before reading or writing anything.  A no-op when the
     // launch is an ordinary one.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Then let the select kernel launch: it waits for this grid before it
+    // reads any partial, but fetches the step's drafted tokens before that,
+    // so it must not start before the work ahead of this grid has finished.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t item = (static_cast<int64_t>(blockIdx.x) * kRowPassThreads + threadIdx.x) >> 5;
     const int64_t rows_per_seq_p = static_cast<int64_t>(a.K) * (a.G + 1);

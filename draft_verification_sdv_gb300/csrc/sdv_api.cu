@@ -62,6 +62,9 @@ struct sdv_ctx {
 static_assert(SDV_FLAG_SHARED_Q == sdv::kFlagSharedQ && SDV_FLAG_GREEDY == sdv::kFlagGreedy &&
                   SDV_FLAG_SHARED_PREFIX_ROW == sdv::kFlagSharedPrefixRow,
               "public layout flags and kernel flags must agree");
+static_assert((sdv::kFlagLateInputs & (SDV_FLAG_SHARED_Q | SDV_FLAG_GREEDY |
+                                       SDV_FLAG_SHARED_PREFIX_ROW)) == 0,
+              "the select kernel's own flag must not be a layout flag");
 static_assert(SDV_HOOK_SAMPLE_NO_COPY == sdv::kHookSampleNoCopy,
               "public test hooks and kernel hooks must agree");
 
@@ -296,11 +299,14 @@ cudaError_t enqueue_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logit
 }
 
 // Enqueue the selection / scan and the draw on the partials of the last row pass.
+// `late_inputs`: the drafts, lengths and temperatures may be written after the
+// row pass was enqueued, so the select kernel reads them only after its wait.
 sdv_status enqueue_finish(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
                           const int32_t* drafts, const int32_t* draft_len, const float* q_row_stat,
                           float temperature, const float* temperature_per_seq, uint64_t seed,
                           int32_t* out_sel, int32_t* out_accept_len, int32_t* out_next_token,
-                          float* out_scores, float* out_lse, cudaEvent_t* ev) {
+                          float* out_scores, float* out_lse, cudaEvent_t* ev,
+                          bool late_inputs) {
     SelectArgs sa;
     sa.p = p_logits;
     sa.q = q_logits;
@@ -313,7 +319,7 @@ sdv_status enqueue_finish(sdv_ctx* ctx, const void* p_logits, const void* q_logi
     sa.G = ctx->G;
     sa.V = ctx->V;
     sa.chunks = ctx->chunks;
-    sa.flags = ctx->flags;
+    sa.flags = ctx->flags | (late_inputs ? kFlagLateInputs : 0u);
     sa.rows_p = ctx->rows_p;
     sa.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
     sa.seed_hi = static_cast<uint32_t>(seed >> 32);
@@ -382,7 +388,7 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     if (ev) cudaEventRecord(ev[1], ctx->stream);
     return enqueue_finish(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
                           temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
-                          out_scores, out_lse, ev);
+                          out_scores, out_lse, ev, false);
 }
 
 }  // namespace
@@ -463,9 +469,11 @@ sdv_status sdv_verify_from_rows(sdv_ctx* ctx, const void* p_logits, const void* 
         st = check_finish(ctx, drafts, draft_len, q_row_stat, out_sel, out_accept_len,
                           out_next_token, out_scores, out_lse);
     if (st != SDV_OK) return st;
+    // The drafts (and lengths, temperatures) may be results of kernels enqueued
+    // after the row pass, here or on a stream joined to this one.
     return enqueue_finish(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
                           temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
-                          out_scores, out_lse, nullptr);
+                          out_scores, out_lse, nullptr, true);
 }
 
 sdv_status sdv_sync(sdv_ctx* ctx) {

@@ -241,7 +241,12 @@ sdv_status sdv_verify_qstat(sdv_ctx* ctx, const void* p_logits, const void* q_lo
  * drafter rows; draft_len may be NULL).  It may be called more than once on one
  * row pass (several draft sets against the same verifier rows).  The caller
  * orders it after the row pass on the context's stream and after whatever
- * produced the drafts (e.g. cudaStreamWaitEvent).  The results equal those of
+ * produced the drafts: kernels enqueued on the context's stream between the
+ * two calls, or work on another stream that the context's stream waits for
+ * (cudaStreamWaitEvent).  Its first kernel reads the drafts, draft lengths and
+ * temperatures only once the work before it on the stream has finished and
+ * its writes are visible (unlike the single call, which fetches the drafted
+ * tokens while the row pass ends).  The results equal those of
  * the single call with the same arguments, bit for bit.  SDV_ERR_ARG, with
  * nothing enqueued: no row pass yet on this context; no q_row_stat when the row
  * pass streamed no drafter rows; temperature arguments other than the row
