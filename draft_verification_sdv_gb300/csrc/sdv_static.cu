@@ -13,9 +13,8 @@
 //
 // Set-up: the first call on a device (with that device current) resolves the
 // device address of the array with cudaGetSymbolAddress and raises the
-// kernels' shared-memory limits; make that first call before any stream
-// capture.  No call allocates: no cudaMalloc, no cudaFree, no allocating
-// library routine.
+// kernels' shared-memory limits; later calls on that device skip it.  No call
+// allocates: no cudaMalloc, no cudaFree, no allocating library routine.
 //
 // Every call shares the one array and leaves its contents behind; the status
 // word is cleared at the start of each call and everything else is written

@@ -464,8 +464,8 @@ sdv_status sdv_adl_step(int B, int window, int kmin, int kmax, int up, int down,
  *
  * Set-up: the first call on a device, with that device current, looks up the
  * device address of the array (cudaGetSymbolAddress), the device's limits,
- * and raises the kernels' shared-memory limits.  Make that first call before
- * any stream capture.
+ * and raises the kernels' shared-memory limits; later calls on that device
+ * do none of this.
  *
  * Arguments: as sdv_verify_ex, with the shape (B, K, gamma, V, dtype) and the
  * stream (a cudaStream_t, NULL = legacy default stream) passed on every call;
