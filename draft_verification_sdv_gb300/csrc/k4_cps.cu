@@ -24,15 +24,16 @@
 //
 // cps_beam_kernel, one warp per sequence: the lattice ends at the first
 // position whose most likely candidate is eos_id (kept alone as the last
-// token); a left-to-right beam of width W keeps, at every step, the W best
-// prefixes.  A path's score is the sum of its log-probabilities; the
-// temperature and the positions' normalisers are common to all paths, so
-// prefixes rank by the sum of their raw logits, taken left to right in fp64
-// (exact for bf16 logits), with equal sums in lexicographic order of their
-// candidate ranks (tracked as each beam's place among the beams).  With a
-// separable score this gives the W best paths of the whole lattice.
-#include <climits>
-
+// token); the paths are the W best of the lattice, the paths a left-to-right
+// beam of width W keeps.  A path's score is the sum of its log-probabilities;
+// the temperature and the positions' normalisers are common to all paths, so
+// paths rank by the sum of their raw logits (exact in fp64 for bf16 logits),
+// with equal sums in lexicographic order of their candidate ranks.  The score
+// being a sum over positions, the W best are found best first: the best path
+// takes every position's first candidate, and every other path enters a
+// frontier once all the paths one rank below it at one position have been
+// taken; W rounds of warp reductions over the frontier replace a beam's
+// gamma steps.
 #include "sdv_device.cuh"
 #include "sdv_plan.h"
 
@@ -40,7 +41,11 @@ namespace sdv {
 namespace {
 
 constexpr int kTopK = 16;                  // list length (mmax <= 16)
-constexpr int kBeamMaxExp = kCpsMaxBeam * kCpsMaxCand;   // expansions per step
+// Frontier entries beyond one per position: the best path adds one per
+// position; the path taken t-th (1 <= t <= W - 2) adds at most t + 3, four
+// from its own deviations and t - 1 for positions where a taken path already
+// deviates (at most 147 for W = 16).
+constexpr int kBeamFrontierExtra = 160;
 
 // Order-preserving 32-bit key of a logit (larger value -> larger key).
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -419,92 +424,88 @@ __global__ void __launch_bounds__(NW * 32, NW <= 4 ? 7 : (NW <= 8 ? 3 : 2)) cps_
     if (lane == 0) a.ncand[row] = n;      // 0 for a row with NaN / +inf / only -inf
 }
 
-// ceil(65536 / n) for n = 1..16: (e * kDivMagic[n]) >> 16 == e / n for e < 256.
-__constant__ unsigned kDivMagic[17] = {0,    65536, 32768, 21846, 16384, 13108, 10923, 9363, 8192,
-                                       7282, 6554,  5958,  5462,  5042,  4682,  4370,  4096};
+// A path of the lattice is its vector of candidate ranks, one per position.
+// Rank 0 is each position's best candidate, so a path differs from the best
+// path (all ranks 0) only at its deviations, the positions of rank > 0.  A
+// top-W path has at most four of them and no rank above W - 1: every path
+// whose ranks are all at or below its own (there are prod_j (r_j + 1) of
+// them) has a key at least as large and comes before it lexicographically,
+// so prod_j (r_j + 1) <= W <= 16.
+//
+// Tag of a path: its deviations in position order, each a 15-bit field
+// (kCpsMaxGamma - position) << 4 | rank, the first in bits 45..59, then
+// 30..44, 15..29, 0..14; unused fields are 0.  Tags of distinct paths differ,
+// and a smaller tag is a lexicographically smaller rank vector: at the first
+// position where two paths differ, the one with the smaller rank there has
+// either the smaller rank in the same field or no deviation at that position
+// (its field, for a later position or none, is smaller).
+constexpr int kTagBits = 15;
+static_assert(kCpsMaxGamma <= 2047 && kCpsMaxCand <= 16, "tag fields hold 11 + 4 bits");
 
-// An integer with the order of a double (keys here are never NaN and never
-// -0: a sum that cancels to zero rounds to +0).  Integer compares keep the
-// ranking off the (slow) fp64 pipe.
-__device__ __forceinline__ long long ordered_i64(double d) {
-    const long long bits = __double_as_longlong(d);
-    return bits ^ ((bits >> 63) & 0x7fffffffffffffffLL);
+__device__ __forceinline__ uint64_t tag_field(int p, int r) {
+    return static_cast<uint64_t>(((kCpsMaxGamma - p) << 4) | r);
 }
 
-// One lattice position as a lane of the beam sees it: the candidate count
-// n (1 at an EOS end), the expanded count nw = min(n, W), the divide
-// constant for e / nw, and expansion e = lane's parent beam, candidate rank
-// and the candidate's raw logit and log-probability.
-struct BeamPos {
-    int n, nw, par, r;
-    unsigned magic;
-    float rl, lp;
-};
+__device__ __forceinline__ unsigned tag_field_at(uint64_t t, int k) {
+    return static_cast<unsigned>(t >> (45 - kTagBits * k)) & 0x7fffu;
+}
 
-__device__ __forceinline__ BeamPos beam_position(const int* nc_s, const float* rl_s, const float* clp_s,
-                                                 int j, int Lc, bool eos_cut, int W, int M, int lane) {
-    BeamPos p;
-    p.n = eos_cut && j == Lc - 1 ? 1 : nc_s[j];          // EOS is kept alone
-    // A parent's expansions come in candidate order (raw logits sorted, ties
-    // by id), so only its first W can be among the W best.
-    p.nw = p.n < W ? p.n : W;
-    // e / nw as a multiply and shift: exact for e < 256 and nw <= 16
-    p.magic = kDivMagic[p.nw];
-    p.par = static_cast<int>((static_cast<unsigned>(lane) * p.magic) >> 16);
-    p.r = lane - p.par * p.nw;
-    p.rl = rl_s[j * M + p.r];                            // r < nw <= M
-    p.lp = clp_s[j * M + p.r];
-    return p;
+// Position of a field (kCpsMaxGamma, past every position, for an unused one).
+__device__ __forceinline__ int field_pos(unsigned f) { return kCpsMaxGamma - static_cast<int>(f >> 4); }
+
+// Rank of the path at position j.
+__device__ __forceinline__ int tag_rank_at(uint64_t t, int j) {
+    int r = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const unsigned f = tag_field_at(t, k);
+        r = f != 0 && field_pos(f) == j ? static_cast<int>(f & 15u) : r;
+    }
+    return r;
+}
+
+// Bits 60 - 15 k .. 59 of a tag: its fields before field k.
+__device__ __forceinline__ uint64_t fields_before(uint64_t t, int k) {
+    return t & ~((1ull << (60 - kTagBits * k)) - 1ull) & ((1ull << 60) - 1ull);
+}
+
+// The path one rank lower at field k (that deviation removed at rank 1).
+__device__ __forceinline__ uint64_t tag_lower(uint64_t t, int k) {
+    const unsigned f = tag_field_at(t, k);
+    if ((f & 15u) > 1u) return t - (1ull << (45 - kTagBits * k));
+    const uint64_t after = t & ((1ull << (45 - kTagBits * k)) - 1ull);
+    return fields_before(t, k) | (after << kTagBits);
 }
 
 __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
-    // dynamic shared memory: the lattice's log-probabilities [G][M] and raw
-    // logits [G][M] (float), counts [G], then the back-pointers [G][W] parent
-    // and [G][W] rank, and the final paths' ranks [W][G]
+    // dynamic shared memory: the frontier (kept-gap bits [F], tags [F]),
+    // then the staged lattice: raw logits, log-probabilities and ids of the
+    // ranks below min(W, mmax) of every position [G][Wc], and the counts [G]
     extern __shared__ __align__(16) unsigned char s_raw[];
-    __shared__ double x_key[kBeamMaxExp];      // this step's expansions
-    __shared__ long long x_ord[kBeamMaxExp];   // x_key as an order-preserving integer
-    __shared__ float x_score[kBeamMaxExp];
-    __shared__ int x_lx[kBeamMaxExp];
-    __shared__ double b_key[kCpsMaxBeam];      // the beams
-    __shared__ float b_score[kCpsMaxBeam];
-    __shared__ int b_lex[kCpsMaxBeam];
-    __shared__ double n_key[kCpsMaxBeam];      // the beams being chosen
-    __shared__ float n_score[kCpsMaxBeam];
-    __shared__ int n_lx[kCpsMaxBeam];
-    __shared__ int s_src[kCpsMaxBeam];         // beam t's expansion (ranked path)
+    __shared__ uint64_t s_out[kCpsMaxBeam];     // the chosen paths' tags, best first
     const int b = blockIdx.x;
     const int lane = threadIdx.x;
     const int G = a.G, W = a.beam, M = a.mmax;
-    float* clp_s = reinterpret_cast<float*>(s_raw);
-    float* rl_s = clp_s + G * M;
-    int* nc_s = reinterpret_cast<int*>(rl_s + G * M);
-    unsigned char* bp_parent = reinterpret_cast<unsigned char*>(nc_s + G);
-    unsigned char* bp_rank = bp_parent + G * W;
-    unsigned char* path_rank = bp_rank + G * W;
+    const int Wc = W < M ? W : M;
+    const int F = G + kBeamFrontierExtra;
+    uint64_t* f_gap = reinterpret_cast<uint64_t*>(s_raw);
+    uint64_t* f_tag = f_gap + F;
+    float* rl_s = reinterpret_cast<float*>(f_tag + F);
+    float* lp_s = rl_s + G * Wc;
+    int* id_s = reinterpret_cast<int*>(lp_s + G * Wc);
+    int* nc_s = id_s + G * Wc;
     int32_t* cids = a.cand_ids + static_cast<int64_t>(b) * G * M;
     float* clp = a.cand_logp + static_cast<int64_t>(b) * G * M;
     float* crl = a.cand_logit + static_cast<int64_t>(b) * G * M;
     int32_t* nc = a.ncand + static_cast<int64_t>(b) * G;
-    if ((G * M) % 4 == 0 &&
-        ((reinterpret_cast<uintptr_t>(clp) | reinterpret_cast<uintptr_t>(crl)) & 15u) == 0) {
-        const float4* c4 = reinterpret_cast<const float4*>(clp);
-        const float4* r4 = reinterpret_cast<const float4*>(crl);
-        float4* cs4 = reinterpret_cast<float4*>(clp_s);
-        float4* rs4 = reinterpret_cast<float4*>(rl_s);
-#pragma unroll 4
-        for (int i = lane; i < G * M / 4; i += 32) {
-            cs4[i] = c4[i];
-            rs4[i] = r4[i];
+    for (int j = lane; j < G; j += 32) {
+        for (int r = 0; r < Wc; ++r) {
+            rl_s[j * Wc + r] = crl[j * M + r];
+            lp_s[j * Wc + r] = clp[j * M + r];
+            id_s[j * Wc + r] = cids[j * M + r];
         }
-    } else {
-#pragma unroll 4
-        for (int i = lane; i < G * M; i += 32) {
-            clp_s[i] = clp[i];
-            rl_s[i] = crl[i];
-        }
+        nc_s[j] = nc[j];
     }
-    for (int i = lane; i < G; i += 32) nc_s[i] = nc[i];
     __syncwarp();
 
     // the lattice: cut at the first position whose best candidate is EOS
@@ -513,7 +514,7 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
     if (a.eos_id >= 0) {
         for (int j0 = 0; j0 < G; j0 += 32) {        // lanes test 32 positions at a time
             const int j = j0 + lane;
-            const bool hit = j < G && nc_s[j] > 0 && cids[j * M] == a.eos_id;
+            const bool hit = j < G && nc_s[j] > 0 && id_s[j * Wc] == a.eos_id;
             const unsigned mask = __ballot_sync(0xffffffffu, hit);
             if (mask) {
                 Lc = j0 + __ffs(mask);
@@ -523,162 +524,148 @@ __global__ void __launch_bounds__(32) cps_beam_kernel(const CpsArgs a) {
         }
     }
     bool empty = false;
-    for (int j = lane; j < Lc; j += 32) empty |= nc_s[j] == 0;
+    for (int j = lane; j < Lc; j += 32) empty |= nc_s[j] <= 0;
     empty = __any_sync(0xffffffffu, empty);
 
-    // Beams, lane w holding beam w: order key (sum of raw logits, fp64:
-    // exact for bf16 logits, and the same operations as any left-to-right
-    // fp64 sum), score (sum of log-probabilities) and place among the beams
-    // in lexicographic order of their candidate ranks (the tie rule).
-    double bkey = 0.0;
-    float bscore = 0.0f;
-    int blex = 0;
-    int ncur = 1;
-    // The per-lane constants of the next position are independent of the
-    // beams, so they are read one position ahead of their use.
-    BeamPos nxt = {};
-    if (Lc > 0 && !empty) nxt = beam_position(nc_s, rl_s, clp_s, 0, Lc, eos_cut, W, M, lane);
-    for (int j = 0; j < Lc && !empty; ++j) {
-        const BeamPos cur = nxt;
-        if (j + 1 < Lc) nxt = beam_position(nc_s, rl_s, clp_s, j + 1, Lc, eos_cut, W, M, lane);
-        const int n = cur.n, nw = cur.nw;
-        const unsigned magic = cur.magic;
-        const int E = ncur * nw;
-        const int keep = E < W ? E : W;
-        if (E <= 32) {
-            // one expansion per lane: e = lane takes candidate cur.r of beam cur.par
-            const bool valid = lane < E;
-            const double key = __shfl_sync(0xffffffffu, bkey, cur.par) + static_cast<double>(cur.rl);
-            const float sc = __shfl_sync(0xffffffffu, bscore, cur.par) + cur.lp;
-            // place in lexicographic order of (parent's place, candidate rank): below E
-            const int lx = __shfl_sync(0xffffffffu, blex, cur.par) * nw + cur.r;
-            const long long ord = ordered_i64(key);
-            int src = 0;                       // lane t < keep: the expansion that becomes beam t
-            if (keep <= 8) {
-                // The kept expansions one at a time, best first: the largest
-                // key (its high word, then its low word), ties to the smaller
-                // lexicographic place.  Three warp reductions a round.
-                const unsigned long long u = static_cast<unsigned long long>(ord) ^ 0x8000000000000000ull;
-                const unsigned hi = static_cast<unsigned>(u >> 32), lo = static_cast<unsigned>(u);
-                const unsigned tag = (static_cast<unsigned>(lx) << 5) | static_cast<unsigned>(lane);
-                bool left = valid;
-                for (int t = 0; t < keep; ++t) {
-                    const unsigned m1 = __reduce_max_sync(0xffffffffu, left ? hi : 0u);
-                    const bool c1 = left && hi == m1;
-                    const unsigned m2 = __reduce_max_sync(0xffffffffu, c1 ? lo : 0u);
-                    const bool c2 = c1 && lo == m2;
-                    const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, c2 ? tag : 0xffffffffu) & 31u);
-                    left = left && lane != win;
-                    src = lane == t ? win : src;
-                }
-            } else {
-                // every expansion's rank (how many come before it), four
-                // sources a round so that their shuffles go out together
-                const long long o = valid ? ord : LLONG_MIN;
-                int rank = 0;
-                for (int s0 = 0; s0 < E; s0 += 4) {
+    // Best-first enumeration.  A path's key is the sum of its raw logits; the
+    // best path's key minus it is its gap, the sum over its deviations of
+    // rl_j(0) - rl_j(r_j) (each difference and the sum in fp64, in position
+    // order: exact for bf16 logits), so keys descending are gaps ascending.
+    // The order (gap asc, tag asc) is the order (key desc, ranks
+    // lexicographically asc), and a path never comes before one whose ranks
+    // are all at or below its own.  So the best path is taken first, and a
+    // path joins the frontier once every path one rank below it at one
+    // position has been taken; the next path taken is the frontier's first.
+    // The first W taken are the W best paths of the lattice, which a beam of
+    // width W keeps (the key is a sum over positions).
+    int np = 0;
+    if (!empty) {
+        np = 1;                                   // the best path, tag 0
+        if (lane == 0) s_out[0] = 0;
+        __syncwarp();
+        int nf = 0;                               // frontier entries ever added
+        auto gap_of = [&](int p, int r) {
+            return static_cast<double>(rl_s[p * Wc]) - static_cast<double>(rl_s[p * Wc + r]);
+        };
+        // Offer the paths one rank above `v` at one position.
+        auto expand = [&](uint64_t v, int taken) {
+            for (int j0 = 0; j0 < Lc; j0 += 32) {
+                const int j = j0 + lane;
+                bool ok = false;
+                uint64_t ct = 0, cg = 0;
+                if (j < Lc) {
+                    // ranks at or above min(W, mmax) cannot be among the W
+                    // best (nor lie in the staged lattice)
+                    const int nj = eos_cut && j == Lc - 1 ? 1 : (nc_s[j] < Wc ? nc_s[j] : Wc);
+                    // v's field at position j, and how many fields come before j
+                    int kj = -1, before = 0;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int s = s0 + u < E ? s0 + u : lane;        // lane itself adds 0
-                        const long long o2 = __shfl_sync(0xffffffffu, o, s);
-                        const int l2 = __shfl_sync(0xffffffffu, lx, s);
-                        rank += (o2 > o) || (o2 == o && l2 < lx);
+                    for (int k = 0; k < 4; ++k) {
+                        const unsigned f = tag_field_at(v, k);
+                        if (f != 0 && field_pos(f) == j) kj = k;
+                        before += f != 0 && field_pos(f) < j;
+                    }
+                    const int rn = (kj >= 0 ? static_cast<int>(tag_field_at(v, kj) & 15u) : 0) + 1;
+                    // a fifth deviation cannot be among the W <= 16 best
+                    ok = rn < nj && (kj >= 0 || tag_field_at(v, 3) == 0);
+                    if (ok) {
+                        if (kj >= 0) {
+                            ct = v + (1ull << (45 - kTagBits * kj));
+                        } else {
+                            const uint64_t after = v & ((1ull << (60 - kTagBits * before)) - 1ull);
+                            ct = fields_before(v, before) |
+                                 (tag_field(j, 1) << (45 - kTagBits * before)) | (after >> kTagBits);
+                        }
+                        int prod = 1;
+                        double g = 0.0;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const unsigned f = tag_field_at(ct, k);
+                            if (f != 0) {
+                                prod *= static_cast<int>(f & 15u) + 1;
+                                g += gap_of(field_pos(f), static_cast<int>(f & 15u));
+                            }
+                        }
+                        ok = prod <= W;
+                        // every other path one rank below it has been taken
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const unsigned f = tag_field_at(ct, k);
+                            if (ok && f != 0 && field_pos(f) != j) {
+                                const uint64_t d = tag_lower(ct, k);
+                                bool found = false;
+                                for (int t = 0; t < taken; ++t) found |= s_out[t] == d;
+                                ok = found;
+                            }
+                        }
+                        cg = static_cast<uint64_t>(__double_as_longlong(g));
                     }
                 }
-                if (valid && rank < keep) s_src[rank] = lane;
-                __syncwarp();
-                if (lane < keep) src = s_src[lane];
-                __syncwarp();
-            }
-            // beam t takes over its expansion's state; its new place among
-            // the kept beams counts the kept places below its own
-            const double nkey = __shfl_sync(0xffffffffu, key, src);
-            const float nsc = __shfl_sync(0xffffffffu, sc, src);
-            const int nlx = __shfl_sync(0xffffffffu, lx, src);
-            const unsigned kept = __reduce_or_sync(0xffffffffu, lane < keep ? 1u << nlx : 0u);
-            if (lane < keep) {
-                const int sp = static_cast<int>((static_cast<unsigned>(src) * magic) >> 16);
-                bp_parent[j * W + lane] = static_cast<unsigned char>(sp);
-                bp_rank[j * W + lane] = static_cast<unsigned char>(src - sp * nw);
-                bkey = nkey;
-                bscore = nsc;
-                blex = __popc(kept & ((1u << nlx) - 1u));
-            }
-        } else {
-            // more expansions than lanes: through shared memory
-            if (lane < ncur) {
-                b_key[lane] = bkey;
-                b_score[lane] = bscore;
-                b_lex[lane] = blex;
+                const unsigned bal = __ballot_sync(0xffffffffu, ok);
+                const int slot = nf + __popc(bal & ((1u << lane) - 1u));
+                if (ok && slot < F) {
+                    f_gap[slot] = cg;
+                    f_tag[slot] = ct;
+                }
+                nf += __popc(bal);
             }
             __syncwarp();
-            for (int e = lane; e < E; e += 32) {
-                const int par = static_cast<int>((e * magic) >> 16), r = e - par * nw;
-                const double key = b_key[par] + static_cast<double>(rl_s[j * M + r]);
-                x_key[e] = key;
-                x_ord[e] = ordered_i64(key);
-                x_score[e] = b_score[par] + clp_s[j * M + r];
-                x_lx[e] = b_lex[par] * n + r;
-            }
-            __syncwarp();
-            // each expansion's rank: how many expansions come before it (key
-            // desc, then lexicographic place asc); the first W are kept
-            for (int e = lane; e < E; e += 32) {
-                const long long k = x_ord[e];
-                const int l = x_lx[e];
-                int rank = 0, e2 = 0;
-                for (; e2 + 4 <= E; e2 += 4) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const long long k2 = x_ord[e2 + u];
-                        rank += (k2 > k) || (k2 == k && x_lx[e2 + u] < l);
-                    }
-                }
-                for (; e2 < E; ++e2) {
-                    const long long k2 = x_ord[e2];
-                    rank += (k2 > k) || (k2 == k && x_lx[e2] < l);
-                }
-                if (rank < keep) {
-                    const int par = static_cast<int>((e * magic) >> 16);
-                    n_key[rank] = x_key[e];
-                    n_score[rank] = x_score[e];
-                    n_lx[rank] = l;
-                    bp_parent[j * W + rank] = static_cast<unsigned char>(par);
-                    bp_rank[j * W + rank] = static_cast<unsigned char>(e - par * nw);
+        };
+        if (W > 1) expand(0ull, 1);
+        for (int t = 1; t < W && nf - (t - 1) > 0; ++t) {
+            // the frontier's first entry: gap bits (a non-negative double
+            // orders as its bits) then tag; taken entries hold all-ones
+            uint64_t bg = ~0ull, bt = ~0ull;
+            int bi = 0;
+            const int n_scan = nf < F ? nf : F;
+            for (int i = lane; i < n_scan; i += 32) {
+                const uint64_t g = f_gap[i], tg = f_tag[i];
+                if (g < bg || (g == bg && tg < bt)) {
+                    bg = g;
+                    bt = tg;
+                    bi = i;
                 }
             }
-            __syncwarp();
-            if (lane < keep) {
-                const int l = n_lx[lane];
-                int pos = 0;
-                for (int t = 0; t < keep; ++t) pos += n_lx[t] < l;
-                bkey = n_key[lane];
-                bscore = n_score[lane];
-                blex = pos;
+            const unsigned g_hi = __reduce_min_sync(0xffffffffu, static_cast<unsigned>(bg >> 32));
+            bool c = static_cast<unsigned>(bg >> 32) == g_hi;
+            const unsigned g_lo = __reduce_min_sync(0xffffffffu, c ? static_cast<unsigned>(bg) : ~0u);
+            c = c && static_cast<unsigned>(bg) == g_lo;
+            const unsigned t_hi = __reduce_min_sync(0xffffffffu, c ? static_cast<unsigned>(bt >> 32) : ~0u);
+            c = c && static_cast<unsigned>(bt >> 32) == t_hi;
+            const unsigned t_lo = __reduce_min_sync(0xffffffffu, c ? static_cast<unsigned>(bt) : ~0u);
+            c = c && static_cast<unsigned>(bt) == t_lo;
+            const unsigned who = __ballot_sync(0xffffffffu, c);
+            const int wi = __shfl_sync(0xffffffffu, bi, __ffs(who) - 1);
+            const uint64_t v = (static_cast<uint64_t>(t_hi) << 32) | t_lo;
+            if (lane == 0) {
+                f_gap[wi] = ~0ull;
+                f_tag[wi] = ~0ull;
+                s_out[t] = v;
             }
             __syncwarp();
-        }
-        ncur = keep;
-    }
-    __syncwarp();
-    const int np = empty ? 0 : ncur;
-    // back-track the final beams' candidate ranks in shared memory, then
-    // gather their ids with independent loads
-    if (lane < np) {
-        int cur = lane;
-        for (int j = Lc - 1; j >= 0; --j) {
-            path_rank[lane * G + j] = bp_rank[j * W + cur];
-            cur = bp_parent[j * W + cur];
+            np = t + 1;
+            if (t + 1 < W) expand(v, t + 1);
         }
     }
-    if (lane < W)
-        a.path_logp[static_cast<int64_t>(b) * W + lane] = lane < np ? bscore : -INFINITY;
     __syncwarp();
+    // Each path's score, its log-probabilities summed in fp32 in a fixed
+    // order: lane l adds positions l, l + 32, ... in turn, then the lanes'
+    // partial sums are added by an xor butterfly (every lane ends with the
+    // same bits).  Its ids are gathered position by position.
+    float* plp = a.path_logp + static_cast<int64_t>(b) * W;
     int32_t* paths = a.paths + static_cast<int64_t>(b) * W * G;
-#pragma unroll 4
-    for (int i = lane; i < W * G; i += 32) {
-        const int w = i / G, j = i - w * G;
-        paths[i] = w < np && j < Lc ? cids[j * M + path_rank[i]] : -1;
+    for (int w = 0; w < W; ++w) {
+        const uint64_t v = w < np ? s_out[w] : 0ull;
+        float part = 0.0f;
+        for (int j = lane; j < G; j += 32) {
+            const int r = tag_rank_at(v, j);
+            const bool on = w < np && j < Lc;
+            if (on) part += lp_s[j * Wc + r];
+            paths[static_cast<int64_t>(w) * G + j] = on ? id_s[j * Wc + r] : -1;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) plp[w] = w < np ? part : -INFINITY;
     }
     if (lane == 0) {
         a.npaths[b] = np;
@@ -722,8 +709,11 @@ cudaError_t launch_cps_prune(const CpsArgs& a, bool bf16, cudaStream_t s) {
 }
 
 cudaError_t launch_cps_beam(const CpsArgs& a, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(a.G) * a.mmax * 8 + static_cast<size_t>(a.G) * 4 +
-                        static_cast<size_t>(3) * a.G * a.beam;
+    // the frontier (16 bytes an entry), the lattice's first min(W, mmax)
+    // ranks (raw logit, log-probability, id) and counts
+    const size_t wc = static_cast<size_t>(a.beam < a.mmax ? a.beam : a.mmax);
+    const size_t smem = (static_cast<size_t>(a.G) + kBeamFrontierExtra) * 16 +
+                        static_cast<size_t>(a.G) * wc * 12 + static_cast<size_t>(a.G) * 4;
     if (smem > 48 * 1024) {
         const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(cps_beam_kernel), smem);
         if (e != cudaSuccess) return e;

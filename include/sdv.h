@@ -341,14 +341,17 @@ sdv_status sdv_profile_read(sdv_ctx* ctx, float* ms_avg, int* steps);
  *      zero (logit -inf) is never a candidate;
  *   2. the lattice ends at the first position whose most likely token is
  *      eos_id, which is kept alone as the last token (eos_id < 0: no cut);
- *   3. a beam of width `beam` runs left to right over the lattice, scoring a
+ *   3. the paths a beam of width `beam` keeps over the lattice, scoring a
  *      path by the sum of its log-probabilities (drafter confidence; the
  *      page's causal fluency proxy is not specified there and is not used).
  *      The temperature and each position's normaliser are common to all of a
- *      sequence's paths, so paths rank by the sum of their raw logits, taken
- *      left to right in fp64 (exact for bf16 logits); equal sums go to the
- *      path whose candidate ranks come first lexicographically.  The result
- *      is the `beam` best paths of the lattice, best first.
+ *      sequence's paths, so paths rank by the sum of their raw logits (in
+ *      fp64, exact for bf16 logits); equal sums go to the path whose
+ *      candidate ranks come first lexicographically.  With a score that sums
+ *      over positions the beam keeps the `beam` best paths of the lattice,
+ *      and these are found best first rather than position by position.  The
+ *      result is those paths, best first, each with its log-probability
+ *      summed in fp32 in a fixed order.
  * The paths serve as the K = beam drafts of a verification step
  * (SDV_FLAG_SHARED_Q, with the same q).
  * Arguments: q_marginals device [B][gamma][V] bf16 or fp32 (16-byte aligned,
@@ -392,7 +395,9 @@ sdv_status sdv_cps_ex(int B, int gamma, int V, sdv_dtype dtype, void* stream,
  * q_marginals / temperature(_per_seq) and writes out_cand_ids, out_cand_logp,
  * out_cand_logit and out_ncand exactly as sdv_cps documents them, before the
  * cut.  sdv_cps_beam is steps 2-3: it reads the lattice (as sdv_cps_prune
- * wrote it), trims it in place at an EOS end (one candidate at the EOS
+ * wrote it: each position's candidates in decreasing order of logit, at most
+ * mmax of them; a count of 0 or less leaves the sequence without a path),
+ * trims it in place at an EOS end (one candidate at the EOS
  * position, none past it) and writes the paths.  V is only used to check
  * eos_id.  Argument rules, ownership and errors as for sdv_cps; sdv_cps is
  * sdv_cps_prune followed by sdv_cps_beam on `stream`.

@@ -180,8 +180,8 @@ def test_cps_halves_equal_whole():
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 def test_cps_exact_ties_on_a_coarse_grid(dt, beam):
     """Logits on a quarter grid: many paths tie exactly in their score; the
-    order must be the tie rule's on both sides, not rounding's.  Beam 3 keeps
-    every step within one warp's lanes; beam 7 also ranks 49 expansions."""
+    order must be the tie rule's on both sides, not rounding's.  Beam 7 also
+    takes paths with two and three deviations from the best path."""
     B, G, V = 6, 8, 2000
     gen = torch.Generator(device="cuda")
     gen.manual_seed(13)
@@ -245,8 +245,9 @@ def test_cps_deterministic_and_argmax_path():
 
 
 def test_cps_largest_lattice():
-    """gamma 1024 positions, 16 candidates, beam 16 (the limits: 190 KB of
-    shared memory for the beam, 256 expansions a step) against the oracle."""
+    """gamma 1024 positions, 16 candidates, beam 16 (the limits: 216 KB of
+    shared memory for the beam, a frontier of up to 1 171 paths) against the
+    oracle."""
     gen = torch.Generator(device="cuda")
     gen.manual_seed(60)
     q = (torch.randn((2, 1024, 256), generator=gen, device="cuda") * 0.7).to(torch.bfloat16)
