@@ -256,3 +256,66 @@ def test_cps_largest_lattice():
     assert (gpu["npaths"] == 16).all()
     with pytest.raises(bd.SdvError):
         bd.sdv_cps(torch.zeros((1, 1025, 64), dtype=torch.bfloat16, device="cuda"))
+
+
+def _lattice_rows(spec, V, device="cuda"):
+    """Marginal rows whose pruned lattice is exactly `spec`: spec[b][j] is the
+    list of (token, logit) candidates of position j (at most 16, bf16-exact
+    logits within one unit of each other); every other token gets logit -20.
+    With tau 0.999 the cut falls after the last listed token: the mass left
+    after it is below 1e-7 and the mass before it at most 0.98, both far from
+    tau."""
+    B, G = len(spec), len(spec[0])
+    q = torch.full((B, G, V), -20.0)
+    for b in range(B):
+        for j in range(G):
+            for tok, val in spec[b][j]:
+                q[b, j, tok] = val
+    return q.to(torch.bfloat16).to(device)
+
+
+def _cands(n, grid, rng, V):
+    toks = rng.choice(V, size=n, replace=False)
+    return [(int(t), float(rng.choice(grid))) for t in toks]
+
+
+@pytest.mark.parametrize("beam", [16, 3])
+def test_cps_beam_frontier_edges(beam):
+    """The best-first beam at its edges, against the oracle's beam: every
+    path tied (only the lexicographic rule orders them), fewer paths than the
+    beam (the frontier runs dry), a single path, a single position, sixteen
+    candidates everywhere on a coarse grid (paths with up to four deviations),
+    and 40 positions (two lanes' worth) with an EOS cut."""
+    rng = np.random.default_rng(71 + beam)
+    V, eos = 64, 7
+    tied = [[(3, 0.0), (9, 0.0)]] * 5
+    few = [[(1, 0.0), (2, 0.5)], [(3, 0.5), (4, 0.0)], [(5, 0.25), (6, 0.25)], [(8, 0.0)], [(10, 0.0)]]
+    single = [[(11 + j, 0.0)] for j in range(5)]
+    wide = [_cands(16, [0.0, 0.5, 1.0], rng, V) if j in (0, 4) else [(12, 0.0)] for j in range(5)]
+    grid = [_cands(4, [0.0, 0.5, 1.0], rng, V) for _ in range(5)]
+    q = _lattice_rows([tied, few, single, wide, grid], V)
+    gpu, orc = run_both(q, 1.0, 0.999, 16, beam)
+    assert compare_cps(gpu, orc, "edges", _qf(q)) == 0
+    assert list(gpu["npaths"]) == [min(beam, 32), min(beam, 8), 1, beam, beam]
+
+    one = _lattice_rows([[_cands(10, [0.0, 0.5], rng, V)]], V)      # gamma 1
+    gpu, orc = run_both(one, 1.0, 0.999, 16, beam)
+    assert compare_cps(gpu, orc, "gamma 1", _qf(one)) == 0
+    assert gpu["npaths"][0] == min(beam, 10)
+
+    G = 40
+    deep = []
+    for b in range(3):
+        rows = []
+        for j in range(G):
+            n = 16 if b == 0 else int(rng.integers(1, 17))
+            c = _cands(n, [0.0, 0.5, 1.0], rng, V)
+            c = [(t, v) for t, v in c if t != eos] or [(eos + 1, 0.0)]
+            rows.append(c)
+        deep.append(rows)
+    deep[2][35] = [(eos, 1.0), (20, 0.0)]                  # sequence 2 ends at position 35
+    q = _lattice_rows(deep, V)
+    gpu, orc = run_both(q, 1.0, 0.999, 16, beam, eos=eos)
+    assert compare_cps(gpu, orc, "gamma 40", _qf(q)) == 0
+    assert gpu["lat_len"][2] == 36 and gpu["lat_len"][0] == G
+    assert (gpu["npaths"] == beam).all()
