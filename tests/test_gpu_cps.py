@@ -5,8 +5,9 @@ Bar: candidate ids and counts, lattice lengths, path ids and path counts
 bit-exact, except sequences the oracle flags in its band (a cumulative mass
 within 1e-5 of tau at a cut); candidate raw logits exact; candidate
 log-probabilities and path scores within 1e-4 (absolute, relative for
-scores).  The path order needs no band: both sides rank paths by the same
-left-to-right fp64 sums of raw logits."""
+scores).  The path order needs no band: the oracle ranks paths by fp64 sums
+of raw logits and the kernel by fp64 sums of their differences to the best
+path's, both exact for these logits, so they order paths alike."""
 import numpy as np
 import pytest
 import torch
