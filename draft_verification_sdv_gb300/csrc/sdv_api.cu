@@ -25,6 +25,7 @@ struct sdv_ctx {
     int nsm;
     // row pass
     int rp_grid;
+    int row_mode;           // row pass: one CTA per row (see plan_row_mode)
     int chunks;
     int64_t nvec, chunk_vec, rows_p, rows_q, rows_total, items;
     // select / sample
@@ -146,8 +147,9 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
 
     cudaError_t e = cudaGetDevice(&ctx->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->nsm, cudaDevAttrMultiProcessorCount, ctx->device);
-    int bps = 0;
+    int bps = 0, rbps = 0;
     if (e == cudaSuccess) e = rowpass_occupancy(ctx->bf16, &bps);
+    if (e == cudaSuccess) e = rowpass_row_occupancy(ctx->bf16, &rbps);
     if (e != cudaSuccess || bps < 1) {
         sdv_destroy(ctx);
         return SDV_ERR_CUDA;
@@ -161,9 +163,17 @@ sdv_status sdv_create_ex(sdv_ctx** out, int B, int K, int gamma, int V, sdv_dtyp
                                                 : static_cast<int64_t>(B) * K * gamma;
     ctx->rows_total = ctx->rows_p + ctx->rows_q;
     const int64_t resident_warps = static_cast<int64_t>(ctx->nsm) * bps * (kRowPassThreads / 32);
-    plan_rowpass_chunks(ctx->rows_total, ctx->nvec, resident_warps, 0, &ctx->chunks, &ctx->chunk_vec);
+    ctx->row_mode = plan_row_mode(ctx->rows_total, static_cast<int64_t>(ctx->nsm) * rbps, ctx->nvec);
+    if (ctx->row_mode) {
+        ctx->chunks = 1;
+        ctx->chunk_vec = ctx->nvec;
+    } else {
+        plan_rowpass_chunks(ctx->rows_total, ctx->nvec, resident_warps, 0, &ctx->chunks, &ctx->chunk_vec);
+    }
     ctx->items = ctx->rows_total * ctx->chunks;
-    ctx->rp_grid = static_cast<int>((ctx->items + (kRowPassThreads / 32) - 1) / (kRowPassThreads / 32));
+    ctx->rp_grid = ctx->row_mode ? static_cast<int>(ctx->items)
+                                 : static_cast<int>((ctx->items + (kRowPassThreads / 32) - 1) /
+                                                    (kRowPassThreads / 32));
 
     // Select plan.
     ctx->sel_smem = select_smem_bytes(K, gamma);
@@ -288,6 +298,7 @@ cudaError_t enqueue_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     // rows come after them in item order)
     ra.items = with_q ? ctx->items : ctx->rows_p * ctx->chunks;
     ra.lens = draft_len;
+    ra.row_mode = ctx->row_mode;
     const cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->stream, pdl);
     if (e == cudaSuccess) {
         ctx->rows_ready = with_q ? 2 : 1;

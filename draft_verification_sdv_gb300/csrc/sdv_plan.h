@@ -131,6 +131,9 @@ struct RowPassArgs {
     int64_t chunk_vec;      // vectors per chunk
     int64_t items;          // rows_total * chunks
     const int32_t* lens = nullptr;   // [B] draft length per sequence (rows past it are skipped)
+    // one CTA of kRowModeThreads per row (items = rows, chunks = 1) instead
+    // of one warp per item
+    int row_mode = 0;
 };
 
 // Select / scan (K2): one CTA per sequence.
@@ -263,10 +266,27 @@ int sample_active_clusters(bool bf16, int cluster, size_t smem);
 // Sequences up to which the sampling pass uses clusters of 16 CTAs (more
 // sequences keep 8, so that all clusters of a batch fit the GPU at once).
 constexpr int kWideSampleMaxB = 16;
-// Resident blocks per SM of the row-pass kernel.
+// Resident blocks per SM of the row-pass kernel, in item and in row mode.
 cudaError_t rowpass_occupancy(bool bf16, int* blocks_per_sm);
+cudaError_t rowpass_row_occupancy(bool bf16, int* blocks_per_sm);
 
 constexpr int kRowPassThreads = 256;
+
+// Row mode: one CTA of four warps per row, the row's 4 KB blocks (kRowBlockVec
+// vectors) dealt to the warps in a fixed interleaved order and merged in the
+// CTA into one partial per row.  Used when the rows fill between three
+// quarters and all of one wave of such CTAs (eight per SM): every row streams
+// at once, with no wave turnover, and the select kernel merges one partial
+// per row.  On the self-selection shape (1 056 rows of 152 064 logits) item
+// mode needs 19 chunks a row to fill its waves.
+constexpr int kRowModeThreads = 128;
+constexpr int kRowModeMinBlocks = 8;
+constexpr int64_t kRowBlockVec = 256;
+
+inline bool plan_row_mode(int64_t rows, int64_t row_slots, int64_t nvec) {
+    return row_slots > 0 && rows <= row_slots && 4 * rows >= 3 * row_slots &&
+           nvec >= (kRowModeThreads / 32) * kRowBlockVec;
+}
 
 // Row-pass chunking.  One warp reduces one (row, chunk) item and the grid is
 // one CTA per kRowPassThreads / 32 items, scheduled by the hardware in many

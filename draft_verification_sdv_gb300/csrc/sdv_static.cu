@@ -42,6 +42,7 @@ struct StaticDevice {
     void* scratch;        // device address of g_static_scratch on this device
     int nsm;
     int rowpass_blocks[2];   // resident row-pass CTAs per SM: [fp32, bf16]
+    int row_blocks[2];       // the same in row mode
     int smem_optin;          // largest dynamic shared memory a block may opt into
 };
 
@@ -58,12 +59,14 @@ cudaError_t setup_device(int dev, StaticDevice** out) {
         void* ptr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
         if (e != cudaSuccess) return e;
-        int nsm = 0, optin = 0, bps_f32 = 0, bps_bf16 = 0;
+        int nsm = 0, optin = 0, bps_f32 = 0, bps_bf16 = 0, rbps_f32 = 0, rbps_bf16 = 0;
         e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
             e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e == cudaSuccess) e = rowpass_occupancy(false, &bps_f32);
         if (e == cudaSuccess) e = rowpass_occupancy(true, &bps_bf16);
+        if (e == cudaSuccess) e = rowpass_row_occupancy(false, &rbps_f32);
+        if (e == cudaSuccess) e = rowpass_row_occupancy(true, &rbps_bf16);
         if (e != cudaSuccess) return e;
         if (bps_f32 < 1 || bps_bf16 < 1 || optin <= 4096) return cudaErrorInvalidConfiguration;
         // Let both kernels take up to the device's opt-in limit, once: the
@@ -77,6 +80,8 @@ cudaError_t setup_device(int dev, StaticDevice** out) {
         d.smem_optin = optin;
         d.rowpass_blocks[0] = bps_f32;
         d.rowpass_blocks[1] = bps_bf16;
+        d.row_blocks[0] = rbps_f32;
+        d.row_blocks[1] = rbps_bf16;
         d.ready = true;
     }
     *out = &d;
@@ -132,7 +137,14 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     if (rows_total > max_items) return SDV_ERR_SCRATCH;
     int chunks = 0;
     int64_t chunk_vec = 0;
-    plan_rowpass_chunks(rows_total, nvec, resident_warps, max_items, &chunks, &chunk_vec);
+    const bool row_mode = plan_row_mode(
+        rows_total, static_cast<int64_t>(sd->nsm) * sd->row_blocks[dtype == SDV_BF16 ? 1 : 0], nvec);
+    if (row_mode) {
+        chunks = 1;
+        chunk_vec = nvec;
+    } else {
+        plan_rowpass_chunks(rows_total, nvec, resident_warps, max_items, &chunks, &chunk_vec);
+    }
     const int64_t items = rows_total * chunks;
     if (items > max_items) return SDV_ERR_SCRATCH;
     const size_t part_bytes = round_up(static_cast<size_t>(items) * sizeof(float2), 256);
@@ -168,6 +180,7 @@ extern "C" sdv_status sdv_verify_static(int B, int K, int gamma, int V, sdv_dtyp
     ra.nvec = nvec;
     ra.chunk_vec = chunk_vec;
     ra.items = items;
+    ra.row_mode = row_mode ? 1 : 0;
     if (launch_rowpass(ra, dtype == SDV_BF16, s, true) != cudaSuccess) return SDV_ERR_CUDA;
 
     SelectArgs sa;
