@@ -330,7 +330,8 @@ inline size_t select_smem_bytes(int K, int G) {
 }
 
 // Lanes per row merge in the select kernel: the largest power of two up to
-// 32, and up to the chunk count, for which the K * G pairs and K bonus rows
+// 32, and up to the first power of two at or above the chunk count (lanes
+// past the last chunk merge nothing), for which the K * G pairs and K bonus rows
 // of a sequence all fit the CTA's threads in one round.  Few rows with many
 // chunks each (the latency cases) get whole warps; the large batches keep
 // one thread per row.
