@@ -58,9 +58,6 @@ def parse_args():
     ap.add_argument("--decode-step", action="store_true",
                     help="time one whole decode step over one pass's marginals: path search, "
                          "verification of the paths at their lattice lengths, draft-length update")
-    ap.add_argument("--decode-serial", action="store_true",
-                    help="with --decode-step: one stream, the path search before the whole "
-                         "verification (no overlap of the search with the verifier row pass)")
     ap.add_argument("--greedy", action="store_true",
                     help="greedy acceptance: verifier rows only, no drafter rows")
     ap.add_argument("--shared-q", action="store_true",
@@ -626,7 +623,13 @@ def run_decode_step(args, rank, world, bd=None, clocks=None):
     draft-length update from the lattice and accepted lengths.  The path
     search hands the marginal rows' softmax statistics to the verification,
     which therefore streams only the verifier rows.  Large-window shape: B 32,
-    gamma 32, V 152064 bf16, per-sequence temperatures."""
+    gamma 32, V 152064 bf16, per-sequence temperatures.
+
+    The three run in order on one stream, as in a decode loop: the verifier
+    rows are the verifier's distributions at the drafted paths' positions, so
+    they exist only once the search has produced the paths (here they are
+    synthesised up front, standing in for the verifier's forward pass), and
+    the next step's search waits for this step's draft-length update."""
     if bd is None:
         from draft_verification_sdv_gb300 import binding as bd
         bd.load(build=True)
@@ -639,42 +642,21 @@ def run_decode_step(args, rank, world, bd=None, clocks=None):
     w = synth.generate_shared(B, K, G, V, q_sigma=sj.expand(B, G).clone(), temps=temps,
                               seed=55 + 1000 * rank, device=dev)
     eos = 151643                                   # the Qwen2.5 end-of-text id
-    serial = bool(getattr(args, "decode_serial", False))
-    # Two streams: the verifier row pass needs no drafts, so it streams on the
-    # verification stream while the path search runs on its own; the rest of
-    # the verification waits for both.
-    s_rows = torch.cuda.current_stream(dev) if serial else torch.cuda.Stream(device=dev)
-    s_cps = s_rows if serial else torch.cuda.Stream(device=dev)
-    s_rows.wait_stream(torch.cuda.current_stream(dev))
-    s_cps.wait_stream(torch.cuda.current_stream(dev))
+    stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
-    v = bd.Verifier(B, K, G, V, w.dtype, shared_q=True, shared_prefix_row=True, stream=s_rows)
+    v = bd.Verifier(B, K, G, V, w.dtype, shared_q=True, shared_prefix_row=True, stream=stream)
     ctl = bd.DraftLengthController(B, G, window=2, kmin=4, kmax=G, up=2, down=1, device=dev)
-    cps = bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, row_stat=True, stream=s_cps)
+    cps = bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, row_stat=True, stream=stream)
     torch.cuda.synchronize(dev)
     out = None
-    searched, verified = torch.cuda.Event(), torch.cuda.Event()
-    verified.record(s_rows)
 
     def step(i):
         nonlocal out
-        if serial:
-            bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, out=cps, row_stat=True,
-                       stream=s_cps)
-            out = v(w.p_logits, w.q_logits, cps["paths"], seed=i, temps=w.temps, out=out,
-                    draft_len=cps["lat_len"], q_stat=cps["row_stat"])
-        else:
-            # the search overwrites its outputs once the last verification has read them
-            s_cps.wait_event(verified)
-            bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, out=cps, row_stat=True,
-                       stream=s_cps)
-            searched.record(s_cps)
-            v.rows(w.p_logits, w.q_logits, temps=w.temps, with_q=False)
-            s_rows.wait_event(searched)
-            out = v.finish(w.p_logits, w.q_logits, cps["paths"], seed=i, temps=w.temps, out=out,
-                           draft_len=cps["lat_len"], q_stat=cps["row_stat"])
-            verified.record(s_rows)
-        ctl.step(cps["lat_len"], out["accept_len"], stream=s_rows)
+        bd.sdv_cps(w.q_logits, 0.8, 15, K, eos_id=eos, temps=w.temps, out=cps, row_stat=True,
+                   stream=stream)
+        out = v(w.p_logits, w.q_logits, cps["paths"], seed=i, temps=w.temps, out=out,
+                draft_len=cps["lat_len"], q_stat=cps["row_stat"])
+        ctl.step(cps["lat_len"], out["accept_len"], stream=stream)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -689,11 +671,10 @@ def run_decode_step(args, rank, world, bd=None, clocks=None):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0 = time.time()
-    e0.record(s_rows)
-    s_cps.wait_event(e0)
+    e0.record(stream)
     for i in range(args.steps):
         step(i)
-    e1.record(s_rows)             # after the last step's verification, which waited for its search
+    e1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if own_clocks:
@@ -723,9 +704,8 @@ def run_decode_step(args, rank, world, bd=None, clocks=None):
                        "beam": K, "mmax": 15, "tau": 0.8, "eos_id": eos,
                        "marginal_rows": "streamed once (the path search's statistics feed "
                                         "the verification)",
-                       "streams": ("one: path search, then the verification" if serial else
-                                   "two: the path search on its own stream while the verifier "
-                                   "row pass streams; selection and draw after both"),
+                       "order": "one stream: path search, verification of its paths, "
+                                "draft-length update",
                        "lattice_len_mean": float(lat.mean()),
                        "l2": l2_note},
             "committed_tokens_per_s": world * committed / (ms * 1e-3),

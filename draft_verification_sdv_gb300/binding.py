@@ -41,9 +41,6 @@ SIGNATURES = {
     "sdv_verify_qstat": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP,
                               _VP]),
     "sdv_verify_host": (_I, [_VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP]),
-    "sdv_rowpass": (_I, [_VP, _VP, _VP, _F, _VP, _I]),
-    "sdv_verify_from_rows": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _U64, _VP, _VP, _VP, _VP,
-                                  _VP]),
     "sdv_sync": (_I, [_VP]),
     "sdv_last_error": (ctypes.c_char_p, [_VP]),
     "sdv_destroy": (None, [_VP]),
@@ -196,28 +193,6 @@ def sdv_verify_len(ctx, p_logits, q_logits, drafts, draft_len, temperature, temp
         ctx, _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
         _dev_ptr(drafts, torch.int32, "drafts"), _dev_ptr(draft_len, torch.int32, "draft_len"),
         float(temperature), _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
-        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
-        _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
-        _dev_ptr(out_next_token, torch.int32, "out_next_token"),
-        _dev_ptr(out_scores, torch.float32, "out_scores"),
-        _dev_ptr(out_lse, torch.float32, "out_lse"))
-
-
-def sdv_rowpass(ctx, p_logits, q_logits, temperature, temperature_per_seq, with_q_rows=True) -> int:
-    return load().sdv_rowpass(ctx, _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
-                              float(temperature),
-                              _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
-                              1 if with_q_rows else 0)
-
-
-def sdv_verify_from_rows(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
-                         temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
-                         out_scores=None, out_lse=None) -> int:
-    return load().sdv_verify_from_rows(
-        ctx, _dev_ptr(p_logits, name="p_logits"), _dev_ptr(q_logits, name="q_logits"),
-        _dev_ptr(drafts, torch.int32, "drafts"), _dev_ptr(draft_len, torch.int32, "draft_len"),
-        _dev_ptr(q_row_stat, torch.float32, "q_row_stat"), float(temperature),
-        _dev_ptr(temperature_per_seq, torch.float32, "temperature_per_seq"),
         int(seed) & 0xFFFFFFFFFFFFFFFF, _dev_ptr(out_sel, torch.int32, "out_sel"),
         _dev_ptr(out_accept_len, torch.int32, "out_accept_len"),
         _dev_ptr(out_next_token, torch.int32, "out_next_token"),
@@ -494,43 +469,6 @@ class Verifier:
             st = sdv_verify_len(self.ctx, p_logits, q_logits, drafts, draft_len, temperature, temps,
                                 seed, out["sel"], out["accept_len"], out["next_token"],
                                 out.get("scores"), out.get("lse"))
-        if st != SDV_OK:
-            raise SdvError(st, sdv_last_error(self.ctx))
-        return out
-
-    def rows(self, p_logits, q_logits, temperature: float = 1.0,
-             temps: Optional[torch.Tensor] = None, with_q: bool = True) -> None:
-        """The row pass alone (sdv_rowpass): the softmax statistics of the
-        verifier rows (and of the drafter rows when `with_q`), to be finished
-        by `finish` once the drafts exist."""
-        _per_seq(temps, self.B, "temps")
-        st = sdv_rowpass(self.ctx, p_logits, q_logits, temperature, temps, with_q)
-        if st != SDV_OK:
-            raise SdvError(st, sdv_last_error(self.ctx))
-
-    def finish(self, p_logits, q_logits, drafts, temperature: float = 1.0, seed: int = 0,
-               temps: Optional[torch.Tensor] = None, scores: bool = False, lse: bool = False,
-               out: Optional[dict] = None, draft_len: Optional[torch.Tensor] = None,
-               q_stat: Optional[torch.Tensor] = None) -> dict:
-        """The rest of the step on the statistics of the last row pass
-        (sdv_verify_from_rows); arguments and outputs as for a call."""
-        B, K, G = self.B, self.K, self.gamma
-        if tuple(drafts.shape) != (B, K, G):
-            raise ValueError("drafts must be [B,K,gamma]")
-        _per_seq(temps, B, "temps")
-        _per_seq(draft_len, B, "draft_len")
-        dev = p_logits.device
-        if out is None:
-            out = {k: torch.empty(B, dtype=torch.int32, device=dev)
-                   for k in ("sel", "accept_len", "next_token")}
-            if scores:
-                out["scores"] = torch.empty((B, K), dtype=torch.float32, device=dev)
-            if lse:
-                out["lse"] = torch.empty((B, K, G + 1 if self.greedy else 2 * G + 1),
-                                         dtype=torch.float32, device=dev)
-        st = sdv_verify_from_rows(self.ctx, p_logits, q_logits, drafts, draft_len, q_stat, temperature,
-                                  temps, seed, out["sel"], out["accept_len"], out["next_token"],
-                                  out.get("scores"), out.get("lse"))
         if st != SDV_OK:
             raise SdvError(st, sdv_last_error(self.ctx))
         return out

@@ -161,9 +161,6 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const SelectArgs
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
-    // Inputs that may come from the kernel just before this one: wait for it
-    // (and for its memory) before reading any of them.
-    if (a.flags & kFlagLateInputs) asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool greedy = (a.flags & kFlagGreedy) != 0;   // no drafter rows
     const float T = a.temps ? a.temps[b] : a.temperature;
     const float c = kLog2e / T;

@@ -46,13 +46,6 @@ struct sdv_ctx {
     int32_t* hs_out;
     // fault-path test hooks (sdv_set_test_hooks)
     unsigned hooks;
-    // what the last row pass left in the partials (sdv_rowpass): 0 nothing,
-    // 1 the verifier rows, 2 the verifier and drafter rows; its temperature
-    // arguments and draft lengths
-    int rows_ready;
-    float rows_T;
-    const float* rows_temps;
-    const int32_t* rows_lens;
     // kernel timing: 4 events per recorded step
     bool prof_on;
     std::vector<cudaEvent_t> prof_ev;
@@ -63,9 +56,6 @@ struct sdv_ctx {
 static_assert(SDV_FLAG_SHARED_Q == sdv::kFlagSharedQ && SDV_FLAG_GREEDY == sdv::kFlagGreedy &&
                   SDV_FLAG_SHARED_PREFIX_ROW == sdv::kFlagSharedPrefixRow,
               "public layout flags and kernel flags must agree");
-static_assert((sdv::kFlagLateInputs & (SDV_FLAG_SHARED_Q | SDV_FLAG_GREEDY |
-                                       SDV_FLAG_SHARED_PREFIX_ROW)) == 0,
-              "the select kernel's own flag must not be a layout flag");
 static_assert(SDV_HOOK_SAMPLE_NO_COPY == sdv::kHookSampleNoCopy,
               "public test hooks and kernel hooks must agree");
 
@@ -299,25 +289,15 @@ cudaError_t enqueue_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logit
     ra.items = with_q ? ctx->items : ctx->rows_p * ctx->chunks;
     ra.lens = draft_len;
     ra.row_mode = ctx->row_mode;
-    const cudaError_t e = launch_rowpass(ra, ctx->bf16, ctx->stream, pdl);
-    if (e == cudaSuccess) {
-        ctx->rows_ready = with_q ? 2 : 1;
-        ctx->rows_T = temperature;
-        ctx->rows_temps = temperature_per_seq;
-        ctx->rows_lens = draft_len;
-    }
-    return e;
+    return launch_rowpass(ra, ctx->bf16, ctx->stream, pdl);
 }
 
-// Enqueue the selection / scan and the draw on the partials of the last row pass.
-// `late_inputs`: the drafts, lengths and temperatures may be written after the
-// row pass was enqueued, so the select kernel reads them only after its wait.
+// Enqueue the selection / scan and the draw on the partials of the row pass.
 sdv_status enqueue_finish(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
                           const int32_t* drafts, const int32_t* draft_len, const float* q_row_stat,
                           float temperature, const float* temperature_per_seq, uint64_t seed,
                           int32_t* out_sel, int32_t* out_accept_len, int32_t* out_next_token,
-                          float* out_scores, float* out_lse, cudaEvent_t* ev,
-                          bool late_inputs) {
+                          float* out_scores, float* out_lse, cudaEvent_t* ev) {
     SelectArgs sa;
     sa.p = p_logits;
     sa.q = q_logits;
@@ -330,7 +310,7 @@ sdv_status enqueue_finish(sdv_ctx* ctx, const void* p_logits, const void* q_logi
     sa.G = ctx->G;
     sa.V = ctx->V;
     sa.chunks = ctx->chunks;
-    sa.flags = ctx->flags | (late_inputs ? kFlagLateInputs : 0u);
+    sa.flags = ctx->flags;
     sa.rows_p = ctx->rows_p;
     sa.seed_lo = static_cast<uint32_t>(seed & 0xffffffffu);
     sa.seed_hi = static_cast<uint32_t>(seed >> 32);
@@ -399,7 +379,7 @@ sdv_status verify_impl(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
     if (ev) cudaEventRecord(ev[1], ctx->stream);
     return enqueue_finish(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
                           temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
-                          out_scores, out_lse, ev, false);
+                          out_scores, out_lse, ev);
 }
 
 }  // namespace
@@ -442,49 +422,6 @@ sdv_status sdv_verify(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
                       int32_t* out_accept_len, int32_t* out_next_token) {
     return sdv_verify_ex(ctx, p_logits, q_logits, drafts, temperature, nullptr, seed, out_sel,
                          out_accept_len, out_next_token, nullptr, nullptr);
-}
-
-sdv_status sdv_rowpass(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
-                       float temperature, const float* temperature_per_seq, int with_q_rows) {
-    if (!ctx) return SDV_ERR_ARG;
-    ctx->err[0] = 0;
-    const bool with_q = with_q_rows != 0 && (ctx->flags & SDV_FLAG_GREEDY) == 0;
-    const sdv_status st = check_rows(ctx, p_logits, q_logits, with_q, temperature, temperature_per_seq);
-    if (st != SDV_OK) return st;
-    const cudaError_t e = enqueue_rows(ctx, p_logits, q_logits, nullptr, with_q, temperature,
-                                       temperature_per_seq, true);
-    return e == cudaSuccess ? SDV_OK : cuda_fail(ctx, e, "row pass launch");
-}
-
-sdv_status sdv_verify_from_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
-                                const int32_t* drafts, const int32_t* draft_len,
-                                const float* q_row_stat, float temperature,
-                                const float* temperature_per_seq, uint64_t seed,
-                                int32_t* out_sel, int32_t* out_accept_len,
-                                int32_t* out_next_token, float* out_scores, float* out_lse) {
-    if (!ctx) return SDV_ERR_ARG;
-    ctx->err[0] = 0;
-    const bool greedy = (ctx->flags & SDV_FLAG_GREEDY) != 0;
-    if (ctx->rows_ready == 0)
-        return fail(ctx, SDV_ERR_ARG, "no row pass has been enqueued on this context");
-    if (!greedy && !q_row_stat && ctx->rows_ready < 2)
-        return fail(ctx, SDV_ERR_ARG,
-                    "the row pass streamed no drafter rows: pass their statistics (q_row_stat)");
-    if (temperature_per_seq != ctx->rows_temps ||
-        (!temperature_per_seq && temperature != ctx->rows_T))
-        return fail(ctx, SDV_ERR_ARG, "temperatures differ from those of the row pass");
-    if (ctx->rows_lens && draft_len != ctx->rows_lens)
-        return fail(ctx, SDV_ERR_ARG, "draft lengths differ from those of the row pass");
-    sdv_status st = check_rows(ctx, p_logits, q_logits, !greedy, temperature, temperature_per_seq);
-    if (st == SDV_OK)
-        st = check_finish(ctx, drafts, draft_len, q_row_stat, out_sel, out_accept_len,
-                          out_next_token, out_scores, out_lse);
-    if (st != SDV_OK) return st;
-    // The drafts (and lengths, temperatures) may be results of kernels enqueued
-    // after the row pass, here or on a stream joined to this one.
-    return enqueue_finish(ctx, p_logits, q_logits, drafts, draft_len, q_row_stat, temperature,
-                          temperature_per_seq, seed, out_sel, out_accept_len, out_next_token,
-                          out_scores, out_lse, nullptr, true);
 }
 
 sdv_status sdv_sync(sdv_ctx* ctx) {

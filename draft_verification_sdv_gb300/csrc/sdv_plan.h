@@ -14,13 +14,6 @@ enum : unsigned {
     kFlagSharedPrefixRow = 4u,   // the verifier row at j = 0 is (b, 0, 0) for every k
 };
 
-// Kernel-only flag of the select kernel (never a layout flag): the drafts,
-// draft lengths and per-sequence temperatures may have been written after the
-// row pass was enqueued -- by a kernel enqueued between the row pass and the
-// selection, or on another stream joined to this one -- so they are read only
-// after griddepcontrol.wait, not fetched while the kernel before it finishes.
-constexpr unsigned kFlagLateInputs = 256u;
-
 // Row index of the verifier row of (b, k, j) within the p buffer.  The row at
 // j = 0 sees only the prefix s, so with kFlagSharedPrefixRow the row of draft
 // 0 serves every draft (the others are not read).

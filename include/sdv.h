@@ -55,7 +55,6 @@
  * seed).
  *
  * CUDA graphs: sdv_verify, sdv_verify_ex, sdv_verify_len, sdv_verify_qstat,
- * sdv_rowpass, sdv_verify_from_rows,
  * sdv_cps, sdv_cps_ex, sdv_cps_prune, sdv_cps_beam and sdv_adl_step check
  * their arguments on the host and enqueue kernels; they allocate nothing,
  * copy nothing and never wait.  Each may therefore be captured into a CUDA graph, in any capture
@@ -219,48 +218,6 @@ sdv_status sdv_verify_qstat(sdv_ctx* ctx, const void* p_logits, const void* q_lo
                             const float* temperature_per_seq, uint64_t seed, int32_t* out_sel,
                             int32_t* out_accept_len, int32_t* out_next_token, float* out_scores,
                             float* out_lse);
-
-/*
- * The step in two calls, for decode loops that compute the drafts while the
- * verifier rows stream.  The row pass needs no drafts: in a DiffuSpec-style
- * step ("DiffuSpec: Unlocking Diffusion Language Models for Speculative
- * Decoding", sections 4.2-4.3) the path search over the drafter marginals and
- * the softmax statistics of the verifier rows are independent, so one stream
- * can run the path search while the context's stream runs the row pass.
- *
- * sdv_rowpass enqueues the row pass on the context's stream: the softmax
- * statistics of every verifier row, and of the drafter rows when
- * with_q_rows != 0 (ignored under SDV_FLAG_GREEDY), into the context's
- * workspace.  It reads no drafts and no draft lengths: every row is streamed
- * (SDV_FLAG_SHARED_PREFIX_ROW still skips the replaced prefix rows).
- *
- * sdv_verify_from_rows enqueues the rest of the step -- ratios, streak scores,
- * selection, scan, draw -- on the statistics the last row pass of this context
- * left (by sdv_rowpass or by any verify call), with the arguments of
- * sdv_verify_qstat (q_row_stat may be NULL when the row pass streamed the
- * drafter rows; draft_len may be NULL).  It may be called more than once on one
- * row pass (several draft sets against the same verifier rows).  The caller
- * orders it after the row pass on the context's stream and after whatever
- * produced the drafts: kernels enqueued on the context's stream between the
- * two calls, or work on another stream that the context's stream waits for
- * (cudaStreamWaitEvent).  Its first kernel reads the drafts, draft lengths and
- * temperatures only once the work before it on the stream has finished and
- * its writes are visible (unlike the single call, which fetches the drafted
- * tokens while the row pass ends).  The results equal those of
- * the single call with the same arguments, bit for bit.  SDV_ERR_ARG, with
- * nothing enqueued: no row pass yet on this context; no q_row_stat when the row
- * pass streamed no drafter rows; temperature arguments other than the row
- * pass's (the same scalar, or the same per-sequence array, unchanged); after a
- * row pass that skipped rows past draft lengths, another draft_len array.
- */
-sdv_status sdv_rowpass(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
-                       float temperature, const float* temperature_per_seq, int with_q_rows);
-sdv_status sdv_verify_from_rows(sdv_ctx* ctx, const void* p_logits, const void* q_logits,
-                                const int32_t* drafts, const int32_t* draft_len,
-                                const float* q_row_stat, float temperature,
-                                const float* temperature_per_seq, uint64_t seed,
-                                int32_t* out_sel, int32_t* out_accept_len,
-                                int32_t* out_next_token, float* out_scores, float* out_lse);
 
 /*
  * End-to-end variant for callers whose data lives in HOST memory: copies the
