@@ -9,6 +9,12 @@ namespace sdv {
 namespace {
 
 __global__ void __launch_bounds__(256) adl_kernel(const AdlArgs a) {
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream (the draw, in a decode step): wait for that grid and its memory
+    // before reading anything.  Then let the next kernel (the next step's
+    // pruning pass, which waits for this grid in turn) become resident.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= a.B) return;
     const int32_t k = a.k[b];
@@ -23,8 +29,16 @@ __global__ void __launch_bounds__(256) adl_kernel(const AdlArgs a) {
 }  // namespace
 
 cudaError_t launch_adl(const AdlArgs& a, cudaStream_t s) {
-    adl_kernel<<<(a.B + 255) / 256, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((a.B + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, adl_kernel, a);
 }
 
 }  // namespace sdv
