@@ -214,26 +214,35 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
             tot[r] = v.x;
             all_ok = all_ok && v.y != 0.0f;
         }
-        for (int r = 0; r < CL; ++r) R += tot[r];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+            if (r < CL) R += tot[r];
         // Residual mass zero on this row: every CTA sees the same R, so the
         // whole cluster takes the fallback pass to p together.
         if (pass == 0 && (t.mode == 1 || t.mode == 3) && R == 0.0f && all_ok) continue;
         const float target = t.w * R;
         {
+            // (loops over the largest cluster, skipping ranks past this one's,
+            // so that the totals stay in registers)
             float run = 0.0f;
-            for (int r = 0; r < CL; ++r) {
-                const float prev = run;
-                run += tot[r];
-                if (tot[r] > 0.0f) last_rank = r;
-                if (owner < 0 && run > target) {
-                    owner = r;
-                    target_excl = prev;
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r) {
+                if (r < CL) {
+                    const float prev = run;
+                    run += tot[r];
+                    if (tot[r] > 0.0f) last_rank = r;
+                    if (owner < 0 && run > target) {
+                        owner = r;
+                        target_excl = prev;
+                    }
                 }
             }
             if (owner < 0 && last_rank >= 0) {         // rounding put the target past the end
                 owner = last_rank;
                 float run2 = 0.0f;
-                for (int r = 0; r < last_rank; ++r) run2 += tot[r];
+#pragma unroll
+                for (int r = 0; r < kMaxCluster; ++r)
+                    if (r < last_rank) run2 += tot[r];
                 target_excl = run2;
             }
         }
